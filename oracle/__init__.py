@@ -1,0 +1,258 @@
+"""CPU oracle for H16/H32 + MXFP4 linear-layer GEMMs (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  It shares no code with the CUDA path: the arithmetic
+lives in ``mxfp4_oracle.c`` (plain C, fp64/integer), and this module only marshals
+numpy arrays through ctypes and composes the primitives the way the pages state
+the three linear-layer GEMMs.
+
+Sources (cited by page title and section):
+  "Pretraining Large Language Models with MXFP4 on Native FP4 Hardware":
+      A.1 (MXFP4 reconstruction), A.2 (tiled deterministic Hadamard),
+      C.1-C.3 (Fprop / Dgrad / Wgrad cancellation), D (1x32, 32x1, 32x32 layouts).
+  "Decomposing MXFP4 quantization error for LLM reinforcement learning":
+      E2M1 grid and E8M0 scale ("pain point"), ideal-scale quantiser and the
+      error decomposition ("core insight", property 1), QDQ equivalence
+      ("experiments").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mxfp4_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+HAD_NONE, HAD_16, HAD_32 = 1, 16, 32
+SCALE_FLOOR, SCALE_CEIL = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (IEEE arithmetic, no FMA contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+               "-fno-fast-math", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB)
+            P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            L.oracle_e2m1_code.argtypes = [ctypes.c_double]
+            L.oracle_e2m1_code.restype = I
+            L.oracle_e2m1_value.argtypes = [I]
+            L.oracle_e2m1_value.restype = ctypes.c_double
+            L.oracle_shared_exponent.argtypes = [ctypes.c_float, I]
+            L.oracle_shared_exponent.restype = I
+            L.oracle_scale_byte.argtypes = [ctypes.c_float, I]
+            L.oracle_scale_byte.restype = I
+            L.oracle_hadamard_pm1.argtypes = [I, P]
+            L.oracle_rotate_f32.argtypes = [P, I64, I, P]
+            L.oracle_rotate_f64.argtypes = [P, I64, I, P]
+            L.oracle_quantize_vec.argtypes = [P, I64, I64, I, I, P, P]
+            for name in ("oracle_quantize_row", "oracle_quantize_colT", "oracle_quantize_2d"):
+                getattr(L, name).argtypes = [P, I64, I64, I64, I, I, P, P]
+            L.oracle_dequant_row.argtypes = [P, P, I64, I64, P]
+            L.oracle_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, P]
+            L.oracle_dot_pairs.argtypes = [P, P, P, P, I64, I64, P, P]
+            L.oracle_num_threads.restype = I
+            L.oracle_set_num_threads.argtypes = [I]
+            _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (numpy uint16)")
+    return x
+
+
+# --------------------------------------------------------------------------- scalars
+def e2m1_code(u: float) -> int:
+    return lib().oracle_e2m1_code(float(u))
+
+
+def e2m1_value(code: int) -> float:
+    return lib().oracle_e2m1_value(int(code))
+
+
+def shared_exponent(amax: float, mode: int) -> int:
+    return lib().oracle_shared_exponent(float(amax), int(mode))
+
+
+def scale_byte(amax: float, mode: int) -> int:
+    return lib().oracle_scale_byte(float(amax), int(mode))
+
+
+def num_threads() -> int:
+    return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    lib().oracle_set_num_threads(int(n))
+
+
+# --------------------------------------------------------------------------- rotation
+def hadamard_pm1(n: int) -> np.ndarray:
+    h = np.zeros((n, n), dtype=np.int8)
+    lib().oracle_hadamard_pm1(n, _p(h))
+    return h
+
+
+def rotate_f32(x: np.ndarray, had: int) -> np.ndarray:
+    """Canonical fp32 rotation of the last axis (blocks of ``had``)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    flat_in, flat_out = x.reshape(-1), out.reshape(-1)
+    lib().oracle_rotate_f32(_p(flat_in), flat_in.size, had, _p(flat_out))
+    return out
+
+
+def rotate_f64(x: np.ndarray, had: int) -> np.ndarray:
+    """Exact (fp64) rotation of the last axis by block-diagonal H_n / sqrt(n)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    lib().oracle_rotate_f64(_p(x.reshape(-1)), x.size, had, _p(out.reshape(-1)))
+    return out
+
+
+# --------------------------------------------------------------------------- quantiser
+def quantize(x_bf16: np.ndarray, had: int, mode: int, layout: str):
+    """Quantise a [R, C] bf16 (uint16 bit patterns) matrix.
+
+    layout 'row'  -> codes [R, C/2],  scales [R, C/32]   (rotation along C)
+    layout 'colT' -> codes [C, R/2],  scales [C, R/32]   (rotation along R)
+    layout '2d'   -> codes [R, C/2],  scales [R/32, C/32] (rotation along C)
+    """
+    x = _u16(x_bf16)
+    R, C = x.shape
+    L = lib()
+    if layout == "row":
+        assert C % 32 == 0
+        codes = np.zeros((R, C // 2), np.uint8)
+        scales = np.zeros((R, C // 32), np.uint8)
+        L.oracle_quantize_row(_p(x), R, C, C, had, mode, _p(codes), _p(scales))
+    elif layout == "colT":
+        assert R % 32 == 0
+        codes = np.zeros((C, R // 2), np.uint8)
+        scales = np.zeros((C, R // 32), np.uint8)
+        L.oracle_quantize_colT(_p(x), R, C, C, had, mode, _p(codes), _p(scales))
+    elif layout == "2d":
+        assert R % 32 == 0 and C % 32 == 0
+        codes = np.zeros((R, C // 2), np.uint8)
+        scales = np.zeros((R // 32, C // 32), np.uint8)
+        L.oracle_quantize_2d(_p(x), R, C, C, had, mode, _p(codes), _p(scales))
+    else:
+        raise ValueError(layout)
+    return codes, scales
+
+
+def quantize_vec(x_bf16: np.ndarray, had: int, mode: int):
+    """Quantise one contiguous vector (length % 32 == 0) along itself."""
+    x = _u16(x_bf16).reshape(-1)
+    n = x.size
+    codes = np.zeros(n // 2, np.uint8)
+    scales = np.zeros(n // 32, np.uint8)
+    lib().oracle_quantize_vec(_p(x), 1, n, had, mode, _p(codes), _p(scales))
+    return codes, scales
+
+
+def unpack_codes(codes: np.ndarray) -> np.ndarray:
+    """Packed nibbles [..., n/2] -> one code per element [..., n] (element 2i low)."""
+    lo = codes & 0xF
+    hi = codes >> 4
+    return np.stack([lo, hi], axis=-1).reshape(*codes.shape[:-1], codes.shape[-1] * 2)
+
+
+def dequant_row(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales)
+    R, C = codes.shape[0], codes.shape[1] * 2
+    out = np.empty((R, C), np.float64)
+    lib().oracle_dequant_row(_p(codes), _p(scales), R, C, _p(out))
+    return out
+
+
+# --------------------------------------------------------------------------- GEMM
+def gemm(ca, sa, cb, sb):
+    """C = dq(A) dq(B)^T for row-layout operands A [M,K], B [N,K]; returns (C, S)
+    with S[m][n] = sum_k |dq a_k| |dq b_k| (both fp64)."""
+    ca, sa, cb, sb = (np.ascontiguousarray(a) for a in (ca, sa, cb, sb))
+    M, K = ca.shape[0], ca.shape[1] * 2
+    N = cb.shape[0]
+    assert cb.shape[1] * 2 == K and sa.shape == (M, K // 32) and sb.shape == (N, K // 32)
+    C = np.empty((M, N), np.float64)
+    S = np.empty((M, N), np.float64)
+    lib().oracle_gemm(_p(ca), _p(sa), _p(cb), _p(sb), M, N, K, _p(C), _p(S))
+    return C, S
+
+
+def dot_pairs(ca, sa, cb, sb):
+    """Row-wise dots of P (row of A, row of B) pairs; returns (C[P], S[P])."""
+    ca, sa, cb, sb = (np.ascontiguousarray(a) for a in (ca, sa, cb, sb))
+    P, K = ca.shape[0], ca.shape[1] * 2
+    C = np.empty(P, np.float64)
+    S = np.empty(P, np.float64)
+    lib().oracle_dot_pairs(_p(ca), _p(sa), _p(cb), _p(sb), P, K, _p(C), _p(S))
+    return C, S
+
+
+# --------------------------------------------------------------------------- linear layer
+# The three GEMMs of a linear layer with the rotation along each contraction
+# ("Pretraining ... Native FP4 Hardware", C.1-C.3).  X [M,K], W [N,K], dY [M,N].
+def fprop(x, w, had, mode):
+    """Y = X W^T: X and W each rotated and quantised along K (row layout)."""
+    return gemm(*quantize(x, had, mode, "row"), *quantize(w, had, mode, "row"))
+
+
+def dgrad(dy, w, had, mode):
+    """dX = dY W: dY along N (row layout), W^T along N (column layout of W)."""
+    return gemm(*quantize(dy, had, mode, "row"), *quantize(w, had, mode, "colT"))
+
+
+def wgrad(dy, x, had, mode):
+    """dW = dY^T X: dY^T and X^T along the tokens M (column layouts)."""
+    return gemm(*quantize(dy, had, mode, "colT"), *quantize(x, had, mode, "colT"))
+
+
+def fprop_sample(x, w, had, mode, rows, cols):
+    """Y[m][n] for the listed (m, n) pairs, quantising only the rows involved."""
+    qa = [quantize_vec(x[m], had, mode) for m in rows]
+    qb = [quantize_vec(w[n], had, mode) for n in cols]
+    return dot_pairs(np.stack([q[0] for q in qa]), np.stack([q[1] for q in qa]),
+                     np.stack([q[0] for q in qb]), np.stack([q[1] for q in qb]))
+
+
+def dgrad_sample(dy, w, had, mode, rows, cols):
+    """dX[m][k] for the listed (m, k) pairs: row m of dY, column k of W."""
+    qa = [quantize_vec(dy[m], had, mode) for m in rows]
+    qb = [quantize_vec(np.ascontiguousarray(w[:, k]), had, mode) for k in cols]
+    return dot_pairs(np.stack([q[0] for q in qa]), np.stack([q[1] for q in qa]),
+                     np.stack([q[0] for q in qb]), np.stack([q[1] for q in qb]))
+
+
+def wgrad_sample(dy, x, had, mode, rows, cols):
+    """dW[n][k] for the listed (n, k) pairs: column n of dY, column k of X."""
+    qa = [quantize_vec(np.ascontiguousarray(dy[:, n]), had, mode) for n in rows]
+    qb = [quantize_vec(np.ascontiguousarray(x[:, k]), had, mode) for k in cols]
+    return dot_pairs(np.stack([q[0] for q in qa]), np.stack([q[1] for q in qa]),
+                     np.stack([q[0] for q in qb]), np.stack([q[1] for q in qb]))

@@ -1,0 +1,356 @@
+/*
+ * mxfp4_oracle.c -- plain, slow CPU oracle for H16/H32 + MXFP4 linear-layer GEMMs.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code, header,
+ * table or constant with the CUDA path and must never be used as a fallback for it.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [MXFP4-HW]  "Pretraining Large Language Models with MXFP4 on Native FP4 Hardware"
+ *               (arXiv:2605.09825): summary ("how it is done"), A.1 "MXFP4 and
+ *               micro-scaling", A.2 "Hadamard transform architecture",
+ *               C "mathematical cancellation" (C.1 Fprop, C.2 Dgrad, C.3 Wgrad),
+ *               D "1D and 2D quantisation strategies".
+ *   [DECOMP]    "Decomposing MXFP4 quantization error for LLM reinforcement learning":
+ *               "pain point" (E8M0 scale, E2M1 grid), "core insight" (ideal-scale
+ *               quantiser), "experiments" (QDQ numerically equal to native MXFP4:
+ *               same grid, same E8M0 block scale, FP32 accumulation).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - shared exponent: OCP MX rule e = floor(log2 amax) - 2 (default) or the
+ *     ceiling rule "smallest e with 6 * 2^e >= amax" (mode 1), clamped to the
+ *     E8M0 range [-127, 127]; amax == 0 gives e = -127;
+ *   - Q_FP4 = nearest E2M1 grid value, ties to the code with an even mantissa bit,
+ *     magnitudes beyond 6 saturate to 6, the sign of zero is kept;
+ *   - the rotation is evaluated in fp32 by the Sylvester recursion
+ *     H_2n [a; b] = [H_n a + H_n b ; H_n a - H_n b] (every add rounded to fp32),
+ *     followed by one fp32 multiply by 1/sqrt(n); the quantiser consumes fp32;
+ *   - Hadamard blocks are contiguous along the rotated dimension, starting at 0.
+ *
+ * Everything here is written as loops over the definitions; OpenMP only splits
+ * independent rows across threads (no reordering inside a computation).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------- */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------- */
+
+/* bf16 is the upper 16 bits of an IEEE binary32. */
+static float bf16_to_float(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+/* E2M1 magnitudes indexed by the 3-bit code (exponent bits, mantissa bit):
+ * [DECOMP] "pain point": grid {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6}. */
+static const double E2M1_MAG[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* Q_FP4 ([MXFP4-HW] A.1): nearest grid value by exhaustive distance search.
+ * Ties go to the code whose mantissa bit (lowest code bit) is 0.  Returns the
+ * 4-bit code: sign in bit 3, magnitude index in bits 0..2. */
+int oracle_e2m1_code(double u) {
+    int sign = signbit(u) ? 1 : 0;
+    double a = fabs(u);
+    /* saturation: every magnitude beyond the largest grid value maps to it (this also
+     * keeps huge |u| away from the distance search, where a - 6 would round to a) */
+    if (a >= E2M1_MAG[7]) return (sign << 3) | 7;
+    int best = 0;
+    double best_d = fabs(a - E2M1_MAG[0]);
+    for (int c = 1; c < 8; ++c) {
+        double d = fabs(a - E2M1_MAG[c]);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (sign << 3) | best;
+}
+
+double oracle_e2m1_value(int code) {
+    double m = E2M1_MAG[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+/* Shared block exponent e (E8M0 stores e + 127).
+ * mode 0 (OCP floor): e = floor(log2 amax) - 2, i.e. the largest e with
+ *                     2^(e+2) <= amax ([MXFP4-HW] A.1, OCP MX convention).
+ * mode 1 (ceiling):   smallest e with 6 * 2^e >= amax, so that the E8M0 scale is
+ *                     never below the ideal scale amax / 6 ([DECOMP] "core insight").
+ * Both clamped to [-127, 127]; amax == 0 gives -127. */
+int oracle_shared_exponent(float amax_f, int mode) {
+    double amax = (double)amax_f;
+    if (!(amax > 0.0)) return -127;
+    int ex;
+    frexp(amax, &ex);              /* amax = f * 2^ex, f in [0.5, 1) */
+    int flog2 = ex - 1;            /* floor(log2 amax), exact */
+    int e;
+    if (mode == 0) {
+        e = flog2 - 2;
+    } else {
+        e = flog2 - 3;
+        while (ldexp(6.0, e) < amax) e += 1;
+        while (ldexp(6.0, e - 1) >= amax) e -= 1;
+    }
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+int oracle_scale_byte(float amax, int mode) { return oracle_shared_exponent(amax, mode) + 127; }
+
+/* ------------------------------------------------------------------------- */
+/* Hadamard rotation                                                          */
+/* ------------------------------------------------------------------------- */
+
+/* Sylvester construction H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]] written out
+ * as an explicit +-1 matrix, row-major n x n ([MXFP4-HW] A.2). */
+void oracle_hadamard_pm1(int n, int8_t* h) {
+    h[0] = 1;
+    for (int m = 1; m < n; m *= 2) {
+        for (int i = 0; i < m; ++i)
+            for (int j = 0; j < m; ++j) {
+                int8_t v = h[i * n + j];
+                h[i * n + (j + m)] = v;
+                h[(i + m) * n + j] = v;
+                h[(i + m) * n + (j + m)] = (int8_t)-v;
+            }
+    }
+}
+
+/* fp32 constant 1/sqrt(n) that normalises H_n so that H H^T = I. */
+static float norm_const(int n) {
+    if (n == 1) return 1.0f;
+    return (float)(1.0 / sqrt((double)n));
+}
+
+/* H_n x by the Sylvester recursion, every add/sub rounded to fp32. */
+static void sylvester_apply_f32(float* v, int n) {
+    if (n == 1) return;
+    int h = n / 2;
+    sylvester_apply_f32(v, h);
+    sylvester_apply_f32(v + h, h);
+    for (int i = 0; i < h; ++i) {
+        float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+    }
+}
+
+/* Canonical fp32 rotation of a contiguous vector of length len (len % n == 0):
+ * each block of n is replaced by fl32(fl32(H_n x) * fl32(1/sqrt(n))). n = 1 is
+ * the identity ("none"). */
+void oracle_rotate_f32(const float* x, int64_t len, int n, float* out) {
+    float c = norm_const(n);
+    for (int64_t b = 0; b < len; b += n) {
+        float blk[64];
+        for (int i = 0; i < n; ++i) blk[i] = x[b + i];
+        sylvester_apply_f32(blk, n);
+        for (int i = 0; i < n; ++i) out[b + i] = blk[i] * c;
+    }
+}
+
+/* Exact rotation in fp64 by explicit matrix-vector products with the +-1 matrix
+ * divided by sqrt(n): used for the cancellation identities and diagnostics. */
+void oracle_rotate_f64(const double* x, int64_t len, int n, double* out) {
+    int8_t h[32 * 32];
+    oracle_hadamard_pm1(n, h);
+    double c = 1.0 / sqrt((double)n);
+    for (int64_t b = 0; b < len; b += n)
+        for (int i = 0; i < n; ++i) {
+            double s = 0.0;
+            for (int j = 0; j < n; ++j) s += (double)h[i * n + j] * x[b + j];
+            out[b + i] = s * c;
+        }
+}
+
+/* ------------------------------------------------------------------------- */
+/* MXFP4 quantisation of 32-element blocks                                    */
+/* ------------------------------------------------------------------------- */
+
+/* Quantise one 32-element block of already-rotated fp32 values with exponent e:
+ * code_i = Q_FP4(v_i / 2^e) ([MXFP4-HW] A.1 reconstruction formula). */
+static void quantize_block(const float* v, int e, uint8_t* codes /*32 nibble codes, one per byte*/) {
+    for (int i = 0; i < 32; ++i) {
+        double u = ldexp((double)v[i], -e);
+        codes[i] = (uint8_t)oracle_e2m1_code(u);
+    }
+}
+
+static float block_amax(const float* v, int n) {
+    float m = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > m) m = a;
+    }
+    return m;
+}
+
+/* Store nibble code c for element index i of a packed row (2 per byte, element
+ * 2j in the low nibble of byte j). */
+static void put_nibble(uint8_t* row, int64_t i, uint8_t c) {
+    uint8_t* b = row + i / 2;
+    if (i % 2 == 0) *b = (uint8_t)((*b & 0xF0) | (c & 0xF));
+    else *b = (uint8_t)((*b & 0x0F) | ((c & 0xF) << 4));
+}
+
+/* Quantise a contiguous vector of len bf16 values (len % 32 == 0) along itself:
+ * rotate by H_n blocks, then one E8M0 scale per 32 elements.
+ * codes: len/2 bytes; scales: len/32 bytes. */
+void oracle_quantize_vec(const uint16_t* x, int64_t stride, int64_t len, int had, int mode,
+                         uint8_t* codes, uint8_t* scales) {
+    float* xf = (float*)malloc(sizeof(float) * (size_t)len);
+    float* v = (float*)malloc(sizeof(float) * (size_t)len);
+    for (int64_t i = 0; i < len; ++i) xf[i] = bf16_to_float(x[i * stride]);
+    oracle_rotate_f32(xf, len, had, v);
+    for (int64_t b = 0; b < len / 32; ++b) {
+        const float* blk = v + b * 32;
+        int e = oracle_shared_exponent(block_amax(blk, 32), mode);
+        uint8_t q[32];
+        quantize_block(blk, e, q);
+        for (int i = 0; i < 32; ++i) put_nibble(codes, b * 32 + i, q[i]);
+        scales[b] = (uint8_t)(e + 127);
+    }
+    free(xf);
+    free(v);
+}
+
+/* 1x32 row-wise layout ([MXFP4-HW] D): x is [R, C] (leading dim ld elements);
+ * each row is rotated and quantised along C.  codes [R, C/2], scales [R, C/32]. */
+void oracle_quantize_row(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                         uint8_t* codes, uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r)
+        oracle_quantize_vec(x + r * ld, 1, C, had, mode, codes + r * (C / 2), scales + r * (C / 32));
+}
+
+/* 32x1 column-wise layout, stored transposed ([MXFP4-HW] D): output row c is
+ * column c of x, rotated and quantised along R.  codes [C, R/2], scales [C, R/32]. */
+void oracle_quantize_colT(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                          uint8_t* codes, uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < C; ++c)
+        oracle_quantize_vec(x + c, ld, R, had, mode, codes + c * (R / 2), scales + c * (R / 32));
+}
+
+/* 32x32 2D layout ([MXFP4-HW] D): rotation along C, one E8M0 scale per 32x32
+ * tile taken from the amax of the tile's rotated values.
+ * codes [R, C/2], scales [R/32, C/32]. */
+void oracle_quantize_2d(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                        uint8_t* codes, uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+    for (int64_t tr = 0; tr < R / 32; ++tr) {
+        float* xf = (float*)malloc(sizeof(float) * (size_t)C);
+        float* v = (float*)malloc(sizeof(float) * 32 * (size_t)C);
+        for (int i = 0; i < 32; ++i) {
+            for (int64_t c = 0; c < C; ++c) xf[c] = bf16_to_float(x[(tr * 32 + i) * ld + c]);
+            oracle_rotate_f32(xf, C, had, v + (int64_t)i * C);
+        }
+        for (int64_t tc = 0; tc < C / 32; ++tc) {
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float a = block_amax(v + (int64_t)i * C + tc * 32, 32);
+                if (a > amax) amax = a;
+            }
+            int e = oracle_shared_exponent(amax, mode);
+            scales[tr * (C / 32) + tc] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; ++i) {
+                uint8_t q[32];
+                quantize_block(v + (int64_t)i * C + tc * 32, e, q);
+                uint8_t* row = codes + (tr * 32 + i) * (C / 2);
+                for (int j = 0; j < 32; ++j) put_nibble(row, tc * 32 + j, q[j]);
+            }
+        }
+        free(xf);
+        free(v);
+    }
+}
+
+/* Dequantise a row-layout tensor: out[r][k] = 2^e(r, k/32) * value(code). */
+void oracle_dequant_row(const uint8_t* codes, const uint8_t* scales, int64_t R, int64_t C, double* out) {
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t k = 0; k < C; ++k) {
+            uint8_t b = codes[r * (C / 2) + k / 2];
+            int c = (k % 2 == 0) ? (b & 0xF) : (b >> 4);
+            int e = (int)scales[r * (C / 32) + k / 32] - 127;
+            out[r * C + k] = ldexp(oracle_e2m1_value(c), e);
+        }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Block-scaled GEMM (QDQ semantics, [DECOMP] "experiments")                 */
+/* ------------------------------------------------------------------------- */
+
+static int twice_value(const uint8_t* row, int64_t k) {
+    /* 2 * E2M1 value is an integer in [-12, 12]. */
+    static const int TW[8] = {0, 1, 2, 3, 4, 6, 8, 12};
+    uint8_t b = row[k / 2];
+    int c = (k % 2 == 0) ? (b & 0xF) : (b >> 4);
+    int m = TW[c & 7];
+    return (c & 8) ? -m : m;
+}
+
+/* One output element: sum over 32-blocks of 2^(ea+eb) * sum_k qa_k * qb_k.  The
+ * inner sum is an exact integer; block terms are summed in fp64 in k order.
+ * Also returns s = sum_k |dq a_k| |dq b_k| (fp64) for the tolerance. */
+static void dot_one(const uint8_t* ca, const uint8_t* sa, const uint8_t* cb, const uint8_t* sb, int64_t K,
+                    double* c_out, double* s_out) {
+    double acc = 0.0, sacc = 0.0;
+    for (int64_t blk = 0; blk < K / 32; ++blk) {
+        long isum = 0, iabs = 0;
+        for (int64_t k = blk * 32; k < blk * 32 + 32; ++k) {
+            int a = twice_value(ca, k), b = twice_value(cb, k);
+            isum += (long)a * b;
+            iabs += (long)abs(a) * abs(b);
+        }
+        int e = ((int)sa[blk] - 127) + ((int)sb[blk] - 127);
+        acc += ldexp((double)isum / 4.0, e);
+        sacc += ldexp((double)iabs / 4.0, e);
+    }
+    *c_out = acc;
+    if (s_out) *s_out = sacc;
+}
+
+/* C[m][n] = sum_k dq(A)[m][k] * dq(B)[n][k] for A [M,K], B [N,K] in row layout with
+ * plain scales (codes [rows, K/2], scales [rows, K/32]). */
+void oracle_gemm(const uint8_t* ca, const uint8_t* sa, const uint8_t* cb, const uint8_t* sb, int64_t M,
+                 int64_t N, int64_t K, double* C, double* S) {
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            dot_one(ca + m * (K / 2), sa + m * (K / 32), cb + n * (K / 2), sb + n * (K / 32), K, &C[m * N + n],
+                    S ? &S[m * N + n] : 0);
+}
+
+/* The same for a list of (row of A, row of B) pairs taken from separately
+ * quantised single rows: a_rows [P, K/2] codes + [P, K/32] scales, likewise b. */
+void oracle_dot_pairs(const uint8_t* ca, const uint8_t* sa, const uint8_t* cb, const uint8_t* sb, int64_t P,
+                      int64_t K, double* C, double* S) {
+#pragma omp parallel for schedule(static)
+    for (int64_t p = 0; p < P; ++p)
+        dot_one(ca + p * (K / 2), sa + p * (K / 32), cb + p * (K / 2), sb + p * (K / 32), K, &C[p], S ? &S[p] : 0);
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
