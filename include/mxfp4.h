@@ -1,0 +1,200 @@
+/*
+ * mxfp4.h -- C ABI of the GB300 (sm_103a) H16/H32 + MXFP4 linear-layer GEMM library
+ * (libmxfp4.so).
+ *
+ * What it computes (cited by web-page title and section):
+ *   "Pretraining Large Language Models with MXFP4 on Native FP4 Hardware"
+ *     - A.1 "MXFP4 and micro-scaling": a block of 32 values shares one power-of-two
+ *       scale 2^E and each element is rounded to the nearest FP4 (E2M1) value:
+ *       x_B ~ 2^E * Q_FP4(x_B / 2^E).
+ *     - A.2 "Hadamard transform architecture": a deterministic, tiled (block-
+ *       diagonal) 16x16 Hadamard rotation is applied before every MXFP4 GEMM.
+ *     - C.1-C.3: the rotation is applied along each GEMM's contraction dimension, so
+ *       it cancels: Y = (XH)(WH)^T = XW^T, dX = (dY H)(W^T H)^T = dY W,
+ *       dW = (dY^T H)(X^T H)^T = dY^T X.
+ *     - D "1D and 2D quantisation strategies": 1x32 row-wise, 32x1 column-wise
+ *       (needs a transpose) and 32x32 2D block scales.
+ *   "Decomposing MXFP4 quantization error for LLM reinforcement learning"
+ *     - E8M0 scales (powers of two only) and the E2M1 grid
+ *       {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6}; the ceiling scale (never below
+ *       amax/6); W4A4 QDQ numerics = same grid, same E8M0 scale, FP32 accumulation.
+ *
+ * Conventions shared by every entry point
+ *   - Ownership: the caller owns every buffer (inputs, quantised tensors, outputs,
+ *     workspace).  The library allocates no memory; its only global state is one
+ *     device status word per device (see mxfp4_device_status).
+ *   - Asynchrony: every compute call validates its arguments on the host, then
+ *     enqueues kernels on `stream` and returns without synchronising.  Pointers
+ *     marked "device" must be device-accessible memory of the current device.
+ *   - Validation: invalid arguments return an error status WITHOUT launching
+ *     anything.  A thread-local message describing the last error is available
+ *     from mxfp4_last_error().
+ *   - Numbers: inputs are finite bf16 with |x| < 2^123.  Non-finite inputs give
+ *     unspecified codes but never a fault or hang.
+ *   - Packed FP4: element 2j in the low nibble of byte j, element 2j+1 in the high
+ *     nibble; code bit 3 = sign, bits 0-2 index {0, .5, 1, 1.5, 2, 3, 4, 6}.
+ *   - E8M0: byte b means 2^(b-127); this library produces 0 <= b <= 253.
+ */
+#ifndef MXFP4_H
+#define MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* mxfp4_stream_t;
+
+typedef enum {
+    MXFP4_OK = 0,
+    MXFP4_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, negative size          */
+    MXFP4_ERR_UNSUPPORTED_SHAPE = 2, /* a quantised dim not a multiple of 32, ...     */
+    MXFP4_ERR_MISALIGNED = 3,        /* pointer not 16-byte aligned, ld % 8 != 0      */
+    MXFP4_ERR_WORKSPACE = 4,         /* workspace null or smaller than required        */
+    MXFP4_ERR_CUDA = 5,              /* a CUDA runtime/driver call or launch failed    */
+    MXFP4_ERR_TIMEOUT = 6,           /* a bounded device-side wait expired             */
+    MXFP4_ERR_UNSUPPORTED_DEVICE = 7 /* the current device is not sm_103 (GB300)       */
+} mxfp4_status;
+
+typedef enum { MXFP4_HAD_NONE = 0, MXFP4_HAD_16 = 16, MXFP4_HAD_32 = 32 } mxfp4_hadamard;
+
+/* FLOOR_OCP: e = floor(log2 amax) - 2 (OCP MX rule).  CEIL: smallest e with
+ * 6 * 2^e >= amax.  Both clamped to the E8M0 range; amax == 0 gives e = -127. */
+typedef enum { MXFP4_SCALE_FLOOR_OCP = 0, MXFP4_SCALE_CEIL = 1 } mxfp4_scale_mode;
+
+/* Layout bitmask for mxfp4_rotate_quantize. */
+enum { MXFP4_LAYOUT_ROW = 1, MXFP4_LAYOUT_COLT = 2, MXFP4_LAYOUT_2D = 4 };
+
+typedef enum { MXFP4_OUT_F32 = 0, MXFP4_OUT_BF16 = 1 } mxfp4_out_dtype;
+
+/* Scale-factor storage.
+ *   PLAIN: row-major [rows][cols/32] bytes (2D layout: [rows/32][cols/32]).
+ *   MMA:   the tile order the tensor cores read.  rows are padded to a multiple of
+ *          128 and the 32-element blocks per row (kb = cols/32) to a multiple of 8;
+ *          padding bytes are written as 0.  The byte for (row r, block k) is at
+ *            ((r/128) * (kb_pad/4) + k/4) * 512 + (r%32) * 16 + ((r/32)%4) * 4 + k%4.
+ *          Only MMA-layout tensors can feed mxfp4_gemm. */
+typedef enum { MXFP4_SF_PLAIN = 0, MXFP4_SF_MMA = 1 } mxfp4_sf_layout;
+
+/* A quantised matrix of `rows` x `cols` logical elements, quantised in blocks of 32
+ * along `cols` (the contraction dimension of the GEMM that consumes it).  For the
+ * column-transposed copy of an [R, C] input the stored matrix is [C, R].
+ *   codes:  device, rows * cols / 2 bytes, row-major (row pitch cols/2 bytes),
+ *           16-byte aligned.
+ *   scales: device, mxfp4_scales_bytes(rows, cols, layout, sf_layout) bytes,
+ *           16-byte aligned.
+ * mxfp4_rotate_quantize fills rows, cols, layout, had and mode; the caller sets
+ * codes, scales and sf_layout. */
+typedef struct {
+    void* codes;
+    uint8_t* scales;
+    int64_t rows;
+    int64_t cols;
+    int32_t layout;    /* one MXFP4_LAYOUT_* value */
+    int32_t sf_layout; /* mxfp4_sf_layout */
+    int32_t had;       /* mxfp4_hadamard used when it was produced */
+    int32_t mode;      /* mxfp4_scale_mode used when it was produced */
+} mxfp4_tensor;
+
+typedef struct {
+    int32_t had;        /* mxfp4_hadamard */
+    int32_t mode;       /* mxfp4_scale_mode */
+    int32_t out_dtype;  /* mxfp4_out_dtype of the GEMM output */
+    int32_t accumulate; /* 1: C += result (fp32 output only); 0: C = result */
+} mxfp4_config;
+
+enum { MXFP4_OP_FPROP = 0, MXFP4_OP_DGRAD = 1, MXFP4_OP_WGRAD = 2 };
+
+/* Bytes of packed codes for a rows x cols quantised matrix. */
+size_t mxfp4_codes_bytes(int64_t rows, int64_t cols);
+/* Bytes of scale factors for a rows x cols quantised matrix in the given layout
+ * (MXFP4_LAYOUT_*) and scale-factor storage (mxfp4_sf_layout); 0 if invalid. */
+size_t mxfp4_scales_bytes(int64_t rows, int64_t cols, int layout, int sf_layout);
+/* codes bytes rounded up to 256 plus scales bytes rounded up to 256: the size of
+ * one quantised tensor when both live in one buffer (codes first). */
+size_t mxfp4_quantized_bytes(int64_t rows, int64_t cols, int layout, int sf_layout);
+
+/* Fused rotate + quantise ("Pretraining ... Native FP4 Hardware", A.1, A.2, D).
+ * x: device bf16 [rows, cols], leading dimension ld >= cols elements (ld % 8 == 0,
+ *    x 16-byte aligned).  Read once.
+ * had, mode: rotation (applied along the quantised dimension of each output, in
+ *    contiguous blocks starting at index 0) and scale rule.
+ * layouts: bitmask of MXFP4_LAYOUT_*; ROW and COLT may be combined (one pass emits
+ *    both), 2D is produced on its own.
+ *    ROW:  row_out  = [rows, cols], rotated/quantised along cols (needs cols % 32 == 0)
+ *    COLT: colT_out = [cols, rows], column j of x rotated/quantised along rows
+ *          (needs rows % 32 == 0 and cols % 32 == 0)
+ *    2D:   twoD_out = [rows, cols], rotated along cols, one scale per 32x32 tile
+ *          (needs rows % 32 == 0, cols % 32 == 0; PLAIN scales only)
+ * Outputs not requested may be NULL.
+ * The rotation is evaluated in fp32 in the Sylvester order (stage strides 1, 2, 4,
+ * 8 (, 16), every add rounded) and multiplied by fl32(1/sqrt(n)); rounding to E2M1
+ * is to nearest, ties to even, saturating at +-6, sign of zero kept. */
+mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                   unsigned layouts, mxfp4_tensor* row_out, mxfp4_tensor* colT_out,
+                                   mxfp4_tensor* twoD_out, mxfp4_stream_t stream);
+
+/* Block-scaled MXFP4 GEMM C = A . B^T with FP32 accumulation on the tcgen05 tensor
+ * cores (QDQ numerics: "Decomposing MXFP4 quantization error", experiments).
+ * A: [M, K] quantised along K, B: [N, K] quantised along K, both MXFP4_SF_MMA,
+ *    same K (cols).
+ * C: device, [M, N] row-major with leading dimension ldc >= N (ldc % 8 == 0,
+ *    16-byte aligned), fp32 or bf16 per out_dtype.  accumulate = 1 adds to C
+ *    (fp32 only).
+ * ws/ws_bytes: unused by this kernel (pass NULL/0); reserved for split-K. */
+mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, int64_t ldc, int out_dtype,
+                        int accumulate, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
+
+/* Workspace bytes needed by mxfp4_linear_{fprop,dgrad,wgrad} (op = MXFP4_OP_*). */
+size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp4_config* cfg);
+
+/* Fprop Y = X W^T ("Pretraining ... Native FP4 Hardware", C.1).
+ * x: device bf16 [M, K] (ld K), w: device bf16 [N, K] (ld K), y: device [M, N] (ld N)
+ * in cfg->out_dtype.  Both operands are rotated and quantised along K (row layout)
+ * into the workspace (256-byte aligned, mxfp4_workspace_bytes bytes), then multiplied.
+ * save_xT (optional, NULL to skip): receives X^T quantised along M, [K, M], the Wgrad
+ *    operand (needs M % 32 == 0); produced in the same pass that reads X.
+ * save_wT (optional): receives W^T quantised along N, [K, N], the Dgrad operand
+ *    (needs N % 32 == 0); produced in the same pass that reads W.
+ * Saved tensors must be MXFP4_SF_MMA.  K % 32 == 0. */
+mxfp4_status mxfp4_linear_fprop(const void* x, const void* w, int64_t M, int64_t N, int64_t K,
+                                const mxfp4_config* cfg, void* y, mxfp4_tensor* save_xT, mxfp4_tensor* save_wT,
+                                void* ws, size_t ws_bytes, mxfp4_stream_t stream);
+
+/* Dgrad dX = dY W ("Pretraining ... Native FP4 Hardware", C.2).
+ * dy: device bf16 [M, N] (ld N); wT: W^T quantised along N ([K, N], from
+ * mxfp4_linear_fprop's save_wT); dx: device [M, K] (ld K).  dY is rotated and
+ * quantised along N (row layout) into the workspace.
+ * save_dyT (optional): receives dY^T quantised along M, [N, M], the Wgrad operand
+ *    (needs M % 32 == 0).  N % 32 == 0. */
+mxfp4_status mxfp4_linear_dgrad(const void* dy, const mxfp4_tensor* wT, int64_t M, int64_t N, int64_t K,
+                                const mxfp4_config* cfg, void* dx, mxfp4_tensor* save_dyT, void* ws,
+                                size_t ws_bytes, mxfp4_stream_t stream);
+
+/* Wgrad dW = dY^T X ("Pretraining ... Native FP4 Hardware", C.3), contraction over
+ * the M tokens.  dyT: [N, M], xT: [K, M] (both quantised along M, MMA scales);
+ * dw: device [N, K] (ld K) in cfg->out_dtype; cfg->accumulate adds to dw. */
+mxfp4_status mxfp4_linear_wgrad(const mxfp4_tensor* dyT, const mxfp4_tensor* xT, const mxfp4_config* cfg,
+                                void* dw, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the current device's status word:
+ * MXFP4_OK, or MXFP4_ERR_TIMEOUT if a kernel's bounded wait expired since the last
+ * call (that kernel returned early and its output is invalid). */
+mxfp4_status mxfp4_device_status(mxfp4_stream_t stream);
+
+/* Bounded-wait limit in nanoseconds for kernels launched afterwards by this host
+ * thread (default 2e9 = 2 s; 0 restores the default). */
+void mxfp4_set_wait_limit_ns(uint64_t ns);
+
+const char* mxfp4_status_string(mxfp4_status status);
+/* Message for the last error returned on this host thread ("" if none). */
+const char* mxfp4_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_H */

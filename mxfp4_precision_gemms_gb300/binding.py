@@ -1,0 +1,335 @@
+"""ctypes binding of libmxfp4.so (include/mxfp4.h).
+
+Argument marshalling only: every step of the path (rotation, scale, quantisation,
+GEMM) runs in the library's CUDA kernels.  torch supplies device memory, streams
+and events.  If the library is missing, every call raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmxfp4.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "mxfp4.h")
+
+HAD_NONE, HAD_16, HAD_32 = 0, 16, 32
+SCALE_FLOOR, SCALE_CEIL = 0, 1
+LAYOUT_ROW, LAYOUT_COLT, LAYOUT_2D = 1, 2, 4
+OUT_F32, OUT_BF16 = 0, 1
+SF_PLAIN, SF_MMA = 0, 1
+OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
+
+STATUS = {0: "MXFP4_OK", 1: "MXFP4_ERR_INVALID_ARG", 2: "MXFP4_ERR_UNSUPPORTED_SHAPE", 3: "MXFP4_ERR_MISALIGNED",
+          4: "MXFP4_ERR_WORKSPACE", 5: "MXFP4_ERR_CUDA", 6: "MXFP4_ERR_TIMEOUT", 7: "MXFP4_ERR_UNSUPPORTED_DEVICE"}
+
+
+class MxTensorC(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("layout", ctypes.c_int32), ("sf_layout", ctypes.c_int32),
+                ("had", ctypes.c_int32), ("mode", ctypes.c_int32)]
+
+
+class MxConfigC(ctypes.Structure):
+    _fields_ = [("had", ctypes.c_int32), ("mode", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("accumulate", ctypes.c_int32)]
+
+
+class Mxfp4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """Loads libmxfp4.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                                   "g.build()'` (there is no CPU fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I64, I, U, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+            T = ctypes.POINTER(MxTensorC)
+            CF = ctypes.POINTER(MxConfigC)
+            sig = {
+                "mxfp4_codes_bytes": ([I64, I64], S),
+                "mxfp4_scales_bytes": ([I64, I64, I, I], S),
+                "mxfp4_quantized_bytes": ([I64, I64, I, I], S),
+                "mxfp4_rotate_quantize": ([P, I64, I64, I64, I, I, U, T, T, T, P], I),
+                "mxfp4_gemm": ([T, T, P, I64, I, I, P, S, P], I),
+                "mxfp4_workspace_bytes": ([I, I64, I64, I64, CF], S),
+                "mxfp4_linear_fprop": ([P, P, I64, I64, I64, CF, P, T, T, P, S, P], I),
+                "mxfp4_linear_dgrad": ([P, T, I64, I64, I64, CF, P, T, P, S, P], I),
+                "mxfp4_linear_wgrad": ([T, T, CF, P, P, S, P], I),
+                "mxfp4_device_status": ([P], I),
+                "mxfp4_set_wait_limit_ns": ([ctypes.c_uint64], None),
+                "mxfp4_status_string": ([I], ctypes.c_char_p),
+                "mxfp4_last_error": ([], ctypes.c_char_p),
+            }
+            for name, (args, res) in sig.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = L
+    return _lib
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/mxfp4.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(mxfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status: int):
+    if status != 0:
+        raise Mxfp4Error(status, lib().mxfp4_last_error().decode())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ----------------------------------------------------------------- quantised tensors
+@dataclass
+class QTensor:
+    """A quantised matrix [rows, cols] (blocks of 32 along cols) held in torch memory."""
+    codes: torch.Tensor   # uint8 [rows, cols/2]
+    scales: torch.Tensor  # uint8: plain [rows, cols/32] / [rows/32, cols/32], or flat MMA order
+    rows: int
+    cols: int
+    layout: int
+    sf_layout: int
+    had: int = 0
+    mode: int = 0
+
+    def c(self) -> MxTensorC:
+        return MxTensorC(self.codes.data_ptr(), self.scales.data_ptr(), self.rows, self.cols, self.layout,
+                         self.sf_layout, self.had, self.mode)
+
+    def plain_scales(self) -> np.ndarray:
+        s = self.scales.cpu().numpy()
+        if self.sf_layout == SF_PLAIN:
+            return s
+        return sf_mma_to_plain(s, self.rows, self.cols)
+
+    @property
+    def nbytes(self) -> int:
+        return self.codes.numel() + self.scales.numel()
+
+
+def codes_bytes(rows: int, cols: int) -> int:
+    return lib().mxfp4_codes_bytes(rows, cols)
+
+
+def scales_bytes(rows: int, cols: int, layout: int, sf_layout: int) -> int:
+    return lib().mxfp4_scales_bytes(rows, cols, layout, sf_layout)
+
+
+def empty_qtensor(rows: int, cols: int, layout: int, sf_layout: int, device="cuda") -> QTensor:
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+    if layout == LAYOUT_2D:
+        scales = torch.empty((rows // 32, cols // 32), dtype=torch.uint8, device=device)
+    elif sf_layout == SF_PLAIN:
+        scales = torch.empty((rows, cols // 32), dtype=torch.uint8, device=device)
+    else:
+        scales = torch.empty(scales_bytes(rows, cols, layout, sf_layout), dtype=torch.uint8, device=device)
+    return QTensor(codes, scales, rows, cols, layout, sf_layout)
+
+
+# ----------------------------------------------------------------- MMA scale order (host marshalling)
+def _mma_index(rows: int, cols: int) -> np.ndarray:
+    kb = cols // 32
+    kb_pad = ((kb + 7) // 8) * 8
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    k = np.arange(kb, dtype=np.int64)[None, :]
+    return ((r // 128) * (kb_pad // 4) + k // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (k % 4)
+
+
+def sf_mma_bytes(rows: int, cols: int) -> int:
+    return ((rows + 127) // 128) * 128 * (((cols // 32 + 7) // 8) * 8)
+
+
+def sf_mma_to_plain(buf: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    return np.asarray(buf).reshape(-1)[_mma_index(rows, cols)]
+
+
+def sf_plain_to_mma(plain: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    out = np.zeros(sf_mma_bytes(rows, cols), np.uint8)
+    out[_mma_index(rows, cols)] = plain
+    return out
+
+
+def qtensor_from_host(codes: np.ndarray, plain_scales: np.ndarray, layout: int = LAYOUT_ROW,
+                      device="cuda") -> QTensor:
+    """Uploads host codes [rows, cols/2] and plain scales [rows, cols/32] as an MMA-order QTensor."""
+    rows, cols = codes.shape[0], codes.shape[1] * 2
+    c = torch.from_numpy(np.ascontiguousarray(codes)).to(device)
+    s = torch.from_numpy(sf_plain_to_mma(plain_scales, rows, cols)).to(device)
+    return QTensor(c, s, rows, cols, layout, SF_MMA)
+
+
+# ----------------------------------------------------------------- entry points
+def rotate_quantize(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR, layouts: int = LAYOUT_ROW,
+                    sf_layout: int = SF_MMA, outs: dict | None = None, stream=None) -> dict:
+    """mxfp4_rotate_quantize on a bf16 CUDA matrix [rows, cols] (row-major, ld = stride(0)).
+    Returns {'row': QTensor, 'colT': QTensor, '2d': QTensor} for the requested layouts."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a CUDA bf16 matrix with unit column stride")
+    R, C = x.shape
+    outs = dict(outs or {})
+    if layouts & LAYOUT_ROW and "row" not in outs:
+        outs["row"] = empty_qtensor(R, C, LAYOUT_ROW, sf_layout, x.device)
+    if layouts & LAYOUT_COLT and "colT" not in outs:
+        outs["colT"] = empty_qtensor(C, R, LAYOUT_COLT, sf_layout, x.device)
+    if layouts & LAYOUT_2D and "2d" not in outs:
+        outs["2d"] = empty_qtensor(R, C, LAYOUT_2D, SF_PLAIN, x.device)
+    cs = {k: v.c() for k, v in outs.items()}
+    ref = lambda k: ctypes.byref(cs[k]) if (k in cs) else None
+    _check(lib().mxfp4_rotate_quantize(_ptr(x), R, C, x.stride(0), had, mode, layouts, ref("row"), ref("colT"),
+                                       ref("2d"), _stream(stream)))
+    for v in outs.values():
+        v.had, v.mode = had, mode
+    return outs
+
+
+def gemm(A: QTensor, B: QTensor, out_dtype: int = OUT_F32, accumulate: bool = False,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C[M,N] = A . B^T (block-scaled MXFP4, fp32 accumulation)."""
+    if out is None:
+        dt = torch.float32 if out_dtype == OUT_F32 else torch.bfloat16
+        out = (torch.zeros if accumulate else torch.empty)((A.rows, B.rows), dtype=dt, device=A.codes.device)
+    a, b = A.c(), B.c()
+    _check(lib().mxfp4_gemm(ctypes.byref(a), ctypes.byref(b), _ptr(out), out.stride(0), out_dtype, int(accumulate),
+                            None, 0, _stream(stream)))
+    return out
+
+
+@dataclass
+class Config:
+    had: int = HAD_16
+    mode: int = SCALE_FLOOR
+    out_dtype: int = OUT_F32
+    accumulate: int = 0
+
+    def c(self) -> MxConfigC:
+        return MxConfigC(self.had, self.mode, self.out_dtype, self.accumulate)
+
+
+class Workspace:
+    """Caller-owned scratch (torch memory), grown on demand, 256-byte aligned."""
+
+    def __init__(self):
+        self.buf = None
+
+    def get(self, nbytes: int, device) -> torch.Tensor | None:
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes + 256 or self.buf.device != torch.device(device):
+            self.buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self.buf.data_ptr()) % 256
+        return self.buf[off:off + nbytes]
+
+
+_default_ws = Workspace()
+
+
+def workspace_bytes(op: int, M: int, N: int, K: int, cfg: Config) -> int:
+    c = cfg.c()
+    return lib().mxfp4_workspace_bytes(op, M, N, K, ctypes.byref(c))
+
+
+def _out(shape, cfg: Config, device, out):
+    if out is not None:
+        return out
+    dt = torch.float32 if cfg.out_dtype == OUT_F32 else torch.bfloat16
+    return (torch.zeros if cfg.accumulate else torch.empty)(shape, dtype=dt, device=device)
+
+
+def _ref(c):
+    return ctypes.byref(c) if c is not None else None
+
+
+def linear_fprop(x: torch.Tensor, w: torch.Tensor, cfg: Config, save_xT: bool = True, save_wT: bool = True,
+                 y: torch.Tensor | None = None, xT: QTensor | None = None, wT: QTensor | None = None,
+                 ws: Workspace | None = None, stream=None):
+    """Y = X W^T with X [M,K], W [N,K] bf16; returns (Y, X^T quantised along M, W^T quantised along N)."""
+    M, K = x.shape
+    N = w.shape[0]
+    y = _out((M, N), cfg, x.device, y)
+    if save_xT and xT is None:
+        xT = empty_qtensor(K, M, LAYOUT_COLT, SF_MMA, x.device)
+    if save_wT and wT is None:
+        wT = empty_qtensor(K, N, LAYOUT_COLT, SF_MMA, x.device)
+    c = cfg.c()
+    nb = workspace_bytes(OP_FPROP, M, N, K, cfg)
+    buf = (ws or _default_ws).get(nb, x.device)
+    cx = xT.c() if save_xT else None
+    cw = wT.c() if save_wT else None
+    _check(lib().mxfp4_linear_fprop(_ptr(x), _ptr(w), M, N, K, ctypes.byref(c), _ptr(y), _ref(cx), _ref(cw),
+                                    _ptr(buf) if buf is not None else None, nb, _stream(stream)))
+    for q, cq in ((xT, cx), (wT, cw)):
+        if cq is not None:
+            q.had, q.mode = cfg.had, cfg.mode
+    return y, (xT if save_xT else None), (wT if save_wT else None)
+
+
+def linear_dgrad(dy: torch.Tensor, wT: QTensor, cfg: Config, save_dyT: bool = True,
+                 dx: torch.Tensor | None = None, dyT: QTensor | None = None, ws: Workspace | None = None,
+                 stream=None):
+    """dX = dY W with dY [M,N] bf16 and W^T [K,N] quantised along N; returns (dX, dY^T quantised along M)."""
+    M, N = dy.shape
+    K = wT.rows
+    dx = _out((M, K), cfg, dy.device, dx)
+    if save_dyT and dyT is None:
+        dyT = empty_qtensor(N, M, LAYOUT_COLT, SF_MMA, dy.device)
+    c = cfg.c()
+    nb = workspace_bytes(OP_DGRAD, M, N, K, cfg)
+    buf = (ws or _default_ws).get(nb, dy.device)
+    cw = wT.c()
+    cd = dyT.c() if save_dyT else None
+    _check(lib().mxfp4_linear_dgrad(_ptr(dy), ctypes.byref(cw), M, N, K, ctypes.byref(c), _ptr(dx), _ref(cd),
+                                    _ptr(buf) if buf is not None else None, nb, _stream(stream)))
+    if cd is not None:
+        dyT.had, dyT.mode = cfg.had, cfg.mode
+    return dx, (dyT if save_dyT else None)
+
+
+def linear_wgrad(dyT: QTensor, xT: QTensor, cfg: Config, dw: torch.Tensor | None = None, stream=None):
+    """dW = dY^T X from dY^T [N,M] and X^T [K,M] (both quantised along M)."""
+    dw = _out((dyT.rows, xT.rows), cfg, dyT.codes.device, dw)
+    c, a, b = cfg.c(), dyT.c(), xT.c()
+    _check(lib().mxfp4_linear_wgrad(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), _ptr(dw), None, 0,
+                                    _stream(stream)))
+    return dw
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status (0 = ok)."""
+    return lib().mxfp4_device_status(_stream(stream))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    lib().mxfp4_set_wait_limit_ns(int(ns))
+
+
+def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """bf16 bit patterns (numpy uint16) -> bf16 torch tensor on `device`."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)

@@ -1,0 +1,240 @@
+// gemm.cu -- block-scaled MXFP4 GEMM C = A . B^T on the sm_103a tcgen05 tensor cores.
+//
+// QDQ numerics ("Decomposing MXFP4 quantization error ...", experiments): E2M1
+// elements, one E8M0 scale per 32 elements of K on both operands, FP32 accumulation.
+// The operands are the quantised copies of "Pretraining Large Language Models with
+// MXFP4 on Native FP4 Hardware" (C.1-C.3), already rotated along K.
+//
+// Structure (one 128 x BN output tile per CTA, 192 threads):
+//   warp 0  TMA producer: 128x128-byte code tiles of A and B (128B swizzle) and the
+//           matching 1 KB scale-factor atoms, into a STAGES-deep shared-memory ring.
+//   warp 1  allocates TMEM; one elected thread copies each stage's scale factors
+//           SMEM->TMEM (tcgen05.cp) and issues 4 tcgen05.mma.kind::mxf4 (K = 64
+//           each) per 256-element stage into an fp32 TMEM accumulator.
+//   warps 2-5 epilogue: TMEM -> registers (tcgen05.ld) -> fp32/bf16 global stores.
+// All waits are bounded; on expiry the status word records a timeout and the CTA
+// drains what it issued and exits.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mx {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK_BYTES = 128;  // 256 E2M1 elements per stage
+constexpr int GEMM_THREADS = 192;
+
+template <int BN, int STAGES>
+struct GemmCfg {
+    static constexpr int A_STAGE = BM * BK_BYTES;
+    static constexpr int B_STAGE = BN * BK_BYTES;
+    static constexpr int SFA_STAGE = 1024;  // 128 rows x 8 blocks
+    static constexpr int SFB_STAGE = (BN / 128) * 1024;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
+    static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 1) * 8;
+    static constexpr int SMEM = OFF_TMEM + 16 + 1024;  // + alignment slack
+    static constexpr int TX_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+    static constexpr int SF_COLS = 8 + 8 * (BN / 128);  // TMEM columns of scales per stage
+    static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
+                                   : TMEM_USED <= 256 ? 256 : 512;
+    static_assert(TMEM_USED <= 512, "TMEM budget");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int64_t row, int64_t col, const uint32_t (&v)[32]) {
+    if (row >= p.M) return;
+    const int64_t n_left = p.N - col;
+    if (n_left <= 0) return;
+    if (!p.out_bf16) {
+        float* dst = reinterpret_cast<float*>(p.C) + row * p.ldc + col;
+        if (n_left >= 32) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                float4 o = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                                       __uint_as_float(v[i + 3]));
+                if (p.accumulate) {
+                    const float4 c = *reinterpret_cast<const float4*>(dst + i);
+                    o.x += c.x;
+                    o.y += c.y;
+                    o.z += c.z;
+                    o.w += c.w;
+                }
+                *reinterpret_cast<float4*>(dst + i) = o;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < n_left) dst[i] = (p.accumulate ? dst[i] : 0.0f) + __uint_as_float(v[i]);
+        }
+    } else {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + row * p.ldc + col;
+        if (n_left >= 32) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __nv_bfloat162 h =
+                        __floats2bfloat162_rn(__uint_as_float(v[i + 2 * j]), __uint_as_float(v[i + 2 * j + 1]));
+                    w[j] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                *reinterpret_cast<uint4*>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < n_left) dst[i] = __float2bfloat16_rn(__uint_as_float(v[i]));
+        }
+    }
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid_constant__ GemmParams p) {
+    using Cfg = GemmCfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem + Cfg::OFF_A;
+    uint8_t* sB = smem + Cfg::OFF_B;
+    uint8_t* sSFA = smem + Cfg::OFF_SFA;
+    uint8_t* sSFB = smem + Cfg::OFF_SFB;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tmem_full = empty + STAGES;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_TMEM);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m0 = (int64_t)blockIdx.y * BM;
+    const int64_t n0 = (int64_t)blockIdx.x * BN;
+    const int num_k = (int)((p.K + 255) / 256);
+    const int64_t atoms_per_row_block = p.kb_pad / 4;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tmem_full, 1);
+        fence_mbar_init();
+        prefetch_tmap(&p.map_a);
+        prefetch_tmap(&p.map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (elect_one()) {
+            int issued = 0;
+            for (int kt = 0; kt < num_k; ++kt) {
+                const int s = kt % STAGES;
+                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                if (kt >= STAGES && !wait_bounded(&empty[s], ph ^ 1u, p.wait_ns, p.status)) break;
+                mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
+                tma_load_2d(sA + s * Cfg::A_STAGE, &p.map_a, &full[s], kt * BK_BYTES, (int32_t)m0);
+                tma_load_2d(sB + s * Cfg::B_STAGE, &p.map_b, &full[s], kt * BK_BYTES, (int32_t)n0);
+                bulk_load(sSFA + s * Cfg::SFA_STAGE, p.sfa + ((m0 / 128) * atoms_per_row_block + 2 * kt) * 512, 1024,
+                          &full[s]);
+#pragma unroll
+                for (int j = 0; j < BN / 128; ++j)
+                    bulk_load(sSFB + s * Cfg::SFB_STAGE + j * 1024,
+                              p.sfb + ((n0 / 128 + j) * atoms_per_row_block + 2 * kt) * 512, 1024, &full[s]);
+                ++issued;
+            }
+            // Drain: every copy this thread issued has landed before the CTA exits.
+            for (int kt = issued > STAGES ? issued - STAGES : 0; kt < issued; ++kt)
+                wait_bounded(&full[kt % STAGES], (uint32_t)(kt / STAGES) & 1u, p.wait_ns, p.status);
+        }
+    } else if (warp == 1) {
+        if (elect_one()) {
+            constexpr uint32_t idesc = idesc_mxf4(BM, BN);
+            for (int kt = 0; kt < num_k; ++kt) {
+                const int s = kt % STAGES;
+                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                if (!wait_bounded(&full[s], ph, p.wait_ns, p.status)) break;
+                tc_fence_after();
+                const uint32_t sfa_t = tmem_base + BN + s * Cfg::SF_COLS;
+                const uint32_t sfb_t = sfa_t + 8;
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+                    tc_cp_32x128b_warpx4(sfa_t + a * 4,
+                                         smem_desc(smem_u32(sSFA + s * Cfg::SFA_STAGE + a * 512), 0, 128, kSwizzleNone));
+#pragma unroll
+                for (int j = 0; j < BN / 128; ++j)
+#pragma unroll
+                    for (int a = 0; a < 2; ++a)
+                        tc_cp_32x128b_warpx4(
+                            sfb_t + j * 8 + a * 4,
+                            smem_desc(smem_u32(sSFB + s * Cfg::SFB_STAGE + j * 1024 + a * 512), 0, 128, kSwizzleNone));
+                const uint32_t a_base = smem_u32(sA + s * Cfg::A_STAGE);
+                const uint32_t b_base = smem_u32(sB + s * Cfg::B_STAGE);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t adesc = smem_desc(a_base + k * 32, 16, 1024, kSwizzle128B);
+                    const uint64_t bdesc = smem_desc(b_base + k * 32, 16, 1024, kSwizzle128B);
+                    const uint32_t sf_id = (uint32_t)(k & 1) * 2u;
+                    tc_mma_mxf4(tmem_base, adesc, bdesc, idesc_with_sf_ids(idesc, sf_id, sf_id), sfa_t + (k >> 1) * 4,
+                                sfb_t + (k >> 1) * 4, (kt | k) != 0);
+                }
+                tc_commit(&empty[s]);
+            }
+            tc_commit(tmem_full);
+        }
+    } else {
+        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its sub-partition)
+        const int q = warp & 3;
+        if (wait_bounded(tmem_full, 0, p.wait_ns, p.status)) {
+            tc_fence_after();
+            const int64_t row = m0 + q * 32 + lane;
+#pragma unroll 1
+            for (int j = 0; j < BN / 32; ++j) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * 32), v);
+                tmem_ld_wait();
+                store_row_chunk(p, row, n0 + j * 32, v);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
+    using Cfg = GemmCfg<BN, STAGES>;
+    auto kern = mxf4_gemm_kernel<BN, STAGES>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM));
+    kern<<<grid, GEMM_THREADS, Cfg::SMEM, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s) { return launch_cfg<128, 6>(p, s); }
+
+}  // namespace mx

@@ -1,0 +1,57 @@
+// internal.h -- declarations shared by the library's translation units (not part
+// of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mxfp4.h"
+
+namespace mx {
+
+// Scale-factor MMA tile order: 128 rows x 4 blocks per 512-byte atom.
+__host__ __device__ inline int64_t sf_kb_pad(int64_t cols) { return ((cols / 32 + 7) / 8) * 8; }
+__host__ __device__ inline int64_t sf_rows_pad(int64_t rows) { return ((rows + 127) / 128) * 128; }
+__host__ __device__ inline int64_t sf_mma_offset(int64_t r, int64_t k, int64_t kb_pad) {
+    return ((r >> 7) * (kb_pad >> 2) + (k >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (k & 3);
+}
+
+struct QuantOut {
+    uint8_t* codes;   // packed nibbles
+    uint8_t* scales;  // E8M0 bytes
+    int32_t sf_mma;   // 1: MMA tile order
+    int64_t kb_pad;   // padded blocks per row (MMA order)
+};
+
+struct QuantParams {
+    const uint16_t* x;  // bf16 [R, C]
+    int64_t R, C, ld;
+    int32_t mode;
+    QuantOut row, colT, twoD;
+};
+
+// Launches the fused rotate+quantise kernel for the requested layouts.
+cudaError_t launch_rotate_quantize(const QuantParams& p, int had, unsigned layouts, cudaStream_t s);
+
+struct GemmParams {
+    CUtensorMap map_a;   // codes of A [M, K/2] bytes, box 128 rows x 128 B, 128B swizzle
+    CUtensorMap map_b;   // codes of B [N, K/2] bytes
+    const uint8_t* sfa;  // MMA-order scales of A
+    const uint8_t* sfb;  // MMA-order scales of B
+    int64_t M, N, K, kb_pad;
+    void* C;
+    int64_t ldc;
+    int32_t out_bf16;
+    int32_t accumulate;
+    uint32_t* status;
+    uint64_t wait_ns;
+};
+
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s);
+
+// Host helpers implemented in mxfp4_api.cu.
+uint32_t* device_status_ptr();  // for the current device
+bool encode_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t cols, uint32_t box_rows);
+
+}  // namespace mx

@@ -1,0 +1,442 @@
+// mxfp4_api.cu -- host side of the C ABI (include/mxfp4.h): argument validation,
+// tensor-map encoding, workspace carving and kernel dispatch.  Nothing here
+// allocates memory; the only global state is one device status word per device.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mx {
+
+__device__ uint32_t g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+thread_local char t_last_error[512] = "";
+thread_local uint64_t t_wait_ns = 0;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+std::mutex g_mu;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_device_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
+
+mxfp4_status fail(mxfp4_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+mxfp4_status ok() {
+    t_last_error[0] = 0;
+    return MXFP4_OK;
+}
+
+mxfp4_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MXFP4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+uint64_t wait_limit() { return t_wait_ns ? t_wait_ns : kDefaultWaitNs; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks that the current device is a GB300 (compute capability 10.3) and looks up
+// the device address of its status word once.
+mxfp4_status check_device(int* dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MXFP4_ERR_UNSUPPORTED_DEVICE, "device index %d", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_device_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        if (g_device_ok[dev] == 1) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_status_word);
+            if (e != cudaSuccess) {
+                g_device_ok[dev] = 0;
+                return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+            }
+            g_status_ptr[dev] = static_cast<uint32_t*>(p);
+        }
+    }
+    if (g_device_ok[dev] != 1)
+        return fail(MXFP4_ERR_UNSUPPORTED_DEVICE, "device %d is not compute capability 10.3 (GB300)", dev);
+    *dev_out = dev;
+    return MXFP4_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load();
+    if (!f) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<EncodeTiledFn>(p);
+            fn.store(f);
+        }
+    }
+    return f;
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool valid_had(int h) { return h == 0 || h == 16 || h == 32; }
+bool valid_mode(int m) { return m == 0 || m == 1; }
+
+}  // namespace
+
+uint32_t* device_status_ptr() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return (dev >= 0 && dev < kMaxDevices) ? g_status_ptr[dev] : nullptr;
+}
+
+// 2D tensor map over packed codes [rows, cols/2] bytes: box = 128 bytes x box_rows,
+// 128-byte swizzle (the K-major layout the MMA descriptors expect), zero fill.
+bool encode_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t cols, uint32_t box_rows) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)(cols / 2), (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(cols / 2)};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+namespace {
+
+// Validates a caller-provided quantised output descriptor.
+mxfp4_status check_out(const mxfp4_tensor* t, const char* name, bool allow_mma) {
+    if (!t) return fail(MXFP4_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!t->codes || !t->scales) return fail(MXFP4_ERR_INVALID_ARG, "%s: codes/scales NULL", name);
+    if (!aligned16(t->codes) || !aligned16(t->scales))
+        return fail(MXFP4_ERR_MISALIGNED, "%s: codes/scales not 16-byte aligned", name);
+    if (t->sf_layout != MXFP4_SF_PLAIN && t->sf_layout != MXFP4_SF_MMA)
+        return fail(MXFP4_ERR_INVALID_ARG, "%s: bad sf_layout %d", name, t->sf_layout);
+    if (t->sf_layout == MXFP4_SF_MMA && !allow_mma)
+        return fail(MXFP4_ERR_INVALID_ARG, "%s: the 2D layout has PLAIN scales only", name);
+    return MXFP4_OK;
+}
+
+QuantOut to_out(const mxfp4_tensor* t) {
+    QuantOut o{};
+    if (t) {
+        o.codes = static_cast<uint8_t*>(t->codes);
+        o.scales = t->scales;
+        o.sf_mma = t->sf_layout == MXFP4_SF_MMA;
+        o.kb_pad = sf_kb_pad(t->cols);
+    }
+    return o;
+}
+
+bool needs_sf_padding(const mxfp4_tensor* t) {
+    return t && t->sf_layout == MXFP4_SF_MMA && (t->rows % 128 != 0 || (t->cols / 32) % 8 != 0);
+}
+
+mxfp4_status check_gemm_operand(const mxfp4_tensor* t, const char* name) {
+    if (!t) return fail(MXFP4_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!t->codes || !t->scales) return fail(MXFP4_ERR_INVALID_ARG, "%s: codes/scales NULL", name);
+    if (!aligned16(t->codes) || !aligned16(t->scales))
+        return fail(MXFP4_ERR_MISALIGNED, "%s: codes/scales not 16-byte aligned", name);
+    if (t->sf_layout != MXFP4_SF_MMA) return fail(MXFP4_ERR_INVALID_ARG, "%s: GEMM operands need MMA scales", name);
+    if (t->layout == MXFP4_LAYOUT_2D)
+        return fail(MXFP4_ERR_INVALID_ARG, "%s: 2D-layout tensors cannot feed the GEMM", name);
+    if (t->rows <= 0 || t->cols <= 0) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "%s: empty", name);
+    if (t->cols % 32 != 0) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "%s: cols %% 32 != 0", name);
+    if (t->rows > (int64_t)INT32_MAX || t->cols / 2 > (int64_t)INT32_MAX)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "%s: too large", name);
+    return MXFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mxfp4_codes_bytes(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols < 0 || cols % 2) return 0;
+    return (size_t)rows * (size_t)(cols / 2);
+}
+
+size_t mxfp4_scales_bytes(int64_t rows, int64_t cols, int layout, int sf_layout) {
+    if (rows < 0 || cols < 0 || cols % 32) return 0;
+    if (layout == MXFP4_LAYOUT_2D) {
+        if (sf_layout != MXFP4_SF_PLAIN || rows % 32) return 0;
+        return (size_t)(rows / 32) * (size_t)(cols / 32);
+    }
+    if (layout != MXFP4_LAYOUT_ROW && layout != MXFP4_LAYOUT_COLT) return 0;
+    if (sf_layout == MXFP4_SF_PLAIN) return (size_t)rows * (size_t)(cols / 32);
+    if (sf_layout == MXFP4_SF_MMA) return (size_t)sf_rows_pad(rows) * (size_t)sf_kb_pad(cols);
+    return 0;
+}
+
+size_t mxfp4_quantized_bytes(int64_t rows, int64_t cols, int layout, int sf_layout) {
+    const size_t s = mxfp4_scales_bytes(rows, cols, layout, sf_layout);
+    if (!s && rows * cols) return 0;
+    return round_up(mxfp4_codes_bytes(rows, cols), 256) + round_up(s, 256);
+}
+
+const char* mxfp4_status_string(mxfp4_status s) {
+    switch (s) {
+        case MXFP4_OK: return "ok";
+        case MXFP4_ERR_INVALID_ARG: return "invalid argument";
+        case MXFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MXFP4_ERR_MISALIGNED: return "misaligned pointer or leading dimension";
+        case MXFP4_ERR_WORKSPACE: return "workspace missing or too small";
+        case MXFP4_ERR_CUDA: return "CUDA error";
+        case MXFP4_ERR_TIMEOUT: return "device-side wait timed out";
+        case MXFP4_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103 / GB300)";
+    }
+    return "unknown status";
+}
+
+const char* mxfp4_last_error(void) { return t_last_error; }
+
+void mxfp4_set_wait_limit_ns(uint64_t ns) { t_wait_ns = ns; }
+
+mxfp4_status mxfp4_device_status(mxfp4_stream_t stream) {
+    int dev;
+    mxfp4_status st = check_device(&dev);
+    if (st) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e, "read status word");
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+    if (word & kStatusTimeout) return fail(MXFP4_ERR_TIMEOUT, "a bounded device wait expired (status 0x%x)", word);
+    return ok();
+}
+
+mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                   unsigned layouts, mxfp4_tensor* row_out, mxfp4_tensor* colT_out,
+                                   mxfp4_tensor* twoD_out, mxfp4_stream_t stream) {
+    if (!x) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
+    if (rows < 0 || cols < 0) return fail(MXFP4_ERR_INVALID_ARG, "negative size");
+    if (!valid_had(had)) return fail(MXFP4_ERR_INVALID_ARG, "hadamard must be 0, 16 or 32 (got %d)", had);
+    if (!valid_mode(mode)) return fail(MXFP4_ERR_INVALID_ARG, "scale mode must be 0 or 1 (got %d)", mode);
+    const bool want_row = layouts & MXFP4_LAYOUT_ROW, want_colT = layouts & MXFP4_LAYOUT_COLT,
+               want_2d = layouts & MXFP4_LAYOUT_2D;
+    if (!layouts || (layouts & ~7u)) return fail(MXFP4_ERR_INVALID_ARG, "bad layout mask 0x%x", layouts);
+    if (want_2d && (want_row || want_colT))
+        return fail(MXFP4_ERR_INVALID_ARG, "the 2D layout is produced on its own");
+    if (cols % 32) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "cols (%lld) %% 32 != 0", (long long)cols);
+    if ((want_colT || want_2d) && rows % 32)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "rows (%lld) %% 32 != 0 for the column / 2D layout",
+                    (long long)rows);
+    if (ld < cols || ld % 8)
+        return fail(MXFP4_ERR_MISALIGNED, "ld (%lld) must be >= cols and a multiple of 8", (long long)ld);
+    if (!aligned16(x)) return fail(MXFP4_ERR_MISALIGNED, "x not 16-byte aligned");
+    if ((rows + 63) / 64 > 65535) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "too many rows");
+    mxfp4_status st;
+    if (want_row && (st = check_out(row_out, "row_out", true))) return st;
+    if (want_colT && (st = check_out(colT_out, "colT_out", true))) return st;
+    if (want_2d && (st = check_out(twoD_out, "twoD_out", false))) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    auto fill = [&](mxfp4_tensor* t, int64_t r, int64_t c, int layout) {
+        t->rows = r;
+        t->cols = c;
+        t->layout = layout;
+        t->had = had;
+        t->mode = mode;
+    };
+    if (want_row) fill(row_out, rows, cols, MXFP4_LAYOUT_ROW);
+    if (want_colT) fill(colT_out, cols, rows, MXFP4_LAYOUT_COLT);
+    if (want_2d) fill(twoD_out, rows, cols, MXFP4_LAYOUT_2D);
+    if (rows == 0 || cols == 0) return ok();
+
+    for (mxfp4_tensor* t : {want_row ? row_out : nullptr, want_colT ? colT_out : nullptr}) {
+        if (needs_sf_padding(t)) {
+            cudaError_t e =
+                cudaMemsetAsync(t->scales, 0, mxfp4_scales_bytes(t->rows, t->cols, t->layout, t->sf_layout), s);
+            if (e != cudaSuccess) return cuda_fail(e, "clear scale padding");
+        }
+    }
+    QuantParams p{};
+    p.x = static_cast<const uint16_t*>(x);
+    p.R = rows;
+    p.C = cols;
+    p.ld = ld;
+    p.mode = mode;
+    p.row = to_out(want_row ? row_out : nullptr);
+    p.colT = to_out(want_colT ? colT_out : nullptr);
+    p.twoD = to_out(want_2d ? twoD_out : nullptr);
+    cudaError_t e = launch_rotate_quantize(p, had, layouts, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize launch");
+    return ok();
+}
+
+mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, int64_t ldc, int out_dtype,
+                        int accumulate, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    mxfp4_status st;
+    if ((st = check_gemm_operand(A, "A")) || (st = check_gemm_operand(B, "B"))) return st;
+    if (A->cols != B->cols)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "contraction mismatch: A cols %lld, B cols %lld", (long long)A->cols,
+                    (long long)B->cols);
+    if (!C) return fail(MXFP4_ERR_INVALID_ARG, "C is NULL");
+    if (out_dtype != MXFP4_OUT_F32 && out_dtype != MXFP4_OUT_BF16)
+        return fail(MXFP4_ERR_INVALID_ARG, "bad out_dtype %d", out_dtype);
+    if (accumulate && out_dtype != MXFP4_OUT_F32) return fail(MXFP4_ERR_INVALID_ARG, "accumulate needs fp32 output");
+    if (ldc < B->rows || ldc % 8)
+        return fail(MXFP4_ERR_MISALIGNED, "ldc (%lld) must be >= N and a multiple of 8", (long long)ldc);
+    if (!aligned16(C)) return fail(MXFP4_ERR_MISALIGNED, "C not 16-byte aligned");
+    int dev;
+    if ((st = check_device(&dev))) return st;
+
+    GemmParams p{};
+    if (!encode_codes_map(&p.map_a, A->codes, A->rows, A->cols, 128) ||
+        !encode_codes_map(&p.map_b, B->codes, B->rows, B->cols, 128))
+        return fail(MXFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    p.sfa = A->scales;
+    p.sfb = B->scales;
+    p.M = A->rows;
+    p.N = B->rows;
+    p.K = A->cols;
+    p.kb_pad = sf_kb_pad(A->cols);
+    p.C = C;
+    p.ldc = ldc;
+    p.out_bf16 = out_dtype == MXFP4_OUT_BF16;
+    p.accumulate = accumulate ? 1 : 0;
+    p.status = device_status_ptr();
+    p.wait_ns = wait_limit();
+    cudaError_t e = launch_gemm(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    return ok();
+}
+
+size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp4_config* cfg) {
+    (void)cfg;
+    switch (op) {
+        case MXFP4_OP_FPROP:
+            return mxfp4_quantized_bytes(M, K, MXFP4_LAYOUT_ROW, MXFP4_SF_MMA) +
+                   mxfp4_quantized_bytes(N, K, MXFP4_LAYOUT_ROW, MXFP4_SF_MMA);
+        case MXFP4_OP_DGRAD:
+            return mxfp4_quantized_bytes(M, N, MXFP4_LAYOUT_ROW, MXFP4_SF_MMA);
+        case MXFP4_OP_WGRAD:
+            return 0;
+    }
+    return 0;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Carves one quantised tensor (codes, then scales at a 256-byte boundary) from ws.
+mxfp4_tensor carve(uint8_t*& ws, int64_t rows, int64_t cols) {
+    mxfp4_tensor t{};
+    t.codes = ws;
+    t.scales = ws + round_up(mxfp4_codes_bytes(rows, cols), 256);
+    t.sf_layout = MXFP4_SF_MMA;
+    ws += mxfp4_quantized_bytes(rows, cols, MXFP4_LAYOUT_ROW, MXFP4_SF_MMA);
+    return t;
+}
+
+mxfp4_status check_cfg(const mxfp4_config* cfg) {
+    if (!cfg) return fail(MXFP4_ERR_INVALID_ARG, "cfg is NULL");
+    if (!valid_had(cfg->had)) return fail(MXFP4_ERR_INVALID_ARG, "cfg.had must be 0, 16 or 32");
+    if (!valid_mode(cfg->mode)) return fail(MXFP4_ERR_INVALID_ARG, "cfg.mode must be 0 or 1");
+    if (cfg->out_dtype != MXFP4_OUT_F32 && cfg->out_dtype != MXFP4_OUT_BF16)
+        return fail(MXFP4_ERR_INVALID_ARG, "cfg.out_dtype invalid");
+    return MXFP4_OK;
+}
+
+mxfp4_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (need && (!ws || ws_bytes < need))
+        return fail(MXFP4_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu at %p)", need, ws_bytes, ws);
+    if (need && (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return fail(MXFP4_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    return MXFP4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mxfp4_status mxfp4_linear_fprop(const void* x, const void* w, int64_t M, int64_t N, int64_t K,
+                                const mxfp4_config* cfg, void* y, mxfp4_tensor* save_xT, mxfp4_tensor* save_wT,
+                                void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
+    mxfp4_status st;
+    if ((st = check_cfg(cfg))) return st;
+    if (!x || !w || !y) return fail(MXFP4_ERR_INVALID_ARG, "x, w and y must be non-NULL");
+    if (M <= 0 || N <= 0 || K <= 0) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "M, N, K must be positive");
+    if (K % 32) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "K %% 32 != 0");
+    if (save_xT && save_xT->sf_layout != MXFP4_SF_MMA) return fail(MXFP4_ERR_INVALID_ARG, "save_xT needs MMA scales");
+    if (save_wT && save_wT->sf_layout != MXFP4_SF_MMA) return fail(MXFP4_ERR_INVALID_ARG, "save_wT needs MMA scales");
+    if ((st = check_ws(ws, ws_bytes, mxfp4_workspace_bytes(MXFP4_OP_FPROP, M, N, K, cfg)))) return st;
+    uint8_t* cur = static_cast<uint8_t*>(ws);
+    mxfp4_tensor xq = carve(cur, M, K), wq = carve(cur, N, K);
+    if ((st = mxfp4_rotate_quantize(x, M, K, K, cfg->had, cfg->mode,
+                                    MXFP4_LAYOUT_ROW | (save_xT ? MXFP4_LAYOUT_COLT : 0), &xq, save_xT, nullptr,
+                                    stream)))
+        return st;
+    if ((st = mxfp4_rotate_quantize(w, N, K, K, cfg->had, cfg->mode,
+                                    MXFP4_LAYOUT_ROW | (save_wT ? MXFP4_LAYOUT_COLT : 0), &wq, save_wT, nullptr,
+                                    stream)))
+        return st;
+    return mxfp4_gemm(&xq, &wq, y, N, cfg->out_dtype, cfg->accumulate, nullptr, 0, stream);
+}
+
+mxfp4_status mxfp4_linear_dgrad(const void* dy, const mxfp4_tensor* wT, int64_t M, int64_t N, int64_t K,
+                                const mxfp4_config* cfg, void* dx, mxfp4_tensor* save_dyT, void* ws,
+                                size_t ws_bytes, mxfp4_stream_t stream) {
+    mxfp4_status st;
+    if ((st = check_cfg(cfg))) return st;
+    if (!dy || !wT || !dx) return fail(MXFP4_ERR_INVALID_ARG, "dy, wT and dx must be non-NULL");
+    if (M <= 0 || N <= 0 || K <= 0) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "M, N, K must be positive");
+    if (N % 32) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "N %% 32 != 0");
+    if (wT->rows != K || wT->cols != N)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "wT must be [K, N] = [%lld, %lld]", (long long)K, (long long)N);
+    if (save_dyT && save_dyT->sf_layout != MXFP4_SF_MMA)
+        return fail(MXFP4_ERR_INVALID_ARG, "save_dyT needs MMA scales");
+    if ((st = check_ws(ws, ws_bytes, mxfp4_workspace_bytes(MXFP4_OP_DGRAD, M, N, K, cfg)))) return st;
+    uint8_t* cur = static_cast<uint8_t*>(ws);
+    mxfp4_tensor dyq = carve(cur, M, N);
+    if ((st = mxfp4_rotate_quantize(dy, M, N, N, cfg->had, cfg->mode,
+                                    MXFP4_LAYOUT_ROW | (save_dyT ? MXFP4_LAYOUT_COLT : 0), &dyq, save_dyT, nullptr,
+                                    stream)))
+        return st;
+    return mxfp4_gemm(&dyq, wT, dx, K, cfg->out_dtype, cfg->accumulate, nullptr, 0, stream);
+}
+
+mxfp4_status mxfp4_linear_wgrad(const mxfp4_tensor* dyT, const mxfp4_tensor* xT, const mxfp4_config* cfg,
+                                void* dw, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
+    mxfp4_status st;
+    if ((st = check_cfg(cfg))) return st;
+    if (!dyT || !xT || !dw) return fail(MXFP4_ERR_INVALID_ARG, "dyT, xT and dw must be non-NULL");
+    if (dyT->cols != xT->cols) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "dyT and xT must share the token dim");
+    return mxfp4_gemm(dyT, xT, dw, xT->rows, cfg->out_dtype, cfg->accumulate, ws, ws_bytes, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+"""C-ABI library checks that need no GPU: it loads, exports every declared symbol,
+sizes its buffers as documented, and rejects invalid arguments before launching."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import __graft_entry__
+from mxfp4_precision_gemms_gb300 import binding as mx
+
+
+@pytest.fixture(scope="module")
+def L():
+    __graft_entry__.build()
+    return mx.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = mx.declared_symbols()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_buffer_sizes(L):
+    assert L.mxfp4_codes_bytes(256, 512) == 256 * 256
+    assert L.mxfp4_scales_bytes(256, 512, mx.LAYOUT_ROW, mx.SF_PLAIN) == 256 * 16
+    # MMA order pads rows to 128 and 32-blocks to a multiple of 8
+    assert L.mxfp4_scales_bytes(200, 96, mx.LAYOUT_ROW, mx.SF_MMA) == 256 * 8
+    assert L.mxfp4_scales_bytes(8192, 4096, mx.LAYOUT_COLT, mx.SF_MMA) == 8192 * 128
+    assert L.mxfp4_scales_bytes(64, 64, mx.LAYOUT_2D, mx.SF_PLAIN) == 4
+    assert L.mxfp4_scales_bytes(64, 64, mx.LAYOUT_2D, mx.SF_MMA) == 0
+    assert L.mxfp4_scales_bytes(64, 48, mx.LAYOUT_ROW, mx.SF_PLAIN) == 0  # cols % 32 != 0
+    q = L.mxfp4_quantized_bytes(8192, 4096, mx.LAYOUT_ROW, mx.SF_MMA)
+    assert q == 8192 * 2048 + 8192 * 128
+    cfg = mx.Config()
+    assert mx.workspace_bytes(mx.OP_FPROP, 8192, 6144, 4096, cfg) == (
+        L.mxfp4_quantized_bytes(8192, 4096, 1, 1) + L.mxfp4_quantized_bytes(6144, 4096, 1, 1))
+    assert mx.workspace_bytes(mx.OP_DGRAD, 8192, 6144, 4096, cfg) == L.mxfp4_quantized_bytes(8192, 6144, 1, 1)
+    assert mx.workspace_bytes(mx.OP_WGRAD, 8192, 6144, 4096, cfg) == 0
+
+
+def _tensor(codes=0x1000, scales=0x2000, rows=128, cols=256, layout=1, sf=1):
+    return mx.MxTensorC(codes, scales, rows, cols, layout, sf, 16, 0)
+
+
+def _rq(L, x=0x1000, rows=64, cols=64, ld=64, had=16, mode=0, layouts=1, row=None, colT=None, twoD=None):
+    return L.mxfp4_rotate_quantize(ctypes.c_void_p(x), rows, cols, ld, had, mode, layouts,
+                                   ctypes.byref(row) if row else None, ctypes.byref(colT) if colT else None,
+                                   ctypes.byref(twoD) if twoD else None, None)
+
+
+def test_rotate_quantize_rejects_bad_arguments(L):
+    """Every case fails validation before any CUDA call (the pointers are never touched)."""
+    t = _tensor()
+    assert _rq(L, x=0, row=t) == 1                       # NULL input
+    assert _rq(L, had=8, row=t) == 1                     # bad Hadamard size
+    assert _rq(L, mode=2, row=t) == 1                    # bad scale mode
+    assert _rq(L, layouts=0, row=t) == 1                 # nothing requested
+    assert _rq(L, layouts=5, row=t, twoD=t) == 1         # 2D mixed with row
+    assert _rq(L, cols=48, ld=48, row=t) == 2            # cols % 32
+    assert _rq(L, rows=40, layouts=2, colT=t) == 2       # rows % 32 for the column copy
+    assert _rq(L, ld=60, row=t) == 3                     # ld % 8
+    assert b"ld" in L.mxfp4_last_error()
+    assert _rq(L, x=0x1008, row=t) == 3                  # misaligned x
+    assert _rq(L, row=None) == 1                         # missing output
+    assert _rq(L, row=_tensor(codes=0x1004)) == 3        # misaligned codes
+    assert _rq(L, layouts=4, twoD=_tensor(sf=1)) == 1    # 2D has plain scales only
+
+
+def test_gemm_rejects_bad_arguments(L):
+    a, b = _tensor(), _tensor()
+    c = ctypes.c_void_p(0x4000)
+    g = lambda A, B, C=c, ldc=128, out=0, acc=0: L.mxfp4_gemm(ctypes.byref(A), ctypes.byref(B), C, ldc, out, acc,
+                                                                  None, 0, None)
+    assert g(a, _tensor(cols=512)) == 2                  # contraction mismatch
+    assert g(a, _tensor(sf=0)) == 1                      # plain scales cannot feed the GEMM
+    assert g(a, b, C=ctypes.c_void_p(0)) == 1            # NULL output
+    assert g(a, b, out=1, acc=1) == 1                    # accumulate needs fp32
+    assert g(a, b, ldc=100) == 3                         # ldc % 8
+    assert g(a, b, ldc=64) == 3                          # ldc < N
+    assert g(a, _tensor(layout=4)) == 1                  # 2D operand
+    assert g(_tensor(cols=48), _tensor(cols=48)) == 2    # cols % 32
+
+
+def test_linear_rejects_bad_arguments(L):
+    cfg = mx.MxConfigC(16, 0, 0, 0)
+    bad = mx.MxConfigC(7, 0, 0, 0)
+    P = ctypes.c_void_p
+    f = lambda M, N, K, c=cfg, ws=P(0x10000), nb=1 << 40: L.mxfp4_linear_fprop(
+        P(0x1000), P(0x2000), M, N, K, ctypes.byref(c), P(0x3000), None, None, ws, nb, None)
+    assert f(64, 64, 64, c=bad) == 1
+    assert f(64, 64, 48) == 2
+    assert f(0, 64, 64) == 2
+    assert f(64, 64, 64, ws=P(0), nb=0) == 4             # workspace missing
+    assert f(64, 64, 64, nb=10) == 4                     # workspace too small
+    assert f(64, 64, 64, ws=P(0x10010)) == 3             # workspace not 256-aligned
+    wT = _tensor(rows=64, cols=96)
+    assert L.mxfp4_linear_dgrad(P(0x1000), ctypes.byref(wT), 64, 64, 64, ctypes.byref(cfg), P(0x3000), None,
+                                P(0x10000), 1 << 40, None) == 2  # wT shape mismatch
+
+
+def test_status_strings(L):
+    for s in range(8):
+        assert L.mxfp4_status_string(s)
+    assert L.mxfp4_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("rows,cols", [(128, 256), (200, 96), (33, 32), (256, 4096)])
+def test_mma_scale_order_roundtrip(rows, cols):
+    """Host-side MMA scale order: a bijection onto the non-padding bytes, matching the
+    documented formula at hand-computed positions."""
+    g = np.random.default_rng(0)
+    plain = g.integers(0, 254, size=(rows, cols // 32), dtype=np.uint8)
+    buf = mx.sf_plain_to_mma(plain, rows, cols)
+    assert buf.size == ((rows + 127) // 128) * 128 * ((cols // 32 + 7) // 8) * 8
+    assert np.array_equal(mx.sf_mma_to_plain(buf, rows, cols), plain)
+    idx = mx._mma_index(rows, cols)
+    assert len(np.unique(idx)) == idx.size
+    assert idx[0, 0] == 0
+    if rows > 33 and cols // 32 > 5:
+        # row 33 = (r%32 = 1, (r/32)%4 = 1); block 5 = (k/4 = 1, k%4 = 1)
+        kb_pad = ((cols // 32 + 7) // 8) * 8
+        assert idx[33, 5] == 1 * 512 + 1 * 16 + 1 * 4 + 1
+        if rows > 130:
+            assert idx[130, 0] == (kb_pad // 4) * 512 + 2 * 16
