@@ -237,7 +237,6 @@ mxfp4_status mxfp4_device_status(mxfp4_stream_t stream) {
 mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
                                    unsigned layouts, mxfp4_tensor* row_out, mxfp4_tensor* colT_out,
                                    mxfp4_tensor* twoD_out, mxfp4_stream_t stream) {
-    if (!x) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
     if (rows < 0 || cols < 0) return fail(MXFP4_ERR_INVALID_ARG, "negative size");
     if (!valid_had(had)) return fail(MXFP4_ERR_INVALID_ARG, "hadamard must be 0, 16 or 32 (got %d)", had);
     if (!valid_mode(mode)) return fail(MXFP4_ERR_INVALID_ARG, "scale mode must be 0 or 1 (got %d)", mode);
@@ -250,6 +249,22 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
     if ((want_colT || want_2d) && rows % 32)
         return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "rows (%lld) %% 32 != 0 for the column / 2D layout",
                     (long long)rows);
+    if ((want_row && !row_out) || (want_colT && !colT_out) || (want_2d && !twoD_out))
+        return fail(MXFP4_ERR_INVALID_ARG, "a requested output descriptor is NULL");
+    auto fill = [&](mxfp4_tensor* t, int64_t r, int64_t c, int layout) {
+        t->rows = r;
+        t->cols = c;
+        t->layout = layout;
+        t->had = had;
+        t->mode = mode;
+    };
+    if (rows == 0 || cols == 0) {  // nothing to read or write: no pointer is used
+        if (want_row) fill(row_out, rows, cols, MXFP4_LAYOUT_ROW);
+        if (want_colT) fill(colT_out, cols, rows, MXFP4_LAYOUT_COLT);
+        if (want_2d) fill(twoD_out, rows, cols, MXFP4_LAYOUT_2D);
+        return ok();
+    }
+    if (!x) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
     if (ld < cols || ld % 8)
         return fail(MXFP4_ERR_MISALIGNED, "ld (%lld) must be >= cols and a multiple of 8", (long long)ld);
     if (!aligned16(x)) return fail(MXFP4_ERR_MISALIGNED, "x not 16-byte aligned");
@@ -262,17 +277,9 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
     if ((st = check_device(&dev))) return st;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    auto fill = [&](mxfp4_tensor* t, int64_t r, int64_t c, int layout) {
-        t->rows = r;
-        t->cols = c;
-        t->layout = layout;
-        t->had = had;
-        t->mode = mode;
-    };
     if (want_row) fill(row_out, rows, cols, MXFP4_LAYOUT_ROW);
     if (want_colT) fill(colT_out, cols, rows, MXFP4_LAYOUT_COLT);
     if (want_2d) fill(twoD_out, rows, cols, MXFP4_LAYOUT_2D);
-    if (rows == 0 || cols == 0) return ok();
 
     for (mxfp4_tensor* t : {want_row ? row_out : nullptr, want_colT ? colT_out : nullptr}) {
         if (needs_sf_padding(t)) {

@@ -54,6 +54,7 @@ def test_rotate_quantize_rejects_bad_arguments(L):
     """Every case fails validation before any CUDA call (the pointers are never touched)."""
     t = _tensor()
     assert _rq(L, x=0, row=t) == 1                       # NULL input
+    assert _rq(L, x=0, rows=0, row=t) == 0               # empty: nothing is touched
     assert _rq(L, had=8, row=t) == 1                     # bad Hadamard size
     assert _rq(L, mode=2, row=t) == 1                    # bad scale mode
     assert _rq(L, layouts=0, row=t) == 1                 # nothing requested

@@ -1,0 +1,94 @@
+"""GPU block-scaled MXFP4 GEMM vs the CPU oracle.
+
+Operands are quantised by the oracle on the CPU and uploaded, so these tests check
+the GEMM alone: |C_gpu - C_oracle| <= 1e-5 * sum_k |dq a_k| |dq b_k| per element
+(plus 2^-8 |C| for bf16 output, the rounding of the output itself)."""
+import numpy as np
+import pytest
+
+import oracle
+from mxfp4_precision_gemms_gb300 import synth
+from tests.gpu_util import assert_within, gpu_ready
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return gpu_ready()
+
+
+def oracle_operands(M, N, K, seed, had=16, mode=0):
+    X, W, _ = synth.linear_inputs(M, N, K, seed)
+    return oracle.quantize(X, had, mode, "row"), oracle.quantize(W, had, mode, "row")
+
+
+def run(torch, qa, qb, out_dtype=0, accumulate=False, init=None):
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    A = mx.qtensor_from_host(*qa)
+    B = mx.qtensor_from_host(*qb)
+    out = None
+    if init is not None:
+        out = torch.from_numpy(init).cuda()
+    C = mx.gemm(A, B, out_dtype=out_dtype, accumulate=accumulate, out=out)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    return C.float().cpu().numpy().astype(np.float64)
+
+
+def test_single_block_scales(torch):
+    """K = 32: every output is 2^(ea+eb) * sum qa*qb; rows use distinct scales, so a
+    wrong scale-factor placement shows up as an exact power-of-two error."""
+    M, N, K = 128, 128, 32
+    g = np.random.default_rng(0)
+    ca = g.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    cb = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = (120 + (np.arange(M) % 13)).astype(np.uint8)[:, None]
+    sb = (124 + (np.arange(N) % 7)).astype(np.uint8)[:, None]
+    want, S = oracle.gemm(ca, sa, cb, sb)
+    got = run(torch, (ca, sa), (cb, sb))
+    assert_within(got, want, S, what="single block")
+
+
+@pytest.mark.parametrize("shape", [(128, 128, 256), (256, 512, 512), (128, 128, 2048), (384, 256, 1024)])
+def test_aligned_shapes(torch, shape):
+    M, N, K = shape
+    qa, qb = oracle_operands(M, N, K, 10)
+    want, S = oracle.gemm(*qa, *qb)
+    assert_within(run(torch, qa, qb), want, S, what=f"{shape}")
+
+
+@pytest.mark.parametrize("shape", [(200, 136, 96), (1, 8, 32), (130, 264, 1056), (77, 1000, 288), (256, 40, 4128)])
+def test_ragged_shapes(torch, shape):
+    M, N, K = shape
+    qa, qb = oracle_operands(M, N, K, 11, had=32, mode=1)
+    want, S = oracle.gemm(*qa, *qb)
+    assert_within(run(torch, qa, qb), want, S, what=f"{shape}")
+
+
+def test_bf16_output(torch):
+    qa, qb = oracle_operands(256, 384, 768, 12)
+    want, S = oracle.gemm(*qa, *qb)
+    assert_within(run(torch, qa, qb, out_dtype=1), want, S, bf16=True, what="bf16 out")
+
+
+def test_accumulate(torch):
+    qa, qb = oracle_operands(256, 256, 512, 13)
+    want, S = oracle.gemm(*qa, *qb)
+    init = np.random.default_rng(1).standard_normal((256, 256)).astype(np.float32)
+    got = run(torch, qa, qb, accumulate=True, init=init)
+    # the fp32 add of the old value rounds once more: allow 2^-23 (|init| + |C|)
+    assert_within(got - init.astype(np.float64), want, S + 0.02 * (np.abs(init) + np.abs(want)), what="accumulate")
+
+
+def test_extreme_scales(torch):
+    """Scale bytes near both ends of the E8M0 range used by the quantiser."""
+    M, N, K = 128, 128, 256
+    g = np.random.default_rng(3)
+    ca = g.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    cb = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = g.integers(100, 154, size=(M, K // 32), dtype=np.uint8)
+    sb = g.integers(100, 154, size=(N, K // 32), dtype=np.uint8)
+    want, S = oracle.gemm(ca, sa, cb, sb)
+    assert_within(run(torch, (ca, sa), (cb, sb)), want, S, what="wide scales")
