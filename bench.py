@@ -1,0 +1,419 @@
+"""Benchmark: H16 + MXFP4 linear-layer GEMMs (Fprop, Dgrad, Wgrad, quantisation
+included) on Llama-3.1-8B-shaped layers at T = 8192 tokens.
+
+One step = for each of the four linears (QKV 6144x4096, O 4096x4096, gate/up
+14336x4096, down 4096x14336): rotate+quantise X and W (row + transposed copies),
+Fprop GEMM (bf16 out); rotate+quantise dY (row + transposed), Dgrad GEMM (bf16 out);
+Wgrad GEMM (fp32 out).  The value is whole-job TFLOP/s (2*M*N*K per GEMM) with the
+inputs resident in HBM; L2 is flushed (256 MB write) before every timed step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the slow, plain reference of the same
+computation) on a bounded token slab of the same workload.  With torchrun (N > 1)
+every rank runs an independent replica on its own GPU (the path needs no exchange);
+time is the max over ranks and the value counts all ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "H16+MXFP4 linear TFLOPS (Fprop/Dgrad/Wgrad, quant incl.)"
+UNIT = "TFLOP/s"
+T_TOKENS = 8192
+WORKLOAD = "llama3.1-8b linears T=8192 (qkv 6144x4096, o 4096x4096, gate_up 14336x4096, down 4096x14336), " \
+           "H16, OCP floor scale, fprop+dgrad+wgrad, bf16 fprop/dgrad out, fp32 wgrad out"
+
+
+def flops_per_step(linears=None):
+    from mxfp4_precision_gemms_gb300 import synth
+
+    linears = linears or synth.LLAMA8B_LINEARS
+    return sum(3 * 2 * T_TOKENS * N * K for _, N, K in linears)
+
+
+def quant_bytes(R, C, dual):
+    """Algorithmic bytes of one rotate+quantise pass: bf16 read + codes + scales per copy."""
+    return R * C * 2 + (2 if dual else 1) * (R * C // 2 + R * C // 32)
+
+
+# --------------------------------------------------------------------------- dist
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, None
+    import torch.distributed as dist
+
+    backend = "nccl" if os.environ.get("BENCH_BACKEND", "") != "gloo" else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist.get_rank(), ws, dist
+
+
+def max_over_ranks(v, dist, device):
+    if dist is None:
+        return v
+    import torch
+
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+class Layer:
+    def __init__(self, name, N, K, seed, dev):
+        import torch
+
+        from mxfp4_precision_gemms_gb300 import binding as mx
+        from mxfp4_precision_gemms_gb300 import synth
+
+        self.name, self.N, self.K = name, N, K
+        X, W, dY = synth.linear_inputs(T_TOKENS, N, K, seed)
+        self.host = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+                     for k, v in (("x", X), ("w", W), ("dy", dY))}
+        self.x, self.w, self.dy = (self.host[k].to(dev) for k in ("x", "w", "dy"))
+        M = T_TOKENS
+        E = mx.empty_qtensor
+        self.xq = E(M, K, mx.LAYOUT_ROW, mx.SF_MMA, dev)
+        self.wq = E(N, K, mx.LAYOUT_ROW, mx.SF_MMA, dev)
+        self.dyq = E(M, N, mx.LAYOUT_ROW, mx.SF_MMA, dev)
+        self.xT = E(K, M, mx.LAYOUT_COLT, mx.SF_MMA, dev)
+        self.wT = E(K, N, mx.LAYOUT_COLT, mx.SF_MMA, dev)
+        self.dyT = E(N, M, mx.LAYOUT_COLT, mx.SF_MMA, dev)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        self.dw = torch.empty((N, K), dtype=torch.float32, device=dev)
+        self.quant_bytes = quant_bytes(M, K, True) + quant_bytes(N, K, True) + quant_bytes(M, N, True)
+        self.gemm_flops = 3 * 2 * M * N * K
+
+
+def run_step(layers, ev=None):
+    """One pass of the hot path.  If `ev` is a list, CUDA events are recorded around
+    every kernel launch: ev gets (kind, start, end, work) tuples."""
+    import torch
+
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    def timed(kind, work, fn):
+        if ev is None:
+            fn()
+            return
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ev.append((kind, a, b, work))
+
+    RC = mx.LAYOUT_ROW | mx.LAYOUT_COLT
+    for L in layers:
+        M, N, K = T_TOKENS, L.N, L.K
+        timed("quant", quant_bytes(M, K, True), lambda: mx.rotate_quantize(
+            L.x, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.xq, "colT": L.xT}))
+        timed("quant", quant_bytes(N, K, True), lambda: mx.rotate_quantize(
+            L.w, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.wq, "colT": L.wT}))
+        timed("gemm", 2 * M * N * K, lambda: mx.gemm(L.xq, L.wq, mx.OUT_BF16, out=L.y))
+        timed("quant", quant_bytes(M, N, True), lambda: mx.rotate_quantize(
+            L.dy, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.dyq, "colT": L.dyT}))
+        timed("gemm", 2 * M * N * K, lambda: mx.gemm(L.dyq, L.wT, mx.OUT_BF16, out=L.dx))
+        timed("gemm", 2 * M * N * K, lambda: mx.gemm(L.dyT, L.xT, mx.OUT_F32, out=L.dw))
+
+
+LAUNCHES_PER_LAYER = 6  # 3 rotate+quantise + 3 GEMM kernels
+
+
+def run_e2e_step(layers, ws):
+    """The same step through the public linear-layer API with host buffers: H2D of
+    X, W, dY from pinned memory, fprop/dgrad/wgrad, D2H of Y, dX, dW."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    cfg = mx.Config(had=mx.HAD_16, mode=mx.SCALE_FLOOR, out_dtype=mx.OUT_BF16)
+    wcfg = mx.Config(had=mx.HAD_16, mode=mx.SCALE_FLOOR, out_dtype=mx.OUT_F32)
+    for L in layers:
+        L.x.copy_(L.host["x"], non_blocking=True)
+        L.w.copy_(L.host["w"], non_blocking=True)
+        L.dy.copy_(L.host["dy"], non_blocking=True)
+        mx.linear_fprop(L.x, L.w, cfg, y=L.y, xT=L.xT, wT=L.wT, ws=ws)
+        mx.linear_dgrad(L.dy, L.wT, cfg, dx=L.dx, dyT=L.dyT, ws=ws)
+        mx.linear_wgrad(L.dyT, L.xT, wcfg, dw=L.dw)
+        L.out_host["y"].copy_(L.y, non_blocking=True)
+        L.out_host["dx"].copy_(L.dx, non_blocking=True)
+        L.out_host["dw"].copy_(L.dw, non_blocking=True)
+
+
+def gpu_arm(args, rank, world, dist):
+    import torch
+
+    from mxfp4_precision_gemms_gb300 import binding as mx
+    from mxfp4_precision_gemms_gb300 import synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mx.lib()
+    layers = [Layer(n, N, K, 2000 + 10 * i, dev) for i, (n, N, K) in enumerate(synth.LLAMA8B_LINEARS)]
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        run_step(layers)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0, "device status after warm-up"
+
+    # ---- timed region: K steps, L2 flushed before each, device-timed with events
+    step_ev, kern_ev = [], []
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run_step(layers, kern_ev)
+            b.record()
+            step_ev.append((a, b))
+        torch.cuda.synchronize()
+    barrier(dist)
+    status = mx.device_status()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
+    ms_per_step = total_ms / args.steps
+    fl = flops_per_step()
+    value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- per-kernel rooflines from the events of the timed region
+    agg = {}
+    for kind, a, b, work in kern_ev:
+        d = agg.setdefault(kind, [0.0, 0.0, 0])
+        d[0] += a.elapsed_time(b)
+        d[1] += work
+        d[2] += 1
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    hbm = peaks.get("hbm_gbs") or 6800.0
+    bf16_sus = peaks.get("bf16_tflops_sustained") or 1700.0
+    fp4_peak = bf16_sus * (13.5 / 2.25)  # nominal dense FP4 / BF16 ratio on GB300
+    g_ms, g_fl, g_n = agg.get("gemm", (0, 0, 0))
+    q_ms, q_by, q_n = agg.get("quant", (0, 0, 0))
+    gemm_tflops = g_fl / (g_ms * 1e-3) / 1e12 if g_ms else 0.0
+    quant_gbs = q_by / (q_ms * 1e-3) / 1e9 if q_ms else 0.0
+    gemm_share = g_ms / (g_ms + q_ms) if g_ms + q_ms else 0.0
+    roof_gemm = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1),
+                 "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4), "traffic": None,
+                 "kernel": "mxf4_gemm_kernel", "peak_source": "measured bf16 sustained x 6 (nominal fp4/bf16)"}
+    roof_quant = {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": hbm, "unit": "GB/s",
+                  "frac": round(quant_gbs / hbm, 4), "traffic": None, "kernel": "rq_kernel",
+                  "peak_source": "measured (hbm_gbs)"}
+    dominant = roof_gemm if gemm_share >= 0.5 else roof_quant
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.skip_e2e:
+        ws = mx.Workspace()
+        for L in layers:
+            L.out_host = {"y": torch.empty(L.y.shape, dtype=L.y.dtype).pin_memory(),
+                          "dx": torch.empty(L.dx.shape, dtype=L.dx.dtype).pin_memory(),
+                          "dw": torch.empty(L.dw.shape, dtype=L.dw.dtype).pin_memory()}
+        for _ in range(max(1, args.warmup)):
+            run_e2e_step(layers, ws)
+        torch.cuda.synchronize()
+        e2e_ms = []
+        barrier(dist)
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run_e2e_step(layers, ws)
+            b.record()
+            b.synchronize()
+            e2e_ms.append(a.elapsed_time(b))
+        tot = max_over_ranks(sum(e2e_ms), dist, dev)
+        h2d = sum(L.x.numel() * 2 + L.w.numel() * 2 + L.dy.numel() * 2 for L in layers)
+        d2h = sum(L.y.numel() * 2 + L.dx.numel() * 2 + L.dw.numel() * 4 for L in layers)
+        e2e = {"value": round(world * fl * args.steps / (tot * 1e-3) / 1e12, 2), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(tot / args.steps, 3)}
+        assert mx.device_status() == 0
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1)+e8m0 -> fp32 acc; bf16 in",
+        "data": "synthetic (seeded: X N(0,1)+1% channels x50, W N(0,0.02), dY N(0,1e-4)+2% tokens x20)",
+        "config": {"workload": WORKLOAD, "tokens": T_TOKENS, "flops_per_step": fl,
+                   "l2": "flushed (256 MB write) before every timed step; per-step events exclude the flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": dominant,
+        "kernels": {"gemm": {**roof_gemm, "launches": g_n, "ms_total": round(g_ms, 3), "share": round(gemm_share, 3)},
+                    "quant": {**roof_quant, "launches": q_n, "ms_total": round(q_ms, 3),
+                              "share": round(1 - gemm_share, 3)}},
+        "gemm_only_tflops": round(gemm_tflops, 1),
+        "quantize_gbs": round(quant_gbs, 1),
+        "e2e": e2e,
+        "gpu_launches": args.steps * LAUNCHES_PER_LAYER * len(layers),
+        "clocks": clk.summary(),
+        "device_status": status,
+    }
+    return out
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+def oracle_sample(tokens: int, linears):
+    """fprop + dgrad + wgrad of the given linears restricted to a `tokens`-row slab, on
+    the CPU oracle.  Returns (flops, seconds)."""
+    import oracle
+    from mxfp4_precision_gemms_gb300 import synth
+
+    fl, sec = 0, 0.0
+    for i, (_, N, K) in enumerate(linears):
+        X, W, dY = synth.linear_inputs(tokens, N, K, 2000 + 10 * i)
+        t = time.perf_counter()
+        oracle.fprop(X, W, 16, 0)
+        oracle.dgrad(dY, W, 16, 0)
+        oracle.wgrad(dY, X, 16, 0)
+        sec += time.perf_counter() - t
+        fl += 3 * 2 * tokens * N * K
+    return fl, sec
+
+
+def cpu_baseline_leg():
+    import oracle
+    from mxfp4_precision_gemms_gb300 import synth
+
+    oracle.lib()
+    tokens = 32
+    fl, sec = oracle_sample(tokens, synth.LLAMA8B_LINEARS)
+    return {"value": round(fl / sec / 1e12, 6), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"fprop+dgrad+wgrad of the four Llama linears on a {tokens}-token slab "
+                      f"({fl / 1e9:.1f} GFLOP, {sec:.1f} s)"}
+
+
+def reference_arm(args, rank, world):
+    """The CPU oracle as the reference arm, on a bounded slab of the same workload."""
+    if rank != 0:
+        return None
+    import oracle
+    from mxfp4_precision_gemms_gb300 import synth
+
+    oracle.lib()
+    tokens = 16
+    lin = synth.LLAMA8B_LINEARS[:1]
+    for _ in range(args.warmup):
+        oracle_sample(tokens, lin)
+    fl = sec = 0
+    for _ in range(args.steps):
+        f, s = oracle_sample(tokens, lin)
+        fl += f
+        sec += s
+    v = fl / sec / 1e12
+    sample = f"qkv linear (6144x4096) fprop+dgrad+wgrad on a {tokens}-token slab per step"
+    return {"metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (integer-exact block sums)",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD + " (token slab)", "tokens": tokens},
+            "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        out = reference_arm(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        if out is not None:
+            print(json.dumps(out))
+        return
+
+    rank, world, dist = dist_init()
+    out = gpu_arm(args, rank, world, dist)
+    if rank == 0:
+        if world == 1 and not args.skip_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline_leg()
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
