@@ -350,7 +350,7 @@ def cpu_baseline_leg():
     from mxfp4_precision_gemms_gb300 import synth
 
     oracle.lib()
-    tokens = 32
+    tokens = 256  # about 10-20 s of CPU work on a 16-core host
     fl, sec = oracle_sample(tokens, synth.LLAMA8B_LINEARS)
     return {"value": round(fl / sec / 1e12, 6), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"fprop+dgrad+wgrad of the four Llama linears on a {tokens}-token slab "
@@ -365,7 +365,7 @@ def reference_arm(args, rank, world):
     from mxfp4_precision_gemms_gb300 import synth
 
     oracle.lib()
-    tokens = 16
+    tokens = 32  # the transposed (Wgrad) copies quantise blocks of 32 tokens
     lin = synth.LLAMA8B_LINEARS[:1]
     for _ in range(args.warmup):
         oracle_sample(tokens, lin)
@@ -386,6 +386,31 @@ def reference_arm(args, rank, world):
             "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_case():
+    """Small case for ncu captures: the down-proj X quantiser (8192x14336 bf16, 235 MB,
+    row + transposed copies) and the gate/up Fprop GEMM (8192x14336x4096, bf16 out),
+    each launched twice (capture the second launch with -s 1 -c 1)."""
+    import torch
+
+    from mxfp4_precision_gemms_gb300 import binding as mx
+    from mxfp4_precision_gemms_gb300 import synth
+
+    torch.cuda.set_device(0)
+    RC = mx.LAYOUT_ROW | mx.LAYOUT_COLT
+    xd = mx.bf16_tensor(synth.activations(8192, 14336, 1))
+    for _ in range(2):
+        mx.rotate_quantize(xd, mx.HAD_16, mx.SCALE_FLOOR, RC)
+    x = mx.bf16_tensor(synth.activations(8192, 4096, 2))
+    w = mx.bf16_tensor(synth.weights(14336, 4096, 3))
+    xq = mx.rotate_quantize(x, mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW)["row"]
+    wq = mx.rotate_quantize(w, mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW)["row"]
+    for _ in range(2):
+        mx.gemm(xq, wq, mx.OUT_BF16)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    print("profile case ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,7 +419,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", action="store_true", help="run the small ncu case and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case()
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

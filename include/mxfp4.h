@@ -189,6 +189,13 @@ mxfp4_status mxfp4_device_status(mxfp4_stream_t stream);
  * thread (default 2e9 = 2 s; 0 restores the default). */
 void mxfp4_set_wait_limit_ns(uint64_t ns);
 
+/* Failure-detection test hook: the next `launches` mxfp4_gemm launches made by this
+ * host thread never load their first K stage, so the tensor-core issuer's bounded
+ * wait expires; the kernel records MXFP4_ERR_TIMEOUT (read with
+ * mxfp4_device_status), drains its copies, frees its TMEM and returns.  Its output
+ * is then invalid.  0 cancels.  Not for production use. */
+void mxfp4_test_inject_gemm_fault(int launches);
+
 const char* mxfp4_status_string(mxfp4_status status);
 /* Message for the last error returned on this host thread ("" if none). */
 const char* mxfp4_last_error(void);

@@ -75,6 +75,7 @@ def lib():
                 "mxfp4_linear_wgrad": ([T, T, CF, P, P, S, P], I),
                 "mxfp4_device_status": ([P], I),
                 "mxfp4_set_wait_limit_ns": ([ctypes.c_uint64], None),
+                "mxfp4_test_inject_gemm_fault": ([I], None),
                 "mxfp4_status_string": ([I], ctypes.c_char_p),
                 "mxfp4_last_error": ([], ctypes.c_char_p),
             }

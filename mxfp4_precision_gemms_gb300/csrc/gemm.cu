@@ -136,11 +136,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
 
     if (warp == 0) {
         if (elect_one()) {
-            int issued = 0;
+            uint32_t armed[STAGES];  // completed-or-pending phases armed per stage
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s) armed[s] = 0;
             for (int kt = 0; kt < num_k; ++kt) {
                 const int s = kt % STAGES;
                 const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
                 if (kt >= STAGES && !wait_bounded(&empty[s], ph ^ 1u, p.wait_ns, p.status)) break;
+                if (kt == 0 && p.test_drop_first_stage) continue;  // fault injection: never arrives
                 mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
                 tma_load_2d(sA + s * Cfg::A_STAGE, &p.map_a, &full[s], kt * BK_BYTES, (int32_t)m0);
                 tma_load_2d(sB + s * Cfg::B_STAGE, &p.map_b, &full[s], kt * BK_BYTES, (int32_t)n0);
@@ -150,11 +153,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
                 for (int j = 0; j < BN / 128; ++j)
                     bulk_load(sSFB + s * Cfg::SFB_STAGE + j * 1024,
                               p.sfb + ((n0 / 128 + j) * atoms_per_row_block + 2 * kt) * 512, 1024, &full[s]);
-                ++issued;
+                armed[s] = (uint32_t)(kt / STAGES) + 1u;
             }
-            // Drain: every copy this thread issued has landed before the CTA exits.
-            for (int kt = issued > STAGES ? issued - STAGES : 0; kt < issued; ++kt)
-                wait_bounded(&full[kt % STAGES], (uint32_t)(kt / STAGES) & 1u, p.wait_ns, p.status);
+            // Drain: every copy this thread issued has landed before the CTA exits
+            // (the last armed phase of each stage has completed).
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s)
+                if (armed[s]) wait_bounded(&full[s], (armed[s] - 1u) & 1u, p.wait_ns, p.status);
         }
     } else if (warp == 1) {
         if (elect_one()) {

@@ -46,6 +46,7 @@ struct GemmParams {
     int32_t accumulate;
     uint32_t* status;
     uint64_t wait_ns;
+    int32_t test_drop_first_stage;  // fault injection (tests only): stage 0 is never loaded
 };
 
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s);

@@ -20,6 +20,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 thread_local char t_last_error[512] = "";
 thread_local uint64_t t_wait_ns = 0;
+thread_local int t_inject_gemm_faults = 0;  // test hook: see mxfp4_test_inject_gemm_fault
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 std::mutex g_mu;
@@ -217,6 +218,8 @@ const char* mxfp4_last_error(void) { return t_last_error; }
 
 void mxfp4_set_wait_limit_ns(uint64_t ns) { t_wait_ns = ns; }
 
+void mxfp4_test_inject_gemm_fault(int launches) { t_inject_gemm_faults = launches > 0 ? launches : 0; }
+
 mxfp4_status mxfp4_device_status(mxfp4_stream_t stream) {
     int dev;
     mxfp4_status st = check_device(&dev);
@@ -337,6 +340,10 @@ mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, i
     p.accumulate = accumulate ? 1 : 0;
     p.status = device_status_ptr();
     p.wait_ns = wait_limit();
+    if (t_inject_gemm_faults > 0) {
+        --t_inject_gemm_faults;
+        p.test_drop_first_stage = 1;
+    }
     cudaError_t e = launch_gemm(p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return ok();
