@@ -180,6 +180,28 @@ mxfp4_status mxfp4_linear_dgrad(const void* dy, const mxfp4_tensor* wT, int64_t 
 mxfp4_status mxfp4_linear_wgrad(const mxfp4_tensor* dyT, const mxfp4_tensor* xT, const mxfp4_config* cfg,
                                 void* dw, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
 
+/* Fprop without caller-provided scratch.  The pages have no counterpart: this entry
+ * exists for callers that cannot allocate device memory -- a plugin inside a host
+ * framework whose allocator owns all device memory and passes it only input and
+ * output pointers, or a latency-critical loop that must not call cudaMalloc or
+ * cudaFree (they can synchronise the device).
+ * Same arguments, results and validation as mxfp4_linear_fprop, minus ws/ws_bytes:
+ * the quantised X and W live in a fixed 64 MiB scratch area inside the library
+ * (mxfp4_noalloc_scratch_bytes()), which every GPU running this library holds until
+ * the process exits.  Shapes whose mxfp4_workspace_bytes(MXFP4_OP_FPROP, ...) exceed
+ * it are rejected with MXFP4_ERR_WORKSPACE before anything is launched.
+ * The first call on a device looks up the scratch area's device address (a CUDA
+ * runtime query, no allocation); make that first call before any stream capture.
+ * All calls share the one area and it keeps the previous call's contents (every
+ * byte this path reads is rewritten first); calls that may overlap on the GPU (for
+ * example on two streams without ordering) race on it and must be serialised.
+ * Nothing here calls cudaMalloc, cudaFree or any allocating library routine. */
+mxfp4_status mxfp4_linear_fprop_noalloc(const void* x, const void* w, int64_t M, int64_t N, int64_t K,
+                                        const mxfp4_config* cfg, void* y, mxfp4_tensor* save_xT,
+                                        mxfp4_tensor* save_wT, mxfp4_stream_t stream);
+/* Size in bytes of the scratch area used by mxfp4_linear_fprop_noalloc. */
+size_t mxfp4_noalloc_scratch_bytes(void);
+
 /* Synchronises `stream`, then returns and clears the current device's status word:
  * MXFP4_OK, or MXFP4_ERR_TIMEOUT if a kernel's bounded wait expired since the last
  * call (that kernel returned early and its output is invalid). */

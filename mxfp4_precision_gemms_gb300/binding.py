@@ -73,6 +73,8 @@ def lib():
                 "mxfp4_linear_fprop": ([P, P, I64, I64, I64, CF, P, T, T, P, S, P], I),
                 "mxfp4_linear_dgrad": ([P, T, I64, I64, I64, CF, P, T, P, S, P], I),
                 "mxfp4_linear_wgrad": ([T, T, CF, P, P, S, P], I),
+                "mxfp4_linear_fprop_noalloc": ([P, P, I64, I64, I64, CF, P, T, T, P], I),
+                "mxfp4_noalloc_scratch_bytes": ([], S),
                 "mxfp4_device_status": ([P], I),
                 "mxfp4_set_wait_limit_ns": ([ctypes.c_uint64], None),
                 "mxfp4_test_inject_gemm_fault": ([I], None),

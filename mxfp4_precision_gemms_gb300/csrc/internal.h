@@ -53,6 +53,8 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s);
 
 // Host helpers implemented in mxfp4_api.cu.
 uint32_t* device_status_ptr();  // for the current device
+// Records the thread-local message returned by mxfp4_last_error() and returns st.
+mxfp4_status record_error(mxfp4_status st, const char* fmt, ...);
 bool encode_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t cols, uint32_t box_rows);
 
 }  // namespace mx

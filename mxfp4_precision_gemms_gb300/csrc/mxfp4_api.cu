@@ -104,6 +104,14 @@ bool valid_mode(int m) { return m == 0 || m == 1; }
 
 }  // namespace
 
+mxfp4_status record_error(mxfp4_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
 uint32_t* device_status_ptr() {
     int dev = 0;
     cudaGetDevice(&dev);
