@@ -5,13 +5,15 @@
 // The operands are the quantised copies of "Pretraining Large Language Models with
 // MXFP4 on Native FP4 Hardware" (C.1-C.3), already rotated along K.
 //
-// Structure (one 128 x BN output tile per CTA, 192 threads):
+// Structure (persistent: one CTA per SM walks 128 x BN output tiles, 192 threads):
 //   warp 0  TMA producer: 128x128-byte code tiles of A and B (128B swizzle) and the
 //           matching 1 KB scale-factor atoms, into a STAGES-deep shared-memory ring.
 //   warp 1  allocates TMEM; one elected thread copies each stage's scale factors
 //           SMEM->TMEM (tcgen05.cp) and issues 4 tcgen05.mma.kind::mxf4 (K = 64
 //           each) per 256-element stage into an fp32 TMEM accumulator.
-//   warps 2-5 epilogue: TMEM -> registers (tcgen05.ld) -> fp32/bf16 global stores.
+//   warps 2-5 epilogue: TMEM -> registers (tcgen05.ld) -> fp32/bf16 global stores;
+//           the accumulator is handed back to the MMA warp as soon as it has been
+//           read, so the next tile's MMAs overlap the last stores.
 // All waits are bounded; on expiry the status word records a timeout and the CTA
 // drains what it issued and exits.
 #include <cuda_bf16.h>
@@ -37,7 +39,7 @@ struct GemmCfg {
     static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
-    static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 1) * 8;
+    static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 3) * 8;
     static constexpr int SMEM = OFF_TMEM + 16 + 1024;  // + alignment slack
     static constexpr int TX_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
     static constexpr int SF_COLS = 8 + 8 * (BN / 128);  // TMEM columns of scales per stage
@@ -106,13 +108,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
     uint8_t* sSFB = smem + Cfg::OFF_SFB;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* empty = full + STAGES;
-    uint64_t* tmem_full = empty + STAGES;
+    uint64_t* acc_full = empty + STAGES;   // MMA -> epilogue: accumulator holds a finished tile
+    uint64_t* acc_empty = acc_full + 1;    // epilogue -> MMA: accumulator has been read out
+    uint64_t* mma_done = acc_empty + 1;    // every MMA issued by this CTA has completed
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_TMEM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)blockIdx.y * BM;
-    const int64_t n0 = (int64_t)blockIdx.x * BN;
     const int num_k = (int)((p.K + 255) / 256);
+    const int64_t num_n = (p.N + BN - 1) / BN;
+    const int64_t num_tiles = ((p.M + BM - 1) / BM) * num_n;
     const int64_t atoms_per_row_block = p.kb_pad / 4;
 
     if (threadIdx.x == 0) {
@@ -120,7 +124,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(tmem_full, 1);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);  // one arrive per epilogue warp
+        mbar_init(mma_done, 1);
         fence_mbar_init();
         prefetch_tmap(&p.map_a);
         prefetch_tmap(&p.map_b);
@@ -135,78 +141,115 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
+        // ---------------- TMA producer
         if (elect_one()) {
-            uint32_t armed[STAGES];  // completed-or-pending phases armed per stage
+            uint32_t armed[STAGES];  // number of phases armed per stage
 #pragma unroll
             for (int s = 0; s < STAGES; ++s) armed[s] = 0;
-            for (int kt = 0; kt < num_k; ++kt) {
-                const int s = kt % STAGES;
-                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
-                if (kt >= STAGES && !wait_bounded(&empty[s], ph ^ 1u, p.wait_ns, p.status)) break;
-                if (kt == 0 && p.test_drop_first_stage) continue;  // fault injection: never arrives
-                mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
-                tma_load_2d(sA + s * Cfg::A_STAGE, &p.map_a, &full[s], kt * BK_BYTES, (int32_t)m0);
-                tma_load_2d(sB + s * Cfg::B_STAGE, &p.map_b, &full[s], kt * BK_BYTES, (int32_t)n0);
-                bulk_load(sSFA + s * Cfg::SFA_STAGE, p.sfa + ((m0 / 128) * atoms_per_row_block + 2 * kt) * 512, 1024,
-                          &full[s]);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int64_t m0 = (tile / num_n) * BM, n0 = (tile % num_n) * BN;
+                for (int kt = 0; kt < num_k; ++kt, ++it) {
+                    const int s = (int)(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (it >= STAGES && !wait_bounded(&empty[s], ph ^ 1u, p.wait_ns, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (it == 0 && p.test_drop_first_stage) continue;  // fault injection: never arrives
+                    mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
+                    tma_load_2d(sA + s * Cfg::A_STAGE, &p.map_a, &full[s], kt * BK_BYTES, (int32_t)m0);
 #pragma unroll
-                for (int j = 0; j < BN / 128; ++j)
-                    bulk_load(sSFB + s * Cfg::SFB_STAGE + j * 1024,
-                              p.sfb + ((n0 / 128 + j) * atoms_per_row_block + 2 * kt) * 512, 1024, &full[s]);
-                armed[s] = (uint32_t)(kt / STAGES) + 1u;
+                    for (int j = 0; j < BN / 128; ++j)  // the tensor map's box is 128 rows
+                        tma_load_2d(sB + s * Cfg::B_STAGE + j * (128 * BK_BYTES), &p.map_b, &full[s], kt * BK_BYTES,
+                                    (int32_t)(n0 + j * 128));
+                    bulk_load(sSFA + s * Cfg::SFA_STAGE, p.sfa + ((m0 / 128) * atoms_per_row_block + 2 * kt) * 512,
+                              1024, &full[s]);
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)
+                        bulk_load(sSFB + s * Cfg::SFB_STAGE + j * 1024,
+                                  p.sfb + ((n0 / 128 + j) * atoms_per_row_block + 2 * kt) * 512, 1024, &full[s]);
+                    armed[s] = it / STAGES + 1u;
+                }
             }
-            // Drain: every copy this thread issued has landed before the CTA exits
-            // (the last armed phase of each stage has completed).
+            // Drain: the last armed phase of every stage has landed before the CTA exits.
 #pragma unroll
             for (int s = 0; s < STAGES; ++s)
                 if (armed[s]) wait_bounded(&full[s], (armed[s] - 1u) & 1u, p.wait_ns, p.status);
         }
     } else if (warp == 1) {
+        // ---------------- tensor-core issuer
         if (elect_one()) {
             constexpr uint32_t idesc = idesc_mxf4(BM, BN);
-            for (int kt = 0; kt < num_k; ++kt) {
-                const int s = kt % STAGES;
-                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
-                if (!wait_bounded(&full[s], ph, p.wait_ns, p.status)) break;
-                tc_fence_after();
-                const uint32_t sfa_t = tmem_base + BN + s * Cfg::SF_COLS;
-                const uint32_t sfb_t = sfa_t + 8;
-#pragma unroll
-                for (int a = 0; a < 2; ++a)
-                    tc_cp_32x128b_warpx4(sfa_t + a * 4,
-                                         smem_desc(smem_u32(sSFA + s * Cfg::SFA_STAGE + a * 512), 0, 128, kSwizzleNone));
-#pragma unroll
-                for (int j = 0; j < BN / 128; ++j)
+            constexpr uint32_t SFB_KSTRIDE = 4 * (BN / 128);  // TMEM columns per 4-block group of B scales
+            uint32_t it = 0, tcount = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++tcount) {
+                if (tcount > 0) {
+                    if (!wait_bounded(acc_empty, (tcount - 1u) & 1u, p.wait_ns, p.status)) break;
+                    tc_fence_after();
+                }
+                for (int kt = 0; kt < num_k; ++kt, ++it) {
+                    const int s = (int)(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bounded(&full[s], ph, p.wait_ns, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem_base + BN + s * Cfg::SF_COLS;
+                    const uint32_t sfb_t = sfa_t + 8;
 #pragma unroll
                     for (int a = 0; a < 2; ++a)
                         tc_cp_32x128b_warpx4(
-                            sfb_t + j * 8 + a * 4,
-                            smem_desc(smem_u32(sSFB + s * Cfg::SFB_STAGE + j * 1024 + a * 512), 0, 128, kSwizzleNone));
-                const uint32_t a_base = smem_u32(sA + s * Cfg::A_STAGE);
-                const uint32_t b_base = smem_u32(sB + s * Cfg::B_STAGE);
+                            sfa_t + a * 4,
+                            smem_desc(smem_u32(sSFA + s * Cfg::SFA_STAGE + a * 512), 0, 128, kSwizzleNone));
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint64_t adesc = smem_desc(a_base + k * 32, 16, 1024, kSwizzle128B);
-                    const uint64_t bdesc = smem_desc(b_base + k * 32, 16, 1024, kSwizzle128B);
-                    const uint32_t sf_id = (uint32_t)(k & 1) * 2u;
-                    tc_mma_mxf4(tmem_base, adesc, bdesc, idesc_with_sf_ids(idesc, sf_id, sf_id), sfa_t + (k >> 1) * 4,
-                                sfb_t + (k >> 1) * 4, (kt | k) != 0);
+                    for (int j = 0; j < BN / 128; ++j)
+#pragma unroll
+                        for (int a = 0; a < 2; ++a)
+                            tc_cp_32x128b_warpx4(sfb_t + a * SFB_KSTRIDE + j * 4,
+                                                 smem_desc(smem_u32(sSFB + s * Cfg::SFB_STAGE + j * 1024 + a * 512),
+                                                           0, 128, kSwizzleNone));
+                    const uint32_t a_base = smem_u32(sA + s * Cfg::A_STAGE);
+                    const uint32_t b_base = smem_u32(sB + s * Cfg::B_STAGE);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t adesc = smem_desc(a_base + k * 32, 16, 1024, kSwizzle128B);
+                        const uint64_t bdesc = smem_desc(b_base + k * 32, 16, 1024, kSwizzle128B);
+                        const uint32_t sf_id = (uint32_t)(k & 1) * 2u;
+                        tc_mma_mxf4(tmem_base, adesc, bdesc, idesc_with_sf_ids(idesc, sf_id, sf_id),
+                                    sfa_t + (k >> 1) * 4, sfb_t + (k >> 1) * SFB_KSTRIDE, (kt | k) != 0);
+                    }
+                    tc_commit(&empty[s]);
                 }
-                tc_commit(&empty[s]);
+                if (ok) tc_commit(acc_full);
             }
-            tc_commit(tmem_full);
+            // Every MMA issued here has completed before TMEM is released.
+            tc_commit(mma_done);
+            wait_bounded(mma_done, 0, p.wait_ns, p.status);
         }
     } else {
-        // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its sub-partition)
+        // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
         const int q = warp & 3;
-        if (wait_bounded(tmem_full, 0, p.wait_ns, p.status)) {
+        uint32_t tcount = 0;
+        for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
+            if (!wait_bounded(acc_full, tcount & 1u, p.wait_ns, p.status)) break;
             tc_fence_after();
-            const int64_t row = m0 + q * 32 + lane;
+            const int64_t row = (tile / num_n) * BM + q * 32 + lane;
+            const int64_t n0 = (tile % num_n) * BN;
 #pragma unroll 1
             for (int j = 0; j < BN / 32; ++j) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * 32), v);
                 tmem_ld_wait();
+                if (j == BN / 32 - 1) {
+                    // accumulator fully read: hand it back before the last stores
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty);
+                }
                 store_row_chunk(p, row, n0 + j * 32, v);
             }
         }
@@ -225,21 +268,30 @@ cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
     using Cfg = GemmCfg<BN, STAGES>;
     auto kern = mxf4_gemm_kernel<BN, STAGES>;
     static bool configured[64] = {};
+    static int sm_count[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
         if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    const dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM));
+    const int64_t tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+    const unsigned grid = (unsigned)(tiles < sm_count[dev] ? tiles : sm_count[dev]);
     kern<<<grid, GEMM_THREADS, Cfg::SMEM, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s) { return launch_cfg<128, 6>(p, s); }
+// Persistent launch: one CTA per SM walks the 128 x BN output tiles; BN = 256 unless
+// the whole N fits in 128 columns.
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s) {
+    if (p.N <= 128) return launch_cfg<128, 6>(p, s);
+    return launch_cfg<256, 4>(p, s);
+}
 
 }  // namespace mx

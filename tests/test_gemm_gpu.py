@@ -37,15 +37,17 @@ def run(torch, qa, qb, out_dtype=0, accumulate=False, init=None):
     return C.float().cpu().numpy().astype(np.float64)
 
 
-def test_single_block_scales(torch):
+@pytest.mark.parametrize("N", [128, 256])
+def test_single_block_scales(torch, N):
     """K = 32: every output is 2^(ea+eb) * sum qa*qb; rows use distinct scales, so a
-    wrong scale-factor placement shows up as an exact power-of-two error."""
-    M, N, K = 128, 128, 32
+    wrong scale-factor placement shows up as an exact power-of-two error (N = 256 covers
+    the second 128-row group of B's scales in a 256-wide tile)."""
+    M, K = 128, 32
     g = np.random.default_rng(0)
     ca = g.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
     cb = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
     sa = (120 + (np.arange(M) % 13)).astype(np.uint8)[:, None]
-    sb = (124 + (np.arange(N) % 7)).astype(np.uint8)[:, None]
+    sb = (112 + (np.arange(N) % 29)).astype(np.uint8)[:, None]
     want, S = oracle.gemm(ca, sa, cb, sb)
     got = run(torch, (ca, sa), (cb, sb))
     assert_within(got, want, S, what="single block")
