@@ -127,6 +127,37 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# --------------------------------------------------------------------------- ncu traffic
+def kernel_sources_sha(files):
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "mxfp4_precision_gemms_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {"gemm": ("gemm.cu", "ptx.cuh", "internal.h"), "quant": ("quantize.cu", "ptx.cuh", "internal.h")}
+
+
+def measured_traffic():
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, averaged over
+    the kernel's launches in one ncu capture of this benchmark), kept in
+    profiles/traffic_llama8b_linears_T8192.json with the hash of the kernel sources it
+    was taken from; a kernel whose sources changed since reports null."""
+    path = os.path.join(ROOT, "profiles", "traffic_llama8b_linears_T8192.json")
+    out = {"gemm": None, "quant": None}
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return out
+    for k, files in KERNEL_SOURCES.items():
+        r = rec.get(k)
+        if r and r.get("sources_sha") == kernel_sources_sha(files):
+            out[k] = r.get("bytes_per_launch")
+    return out
+
+
 # --------------------------------------------------------------------------- GPU arm
 class Layer:
     def __init__(self, name, N, K, seed, dev):
@@ -268,11 +299,12 @@ def gpu_arm(args, rank, world, dist):
     gemm_tflops = g_fl / (g_ms * 1e-3) / 1e12 if g_ms else 0.0
     quant_gbs = q_by / (q_ms * 1e-3) / 1e9 if q_ms else 0.0
     gemm_share = g_ms / (g_ms + q_ms) if g_ms + q_ms else 0.0
+    traffic = measured_traffic()
     roof_gemm = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1),
-                 "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4), "traffic": None,
+                 "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4), "traffic": traffic["gemm"],
                  "kernel": "mxf4_gemm_kernel", "peak_source": "measured bf16 sustained x 6 (nominal fp4/bf16)"}
     roof_quant = {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": hbm, "unit": "GB/s",
-                  "frac": round(quant_gbs / hbm, 4), "traffic": None, "kernel": "rq_kernel",
+                  "frac": round(quant_gbs / hbm, 4), "traffic": traffic["quant"], "kernel": "rq_kernel",
                   "peak_source": "measured (hbm_gbs)"}
     dominant = roof_gemm if gemm_share >= 0.5 else roof_quant
 
@@ -411,6 +443,38 @@ def profile_case():
     print("profile case ok")
 
 
+def write_traffic(csv_path):
+    """Averages dram__bytes_read.sum + dram__bytes_write.sum per launch of each kernel
+    from an ncu --csv capture of this benchmark and records it with the source hashes."""
+    import csv
+
+    per = {"gemm": [], "quant": []}
+    rows = [r for r in csv.reader(open(csv_path)) if r]
+    hdr = next(r for r in rows if r[0] == "ID")
+    launches = {}
+    for r in rows:
+        if len(r) != len(hdr) or r[0] == "ID":
+            continue
+        d = dict(zip(hdr, r))
+        if d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}[d["Metric Unit"]]
+        launches.setdefault((d["ID"], d["Kernel Name"]), 0.0)
+        launches[(d["ID"], d["Kernel Name"])] += float(d["Metric Value"].replace(",", "")) * scale
+    for (_, name), b in launches.items():
+        if "mxf4_gemm" in name:
+            per["gemm"].append(b)
+        elif "rq_" in name:
+            per["quant"].append(b)
+    rec = {k: {"bytes_per_launch": round(sum(v) / len(v)), "launches": len(v),
+               "sources_sha": kernel_sources_sha(KERNEL_SOURCES[k])} for k, v in per.items() if v}
+    rec["command"] = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none --csv "
+                      "--log-file <csv> python bench.py --steps 1 --warmup 3 --skip-e2e --skip-cpu-baseline")
+    path = os.path.join(ROOT, "profiles", "traffic_llama8b_linears_T8192.json")
+    json.dump(rec, open(path, "w"), indent=1)
+    print(json.dumps(rec))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,9 +484,14 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", action="store_true", help="run the small ncu case and exit")
+    ap.add_argument("--traffic-from", metavar="CSV", help="turn an ncu CSV of dram bytes for this benchmark "
+                    "into profiles/traffic_llama8b_linears_T8192.json and exit")
     args = ap.parse_args()
     if args.profile_case:
         profile_case()
+        return
+    if args.traffic_from:
+        write_traffic(args.traffic_from)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -132,6 +132,22 @@ bool encode_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D tensor map over a bf16 matrix [rows, cols] (leading dimension ld elements): box
+// = 64 columns (128 bytes) x 128 rows, 128-byte swizzle, zero fill out of bounds.
+bool encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint64_t quant_wait_ns() { return wait_limit(); }
+
 }  // namespace mx
 
 using namespace mx;
@@ -279,7 +295,7 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
     if (ld < cols || ld % 8)
         return fail(MXFP4_ERR_MISALIGNED, "ld (%lld) must be >= cols and a multiple of 8", (long long)ld);
     if (!aligned16(x)) return fail(MXFP4_ERR_MISALIGNED, "x not 16-byte aligned");
-    if ((rows + 63) / 64 > 65535) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "too many rows");
+    if ((rows + 127) / 128 > 65535) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "too many rows");
     mxfp4_status st;
     if (want_row && (st = check_out(row_out, "row_out", true))) return st;
     if (want_colT && (st = check_out(colT_out, "colT_out", true))) return st;
