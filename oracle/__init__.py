@@ -69,6 +69,7 @@ def lib():
             L.oracle_dequant_row.argtypes = [P, P, I64, I64, P]
             L.oracle_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, P]
             L.oracle_dot_pairs.argtypes = [P, P, P, P, I64, I64, P, P]
+            L.oracle_error_decomposition.argtypes = [P, I64, I64, I64, I, I, P]
             L.oracle_num_threads.restype = I
             L.oracle_set_num_threads.argtypes = [I]
             _lib = L
@@ -256,3 +257,16 @@ def wgrad_sample(dy, x, had, mode, rows, cols):
     qb = [quantize_vec(np.ascontiguousarray(x[:, k]), had, mode) for k in cols]
     return dot_pairs(np.stack([q[0] for q in qa]), np.stack([q[1] for q in qa]),
                      np.stack([q[0] for q in qb]), np.stack([q[1] for q in qb]))
+
+
+# --------------------------------------------------------------------------- error decomposition
+def error_decomposition(x_bf16, had, mode):
+    """Sums over a row-quantised [R, C] tensor of the three error components of the
+    MXFP4 error ("Decomposing MXFP4 quantization error ...", core insight):
+    dict with e2, scale2, dz2, grid2, scale_grid, n_deadzone, n (fp64 sums)."""
+    x = _u16(x_bf16)
+    R, C = x.shape
+    out = np.zeros(7, np.float64)
+    lib().oracle_error_decomposition(_p(x), R, C, C, had, mode, _p(out))
+    keys = ("e2", "scale2", "dz2", "grid2", "scale_grid", "n_deadzone", "n")
+    return dict(zip(keys, out.tolist()))

@@ -354,3 +354,60 @@ void oracle_set_num_threads(int n) {
     (void)n;
 #endif
 }
+
+/* ------------------------------------------------------------------------- */
+/* Error decomposition ([DECOMP] "core insight", property 1)                 */
+/* ------------------------------------------------------------------------- */
+
+/* Round |u| (a real number, given in fp64) to the E2M1 grid with the same rule as
+ * oracle_e2m1_code; returns the signed grid value. */
+static double grid_round(double u) { return oracle_e2m1_value(oracle_e2m1_code(u)); }
+
+/* For x [R, C] (bf16, ld elements per row), quantised row-wise (rotation along C):
+ * per 32-block, with the E8M0 scale s_b of `mode` and the ideal scale s* = amax/6,
+ *   Q(x)  = s_b * grid(x / s_b)          (the MXFP4 value)
+ *   Q*(x) = s*  * grid(x / s*)           (ideal-scale quantiser)
+ *   e_scale = Q - Q*, e_DZ = (Q* - x) on the deadzone |x| < amax/24, e_grid = (Q* - x) off it.
+ * out[0..6] = sum e^2, sum e_scale^2, sum e_DZ^2, sum e_grid^2, sum e_scale*e_grid,
+ *             number of deadzone elements, number of elements (all in fp64). */
+void oracle_error_decomposition(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                                double* out) {
+    double acc[7] = {0, 0, 0, 0, 0, 0, 0};
+#pragma omp parallel
+    {
+        double loc[7] = {0, 0, 0, 0, 0, 0, 0};
+        float* xf = (float*)malloc(sizeof(float) * (size_t)C);
+        float* v = (float*)malloc(sizeof(float) * (size_t)C);
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < R; ++r) {
+            for (int64_t c = 0; c < C; ++c) xf[c] = bf16_to_float(x[r * ld + c]);
+            oracle_rotate_f32(xf, C, had, v);
+            for (int64_t b = 0; b < C / 32; ++b) {
+                const float* blk = v + b * 32;
+                float amax_f = block_amax(blk, 32);
+                int e = oracle_shared_exponent(amax_f, mode);
+                double amax = (double)amax_f;
+                double sstar = amax / 6.0;
+                for (int i = 0; i < 32; ++i) {
+                    double xv = (double)blk[i];
+                    double q = ldexp(grid_round(ldexp(xv, -e)), e);
+                    double qs = sstar > 0.0 ? sstar * grid_round(xv / sstar) : 0.0;
+                    int dz = fabs(xv) < amax / 24.0;
+                    double es = q - qs, ed = dz ? qs - xv : 0.0, eg = dz ? 0.0 : qs - xv, et = q - xv;
+                    loc[0] += et * et;
+                    loc[1] += es * es;
+                    loc[2] += ed * ed;
+                    loc[3] += eg * eg;
+                    loc[4] += es * eg;
+                    loc[5] += dz;
+                    loc[6] += 1.0;
+                }
+            }
+        }
+#pragma omp critical
+        for (int k = 0; k < 7; ++k) acc[k] += loc[k];
+        free(xf);
+        free(v);
+    }
+    for (int k = 0; k < 7; ++k) out[k] = acc[k];
+}

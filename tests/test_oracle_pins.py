@@ -431,3 +431,41 @@ def test_linear_close_to_exact(oracle_mod):
         for k in got:
             rel = np.linalg.norm(got[k] - exact[k]) / np.linalg.norm(exact[k])
             assert rel < 0.35, (had, k, rel)
+
+
+# ---------------------------------------------------------------- error decomposition sums
+
+
+def test_error_decomposition_sums_match_exact_rationals(oracle_mod):
+    """The fp64 sums of the oracle's decomposition equal the exact rational sums of the
+    component definitions (computed here from the oracle's codes with Fractions), and
+    satisfy the MSE identity with one cross term under the ceiling scale."""
+    g = np.random.default_rng(11)
+    blk = (g.standard_t(3, size=(4, 64)) * 0.3).astype(np.float32)
+    blk[0, 3] *= 40
+    xb = synth.bf16_bits(blk)
+    d = oracle_mod.error_decomposition(xb, 1, 1)
+    tot = {"e2": 0, "scale2": 0, "dz2": 0, "grid2": 0, "scale_grid": 0, "n_deadzone": 0}
+    for r in range(4):
+        for b in range(2):
+            es, edz, eg, e = _decompose(oracle_mod, np.ascontiguousarray(xb[r, 32 * b:32 * b + 32]), 1)
+            tot["e2"] += _dot(e, e)
+            tot["scale2"] += _dot(es, es)
+            tot["dz2"] += _dot(edz, edz)
+            tot["grid2"] += _dot(eg, eg)
+            tot["scale_grid"] += _dot(es, eg)
+            amax = max(abs(Fraction(float(v))) for v in synth.bf16_to_f32(xb[r, 32 * b:32 * b + 32]))
+            tot["n_deadzone"] += sum(abs(Fraction(float(v))) < amax / 24 for v in synth.bf16_to_f32(xb[r, 32 * b:32 * b + 32]))
+    for k, v in tot.items():
+        assert abs(d[k] - float(v)) <= 1e-12 * max(1.0, abs(float(v))), (k, d[k], float(v))
+    assert d["n"] == 256
+    assert abs(d["e2"] - (d["scale2"] + d["dz2"] + d["grid2"] + 2 * d["scale_grid"])) <= 1e-12 * d["e2"]
+
+
+def test_error_decomposition_h16_reduces_error_on_outliers(oracle_mod):
+    """Reported, not a pin of the pages' numbers: on outlier-heavy activations the
+    rotation lowers the total MXFP4 error."""
+    X = synth.activations(256, 512, 0)
+    none = oracle_mod.error_decomposition(X, 1, 1)
+    h16 = oracle_mod.error_decomposition(X, 16, 1)
+    assert h16["e2"] < none["e2"]
