@@ -5,15 +5,15 @@
 // The operands are the quantised copies of "Pretraining Large Language Models with
 // MXFP4 on Native FP4 Hardware" (C.1-C.3), already rotated along K.
 //
-// Structure (persistent: one CTA per SM walks 128 x BN output tiles, 192 threads):
+// Structure (persistent: one CTA per SM walks 128 x BN output tiles, 320 threads):
 //   warp 0  TMA producer: 128x128-byte code tiles of A and B (128B swizzle) and the
 //           matching 1 KB scale-factor atoms, into a STAGES-deep shared-memory ring.
 //   warp 1  allocates TMEM; one elected thread copies each stage's scale factors
 //           SMEM->TMEM (tcgen05.cp) and issues 4 tcgen05.mma.kind::mxf4 (K = 64
 //           each) per 256-element stage into an fp32 TMEM accumulator.
-//   warps 2-5 epilogue: TMEM -> registers (tcgen05.ld) -> fp32/bf16 global stores;
+//   warps 2-9 epilogue: TMEM -> registers (tcgen05.ld) -> fp32/bf16 global stores;
 //           the accumulator is handed back to the MMA warp as soon as it has been
-//           read, so the next tile's MMAs overlap the last stores.
+//           read, so the next tile's MMAs overlap the stores.
 // All waits are bounded; on expiry the status word records a timeout and the CTA
 // drains what it issued and exits.
 #include <cuda_bf16.h>
@@ -24,9 +24,17 @@
 namespace mx {
 namespace {
 
+// Tuning knob (compile-time): pipeline depth of the 256-wide tiles.
+#ifndef MXG_STAGES_256
+#define MXG_STAGES_256 4
+#endif
+
 constexpr int BM = 128;
 constexpr int BK_BYTES = 128;  // 256 E2M1 elements per stage
-constexpr int GEMM_THREADS = 192;
+constexpr int EPI_WARPS = 8;  // two per TMEM lane quadrant, each owning half the columns
+constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int STG_PITCH = 80;                      // bytes per staged row: 64 B of data + 16 B pad
+constexpr int STG_WARP_BYTES = 32 * STG_PITCH;     // one warp's staging: 32 rows x 64 B
 
 template <int BN, int STAGES>
 struct GemmCfg {
@@ -40,7 +48,8 @@ struct GemmCfg {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
     static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 3) * 8;
-    static constexpr int SMEM = OFF_TMEM + 16 + 1024;  // + alignment slack
+    static constexpr int OFF_STG = (OFF_TMEM + 16 + 127) / 128 * 128;  // epilogue staging (16-byte vector access)
+    static constexpr int SMEM = OFF_STG + EPI_WARPS * STG_WARP_BYTES + 1024;  // + alignment slack
     static constexpr int TX_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
     static constexpr int SF_COLS = 8 + 8 * (BN / 128);  // TMEM columns of scales per stage
     static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
@@ -48,52 +57,68 @@ struct GemmCfg {
                                    : TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(OFF_STG % 16 == 0 && STG_PITCH % 16 == 0, "staging rows are accessed as 16-byte vectors");
+    static_assert(OFF_BAR % 8 == 0 && OFF_A % 1024 == 0 && OFF_B % 1024 == 0, "barrier / swizzle-atom alignment");
 };
 
-__device__ __forceinline__ void store_row_chunk(const GemmParams& p, int64_t row, int64_t col, const uint32_t (&v)[32]) {
-    if (row >= p.M) return;
-    const int64_t n_left = p.N - col;
-    if (n_left <= 0) return;
-    if (!p.out_bf16) {
-        float* dst = reinterpret_cast<float*>(p.C) + row * p.ldc + col;
-        if (n_left >= 32) {
+// Writes 64 bytes per row for the 32 rows of one epilogue warp (lane i holds row
+// row_base + i): the rows are staged in shared memory and written back with four
+// lanes per row, so each store instruction covers 8 rows x 64 contiguous bytes
+// instead of 32 scattered 16-byte pieces.  esz is the output element size (2 or 4).
+__device__ __forceinline__ void stage_and_store(const GemmParams& p, uint8_t* stg, int lane, int64_t row_base,
+                                                int64_t col0, const uint32_t* w, int esz) {
+    __syncwarp();
+    uint4* mine = reinterpret_cast<uint4*>(stg + lane * STG_PITCH);
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                float4 o = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
-                                       __uint_as_float(v[i + 3]));
-                if (p.accumulate) {
-                    const float4 c = *reinterpret_cast<const float4*>(dst + i);
-                    o.x += c.x;
-                    o.y += c.y;
-                    o.z += c.z;
-                    o.w += c.w;
-                }
-                *reinterpret_cast<float4*>(dst + i) = o;
+    for (int c = 0; c < 4; ++c) mine[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    __syncwarp();
+    const int epc = 16 / esz;  // elements per 16-byte piece
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int r = it * 8 + (lane >> 2), c = lane & 3;
+        const int64_t grow = row_base + r;
+        const int64_t gcol = col0 + c * epc;
+        if (grow >= p.M || gcol >= p.N) continue;
+        const uint4 val = *reinterpret_cast<const uint4*>(stg + r * STG_PITCH + c * 16);
+        uint8_t* dst = reinterpret_cast<uint8_t*>(p.C) + (grow * p.ldc + gcol) * esz;
+        if (gcol + epc <= p.N) {
+            if (p.accumulate) {  // fp32 only
+                const float4 o = *reinterpret_cast<const float4*>(dst);
+                *reinterpret_cast<float4*>(dst) =
+                    make_float4(o.x + __uint_as_float(val.x), o.y + __uint_as_float(val.y),
+                                o.z + __uint_as_float(val.z), o.w + __uint_as_float(val.w));
+            } else {
+                *reinterpret_cast<uint4*>(dst) = val;
             }
         } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i < n_left) dst[i] = (p.accumulate ? dst[i] : 0.0f) + __uint_as_float(v[i]);
+            const uint32_t vw[4] = {val.x, val.y, val.z, val.w};
+            for (int e = 0; e < p.N - gcol; ++e) {
+                if (esz == 4) {
+                    float* d = reinterpret_cast<float*>(dst) + e;
+                    *d = (p.accumulate ? *d : 0.0f) + __uint_as_float(vw[e]);
+                } else {
+                    const uint32_t hw = (vw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+                    reinterpret_cast<uint16_t*>(dst)[e] = (uint16_t)hw;
+                }
+            }
         }
+    }
+}
+
+// One TMEM chunk (32 fp32 columns of this lane's row) -> bf16 or fp32 global output.
+__device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stg, int lane, int64_t row_base,
+                                           int64_t col0, const uint32_t (&v)[32]) {
+    if (p.out_bf16) {
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            w[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        stage_and_store(p, stg, lane, row_base, col0, w, 2);
     } else {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + row * p.ldc + col;
-        if (n_left >= 32) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const __nv_bfloat162 h =
-                        __floats2bfloat162_rn(__uint_as_float(v[i + 2 * j]), __uint_as_float(v[i + 2 * j + 1]));
-                    w[j] = *reinterpret_cast<const uint32_t*>(&h);
-                }
-                *reinterpret_cast<uint4*>(dst + i) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i < n_left) dst[i] = __float2bfloat16_rn(__uint_as_float(v[i]));
-        }
+        stage_and_store(p, stg, lane, row_base, col0, v, 4);
+        stage_and_store(p, stg, lane, row_base, col0 + 16, v + 16, 4);
     }
 }
 
@@ -125,7 +150,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);  // one arrive per epilogue warp
+        mbar_init(acc_empty, EPI_WARPS);  // one arrive per epilogue warp
         mbar_init(mma_done, 1);
         fence_mbar_init();
         prefetch_tmap(&p.map_a);
@@ -231,27 +256,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
             wait_bounded(mma_done, 0, p.wait_ns, p.status);
         }
     } else {
-        // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4) .. +31
+        // ---------------- epilogue: warp w may only read TMEM lanes 32*(w%4) .. +31; the
+        // two warps of each lane quadrant split the columns in halves.  Each thread
+        // pulls its whole slice out of TMEM (one wait), hands the accumulator back to
+        // the MMA warp, and only then stores, so the stores overlap the next tile.
         const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        uint8_t* stg = smem + Cfg::OFF_STG + (warp - 2) * STG_WARP_BYTES;
+        constexpr int CH = BN / 2 / 32;  // 32-column chunks per thread
         uint32_t tcount = 0;
         for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
             if (!wait_bounded(acc_full, tcount & 1u, p.wait_ns, p.status)) break;
             tc_fence_after();
-            const int64_t row = (tile / num_n) * BM + q * 32 + lane;
-            const int64_t n0 = (tile % num_n) * BN;
-#pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * 32), v);
-                tmem_ld_wait();
-                if (j == BN / 32 - 1) {
-                    // accumulator fully read: hand it back before the last stores
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(acc_empty);
-                }
-                store_row_chunk(p, row, n0 + j * 32, v);
-            }
+            const int64_t row_base = (tile / num_n) * BM + q * 32;
+            const int64_t c0 = (tile % num_n) * BN + h * (BN / 2);
+            uint32_t v[CH][32];
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (BN / 2) + c * 32), v[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+#pragma unroll
+            for (int c = 0; c < CH; ++c) store_chunk(p, stg, lane, row_base, c0 + c * 32, v[c]);
         }
     }
 
@@ -291,7 +319,11 @@ cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
 // the whole N fits in 128 columns.
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s) {
     if (p.N <= 128) return launch_cfg<128, 6>(p, s);
-    return launch_cfg<256, 4>(p, s);
+#ifdef MXG_FORCE_BN128
+    return launch_cfg<128, 6>(p, s);
+#else
+    return launch_cfg<256, MXG_STAGES_256>(p, s);
+#endif
 }
 
 }  // namespace mx
