@@ -220,23 +220,42 @@ def run_step(layers, ev=None):
 LAUNCHES_PER_LAYER = 6  # 3 rotate+quantise + 3 GEMM kernels
 
 
-def run_e2e_step(layers, ws):
+def run_e2e_step(layers, ws, streams):
     """The same step through the public linear-layer API with host buffers: H2D of
-    X, W, dY from pinned memory, fprop/dgrad/wgrad, D2H of Y, dX, dW."""
+    X, W, dY from pinned memory, fprop/dgrad/wgrad, D2H of Y, dX, dW.  Three streams
+    (copy-in, compute, copy-out) ordered per layer by events, so layer i+1's inputs
+    upload and layer i-1's outputs download while layer i computes."""
+    import torch
+
     from mxfp4_precision_gemms_gb300 import binding as mx
 
+    s_in, s_comp, s_out = streams
     cfg = mx.Config(had=mx.HAD_16, mode=mx.SCALE_FLOOR, out_dtype=mx.OUT_BF16)
     wcfg = mx.Config(had=mx.HAD_16, mode=mx.SCALE_FLOOR, out_dtype=mx.OUT_F32)
+    start = torch.cuda.current_stream()
+    for st in streams:
+        st.wait_stream(start)
     for L in layers:
-        L.x.copy_(L.host["x"], non_blocking=True)
-        L.w.copy_(L.host["w"], non_blocking=True)
-        L.dy.copy_(L.host["dy"], non_blocking=True)
-        mx.linear_fprop(L.x, L.w, cfg, y=L.y, xT=L.xT, wT=L.wT, ws=ws)
-        mx.linear_dgrad(L.dy, L.wT, cfg, dx=L.dx, dyT=L.dyT, ws=ws)
-        mx.linear_wgrad(L.dyT, L.xT, wcfg, dw=L.dw)
-        L.out_host["y"].copy_(L.y, non_blocking=True)
-        L.out_host["dx"].copy_(L.dx, non_blocking=True)
-        L.out_host["dw"].copy_(L.dw, non_blocking=True)
+        with torch.cuda.stream(s_in):
+            L.x.copy_(L.host["x"], non_blocking=True)
+            L.w.copy_(L.host["w"], non_blocking=True)
+            L.dy.copy_(L.host["dy"], non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+        s_comp.wait_event(ev_in)
+        with torch.cuda.stream(s_comp):
+            mx.linear_fprop(L.x, L.w, cfg, y=L.y, xT=L.xT, wT=L.wT, ws=ws, stream=s_comp)
+            mx.linear_dgrad(L.dy, L.wT, cfg, dx=L.dx, dyT=L.dyT, ws=ws, stream=s_comp)
+            mx.linear_wgrad(L.dyT, L.xT, wcfg, dw=L.dw, stream=s_comp)
+            ev_c = torch.cuda.Event()
+            ev_c.record(s_comp)
+        s_out.wait_event(ev_c)
+        with torch.cuda.stream(s_out):
+            L.out_host["y"].copy_(L.y, non_blocking=True)
+            L.out_host["dx"].copy_(L.dx, non_blocking=True)
+            L.out_host["dw"].copy_(L.dw, non_blocking=True)
+    for st in streams:
+        start.wait_stream(st)
 
 
 def gpu_arm(args, rank, world, dist):
@@ -316,8 +335,9 @@ def gpu_arm(args, rank, world, dist):
             L.out_host = {"y": torch.empty(L.y.shape, dtype=L.y.dtype).pin_memory(),
                           "dx": torch.empty(L.dx.shape, dtype=L.dx.dtype).pin_memory(),
                           "dw": torch.empty(L.dw.shape, dtype=L.dw.dtype).pin_memory()}
+        streams = (torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream())
         for _ in range(max(1, args.warmup)):
-            run_e2e_step(layers, ws)
+            run_e2e_step(layers, ws, streams)
         torch.cuda.synchronize()
         e2e_ms = []
         barrier(dist)
@@ -325,7 +345,7 @@ def gpu_arm(args, rank, world, dist):
             flush.fill_(1.0)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            run_e2e_step(layers, ws)
+            run_e2e_step(layers, ws, streams)
             b.record()
             b.synchronize()
             e2e_ms.append(a.elapsed_time(b))
@@ -335,6 +355,12 @@ def gpu_arm(args, rank, world, dist):
         e2e = {"value": round(world * fl * args.steps / (tot * 1e-3) / 1e12, 2), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(tot / args.steps, 3)}
         assert mx.device_status() == 0
+
+    fp8 = None
+    if not args.skip_fp8:
+        fp8 = fp8_comparator(layers, flush, args.steps, args.warmup)
+        if fp8 is not None:
+            fp8["mxfp4_step_speedup"] = round(fp8["ms_per_step"] / ms_per_step, 3)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -354,125 +380,86 @@ def gpu_arm(args, rank, world, dist):
         "gpu_launches": args.steps * LAUNCHES_PER_LAYER * len(layers),
         "clocks": clk.summary(),
         "device_status": status,
+        "fp8_comparator": fp8,
     }
     return out
 
 
-# --------------------------------------------------------------------------- oracle (CPU)
-def oracle_sample(tokens: int, linears):
-    """fprop + dgrad + wgrad of the given linears restricted to a `tokens`-row slab, on
-    the CPU oracle.  Returns (flops, seconds)."""
-    import oracle
-    from mxfp4_precision_gemms_gb300 import synth
-
-    fl, sec = 0, 0.0
-    for i, (_, N, K) in enumerate(linears):
-        X, W, dY = synth.linear_inputs(tokens, N, K, 2000 + 10 * i)
-        t = time.perf_counter()
-        oracle.fprop(X, W, 16, 0)
-        oracle.dgrad(dY, W, 16, 0)
-        oracle.wgrad(dY, X, 16, 0)
-        sec += time.perf_counter() - t
-        fl += 3 * 2 * tokens * N * K
-    return fl, sec
-
-
-def cpu_baseline_leg():
-    import oracle
-    from mxfp4_precision_gemms_gb300 import synth
-
-    oracle.lib()
-    tokens = 256  # about 10-20 s of CPU work on a 16-core host
-    fl, sec = oracle_sample(tokens, synth.LLAMA8B_LINEARS)
-    return {"value": round(fl / sec / 1e12, 6), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"fprop+dgrad+wgrad of the four Llama linears on a {tokens}-token slab "
-                      f"({fl / 1e9:.1f} GFLOP, {sec:.1f} s)"}
-
-
-def reference_arm(args, rank, world):
-    """The CPU oracle as the reference arm, on a bounded slab of the same workload."""
-    if rank != 0:
-        return None
-    import oracle
-    from mxfp4_precision_gemms_gb300 import synth
-
-    oracle.lib()
-    tokens = 32  # the transposed (Wgrad) copies quantise blocks of 32 tokens
-    lin = synth.LLAMA8B_LINEARS[:1]
-    for _ in range(args.warmup):
-        oracle_sample(tokens, lin)
-    fl = sec = 0
-    for _ in range(args.steps):
-        f, s = oracle_sample(tokens, lin)
-        fl += f
-        sec += s
-    v = fl / sec / 1e12
-    sample = f"qkv linear (6144x4096) fprop+dgrad+wgrad on a {tokens}-token slab per step"
-    return {"metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 2), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (integer-exact block sums)",
-            "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD + " (token slab)", "tokens": tokens},
-            "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-
-
-def profile_case():
-    """Small case for ncu captures: the down-proj X quantiser (8192x14336 bf16, 235 MB,
-    row + transposed copies) and the gate/up Fprop GEMM (8192x14336x4096, bf16 out),
-    each launched twice (capture the second launch with -s 1 -c 1)."""
+def fp8_comparator(layers, flush, steps, warmup):
+    """The same linear step with a library FP8 GEMM (torch._scaled_mm, per-tensor E4M3
+    scales, bf16 out; fp32-out Wgrad): the FP8 baseline the pages compare MXFP4 against.
+    Measurement only -- it is not a code path of this library."""
     import torch
 
-    from mxfp4_precision_gemms_gb300 import binding as mx
-    from mxfp4_precision_gemms_gb300 import synth
+    if not hasattr(torch, "_scaled_mm"):
+        return None
+    e4m3 = torch.float8_e4m3fn
+    fmax = torch.finfo(e4m3).max
 
-    torch.cuda.set_device(0)
-    RC = mx.LAYOUT_ROW | mx.LAYOUT_COLT
-    xd = mx.bf16_tensor(synth.activations(8192, 14336, 1))
-    for _ in range(2):
-        mx.rotate_quantize(xd, mx.HAD_16, mx.SCALE_FLOOR, RC)
-    x = mx.bf16_tensor(synth.activations(8192, 4096, 2))
-    w = mx.bf16_tensor(synth.weights(14336, 4096, 3))
-    xq = mx.rotate_quantize(x, mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW)["row"]
-    wq = mx.rotate_quantize(w, mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW)["row"]
-    for _ in range(2):
-        mx.gemm(xq, wq, mx.OUT_BF16)
-    torch.cuda.synchronize()
-    assert mx.device_status() == 0
-    print("profile case ok")
+    def q(t):
+        s = (t.abs().amax().float() / fmax).clamp(min=1e-30)
+        return (t.float() / s).to(e4m3), s
 
+    def step():
+        for L in layers:
+            xq, sx = q(L.x)
+            wq, sw = q(L.w)
+            dyq, sdy = q(L.dy)
+            torch._scaled_mm(xq, wq.t(), scale_a=sx, scale_b=sw, out_dtype=torch.bfloat16)
+            wtq = wq.t().contiguous()  # W^T [K, N] row-major for dX = dY W
+            torch._scaled_mm(dyq, wtq.t(), scale_a=sdy, scale_b=sw, out_dtype=torch.bfloat16)
+            dytq, xtq = dyq.t().contiguous(), xq.t().contiguous()  # dW = dY^T X
+            torch._scaled_mm(dytq, xtq.t(), scale_a=sdy, scale_b=sx, out_dtype=torch.float32)
 
-def write_traffic(csv_path):
-    """Averages dram__bytes_read.sum + dram__bytes_write.sum per launch of each kernel
-    from an ncu --csv capture of this benchmark and records it with the source hashes."""
-    import csv
+    try:
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(steps):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            step()
+            b.record()
+            b.synchronize()
+            tot += a.elapsed_time(b)
+    except Exception as e:  # a torch build without FP8 GEMMs for this GPU
+        return {"unavailable": str(e).splitlines()[0][:200]}
+    ms = tot / steps
 
-    per = {"gemm": [], "quant": []}
-    rows = [r for r in csv.reader(open(csv_path)) if r]
-    hdr = next(r for r in rows if r[0] == "ID")
-    launches = {}
-    for r in rows:
-        if len(r) != len(hdr) or r[0] == "ID":
-            continue
-        d = dict(zip(hdr, r))
-        if d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
-            continue
-        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}[d["Metric Unit"]]
-        launches.setdefault((d["ID"], d["Kernel Name"]), 0.0)
-        launches[(d["ID"], d["Kernel Name"])] += float(d["Metric Value"].replace(",", "")) * scale
-    for (_, name), b in launches.items():
-        if "mxf4_gemm" in name:
-            per["gemm"].append(b)
-        elif "rq_" in name:
-            per["quant"].append(b)
-    rec = {k: {"bytes_per_launch": round(sum(v) / len(v)), "launches": len(v),
-               "sources_sha": kernel_sources_sha(KERNEL_SOURCES[k])} for k, v in per.items() if v}
-    rec["command"] = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none --csv "
-                      "--log-file <csv> python bench.py --steps 1 --warmup 3 --skip-e2e --skip-cpu-baseline")
-    path = os.path.join(ROOT, "profiles", "traffic_llama8b_linears_T8192.json")
-    json.dump(rec, open(path, "w"), indent=1)
-    print(json.dumps(rec))
+    # the FP8 GEMMs alone, operands quantised beforehand
+    pre = []
+    for L in layers:
+        xq, sx = q(L.x)
+        wq, sw = q(L.w)
+        dyq, sdy = q(L.dy)
+        pre.append((xq, sx, wq, sw, wq.t().contiguous(), dyq, sdy, dyq.t().contiguous(), xq.t().contiguous()))
+
+    def gemms():
+        for xq, sx, wq, sw, wtq, dyq, sdy, dytq, xtq in pre:
+            torch._scaled_mm(xq, wq.t(), scale_a=sx, scale_b=sw, out_dtype=torch.bfloat16)
+            torch._scaled_mm(dyq, wtq.t(), scale_a=sdy, scale_b=sw, out_dtype=torch.bfloat16)
+            torch._scaled_mm(dytq, xtq.t(), scale_a=sdy, scale_b=sx, out_dtype=torch.float32)
+
+    for _ in range(warmup):
+        gemms()
+    gt = 0.0
+    for _ in range(steps):
+        flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gemms()
+        b.record()
+        b.synchronize()
+        gt += a.elapsed_time(b)
+    gms = gt / steps
+    return {"impl": "torch._scaled_mm e4m3 per-tensor", "ms_per_step": round(ms, 4),
+            "tflops": round(flops_per_step() / (ms * 1e-3) / 1e12, 1),
+            "gemm_only_ms_per_step": round(gms, 4),
+            "gemm_only_tflops": round(flops_per_step() / (gms * 1e-3) / 1e12, 1),
+            "note": "ms_per_step includes unfused torch quantisation and transposes; gemm_only times the "
+                    "12 FP8 GEMMs of the step on pre-quantised operands"}
 
 
 def main():
@@ -483,6 +470,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-fp8", action="store_true", help="skip the FP8 (torch._scaled_mm) comparator")
     ap.add_argument("--profile-case", action="store_true", help="run the small ncu case and exit")
     ap.add_argument("--traffic-from", metavar="CSV", help="turn an ncu CSV of dram bytes for this benchmark "
                     "into profiles/traffic_llama8b_linears_T8192.json and exit")

@@ -148,6 +148,21 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
 mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, int64_t ldc, int out_dtype,
                         int accumulate, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
 
+/* Error-decomposition measurement ("Decomposing MXFP4 quantization error for LLM
+ * reinforcement learning", core insight and property 1).  x: device bf16 [rows, cols]
+ * (ld elements, cols % 32 == 0), rotated along cols with `had` and quantised row-wise
+ * with scale rule `mode`, as mxfp4_rotate_quantize does.  Per 32-block, with s_b the
+ * E8M0 scale and s* = amax/6 the ideal scale, Q = s_b*grid(x/s_b), Q* = s*·grid(x/s*):
+ *   e_scale = Q - Q*, e_DZ = Q* - x where |x| < amax/24 (the deadzone), e_grid = Q* - x
+ *   elsewhere.
+ * out: device, 7 doubles (8-byte aligned), overwritten with the tensor-wide sums
+ *   [sum e^2, sum e_scale^2, sum e_DZ^2, sum e_grid^2, sum e_scale*e_grid,
+ *    deadzone count, element count].
+ * Under the ceiling scale, sum e^2 = scale2 + dz2 + grid2 + 2*scale_grid (property 1).
+ * fp64 sums are accumulated atomically, so the last bits depend on the order. */
+mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                       double* out, mxfp4_stream_t stream);
+
 /* Workspace bytes needed by mxfp4_linear_{fprop,dgrad,wgrad} (op = MXFP4_OP_*). */
 size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp4_config* cfg);
 

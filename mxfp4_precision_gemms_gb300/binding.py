@@ -75,6 +75,7 @@ def lib():
                 "mxfp4_linear_wgrad": ([T, T, CF, P, P, S, P], I),
                 "mxfp4_linear_fprop_noalloc": ([P, P, I64, I64, I64, CF, P, T, T, P], I),
                 "mxfp4_noalloc_scratch_bytes": ([], S),
+                "mxfp4_error_decomposition": ([P, I64, I64, I64, I, I, P, P], I),
                 "mxfp4_device_status": ([P], I),
                 "mxfp4_set_wait_limit_ns": ([ctypes.c_uint64], None),
                 "mxfp4_test_inject_gemm_fault": ([I], None),
@@ -321,6 +322,20 @@ def linear_wgrad(dyT: QTensor, xT: QTensor, cfg: Config, dw: torch.Tensor | None
     _check(lib().mxfp4_linear_wgrad(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), _ptr(dw), None, 0,
                                     _stream(stream)))
     return dw
+
+
+DECOMP_KEYS = ("e2", "scale2", "dz2", "grid2", "scale_grid", "n_deadzone", "n")
+
+
+def error_decomposition(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_CEIL, stream=None) -> dict:
+    """Tensor-wide sums of the MXFP4 error components of a row-quantised bf16 matrix
+    (mxfp4_error_decomposition); returns a dict keyed by DECOMP_KEYS."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a CUDA bf16 matrix with unit column stride")
+    out = torch.empty(7, dtype=torch.float64, device=x.device)
+    _check(lib().mxfp4_error_decomposition(_ptr(x), x.shape[0], x.shape[1], x.stride(0), had, mode, _ptr(out),
+                                           _stream(stream)))
+    return dict(zip(DECOMP_KEYS, out.cpu().tolist()))
 
 
 def device_status(stream=None) -> int:

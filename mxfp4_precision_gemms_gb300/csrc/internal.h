@@ -59,6 +59,9 @@ struct GemmParams {
 
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s);
 
+cudaError_t launch_error_decomposition(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                                       double* out, cudaStream_t s);
+
 // Host helpers implemented in mxfp4_api.cu.
 uint32_t* device_status_ptr();  // for the current device
 // Records the thread-local message returned by mxfp4_last_error() and returns st.

@@ -373,6 +373,29 @@ mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, i
     return ok();
 }
 
+mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                       double* out, mxfp4_stream_t stream) {
+    if (rows < 0 || cols < 0) return fail(MXFP4_ERR_INVALID_ARG, "negative size");
+    if (!valid_had(had)) return fail(MXFP4_ERR_INVALID_ARG, "hadamard must be 0, 16 or 32 (got %d)", had);
+    if (!valid_mode(mode)) return fail(MXFP4_ERR_INVALID_ARG, "scale mode must be 0 or 1 (got %d)", mode);
+    if (cols % 32) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "cols (%lld) %% 32 != 0", (long long)cols);
+    if (!out) return fail(MXFP4_ERR_INVALID_ARG, "out is NULL");
+    if (reinterpret_cast<uintptr_t>(out) & 7u) return fail(MXFP4_ERR_MISALIGNED, "out not 8-byte aligned");
+    if (rows && cols) {
+        if (!x) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
+        if (ld < cols || ld % 8)
+            return fail(MXFP4_ERR_MISALIGNED, "ld (%lld) must be >= cols and a multiple of 8", (long long)ld);
+        if (!aligned16(x)) return fail(MXFP4_ERR_MISALIGNED, "x not 16-byte aligned");
+    }
+    int dev;
+    mxfp4_status st;
+    if ((st = check_device(&dev))) return st;
+    cudaError_t e = launch_error_decomposition(static_cast<const uint16_t*>(x), rows, cols, ld, had, mode, out,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "error decomposition launch");
+    return ok();
+}
+
 size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp4_config* cfg) {
     (void)cfg;
     switch (op) {
