@@ -163,6 +163,13 @@ mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, i
 mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
                                        double* out, mxfp4_stream_t stream);
 
+/* Tensor-core peak probe (measurement helper, synchronous): every SM issues `iters`
+ * back-to-back M=128 N=256 tcgen05.mma instructions on operands resident in shared
+ * memory, and *tflops receives the dense rate.  kind 0: kind::mxf4 (E2M1, UE8M0 per
+ * 32, the GEMM's instruction); 1: kind::mxf4nvf4 with the same 2X UE8M0 scaling;
+ * 2: kind::f16 with bf16 operands (calibration).  Allocates no global memory. */
+mxfp4_status mxfp4_mma_peak_probe(int kind, int64_t iters, double* tflops);
+
 /* Workspace bytes needed by mxfp4_linear_{fprop,dgrad,wgrad} (op = MXFP4_OP_*). */
 size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp4_config* cfg);
 

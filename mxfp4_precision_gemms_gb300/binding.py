@@ -76,6 +76,7 @@ def lib():
                 "mxfp4_linear_fprop_noalloc": ([P, P, I64, I64, I64, CF, P, T, T, P], I),
                 "mxfp4_noalloc_scratch_bytes": ([], S),
                 "mxfp4_error_decomposition": ([P, I64, I64, I64, I, I, P, P], I),
+                "mxfp4_mma_peak_probe": ([I, I64, ctypes.POINTER(ctypes.c_double)], I),
                 "mxfp4_device_status": ([P], I),
                 "mxfp4_set_wait_limit_ns": ([ctypes.c_uint64], None),
                 "mxfp4_test_inject_gemm_fault": ([I], None),
@@ -336,6 +337,14 @@ def error_decomposition(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_CE
     _check(lib().mxfp4_error_decomposition(_ptr(x), x.shape[0], x.shape[1], x.stride(0), had, mode, _ptr(out),
                                            _stream(stream)))
     return dict(zip(DECOMP_KEYS, out.cpu().tolist()))
+
+
+def mma_peak_tflops(kind: int = 0, iters: int = 1 << 16) -> float:
+    """Dense tensor-core rate from mxfp4_mma_peak_probe (0: kind::mxf4, 1: kind::mxf4nvf4
+    2X, 2: bf16 kind::f16), in TFLOP/s."""
+    out = ctypes.c_double(0.0)
+    _check(lib().mxfp4_mma_peak_probe(kind, iters, ctypes.byref(out)))
+    return out.value
 
 
 def device_status(stream=None) -> int:

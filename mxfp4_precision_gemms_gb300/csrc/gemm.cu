@@ -36,7 +36,7 @@ constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int STG_PITCH = 80;                      // bytes per staged row: 64 B of data + 16 B pad
 constexpr int STG_WARP_BYTES = 32 * STG_PITCH;     // one warp's staging: 32 rows x 64 B
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int ACC>
 struct GemmCfg {
     static constexpr int A_STAGE = BM * BK_BYTES;
     static constexpr int B_STAGE = BN * BK_BYTES;
@@ -47,12 +47,13 @@ struct GemmCfg {
     static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
-    static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 3) * 8;
+    static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 2 * ACC + 1) * 8;
     static constexpr int OFF_STG = (OFF_TMEM + 16 + 127) / 128 * 128;  // epilogue staging (16-byte vector access)
     static constexpr int SMEM = OFF_STG + EPI_WARPS * STG_WARP_BYTES + 1024;  // + alignment slack
     static constexpr int TX_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
     static constexpr int SF_COLS = 8 + 8 * (BN / 128);  // TMEM columns of scales per stage
-    static constexpr int TMEM_USED = BN + STAGES * SF_COLS;
+    static constexpr int ACC_COLS = ACC * BN;               // fp32 accumulators (one per buffered tile)
+    static constexpr int TMEM_USED = ACC_COLS + STAGES * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget");
@@ -122,9 +123,9 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stg, i
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int ACC>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid_constant__ GemmParams p) {
-    using Cfg = GemmCfg<BN, STAGES>;
+    using Cfg = GemmCfg<BN, STAGES, ACC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + Cfg::OFF_A;
@@ -133,9 +134,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
     uint8_t* sSFB = smem + Cfg::OFF_SFB;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* empty = full + STAGES;
-    uint64_t* acc_full = empty + STAGES;   // MMA -> epilogue: accumulator holds a finished tile
-    uint64_t* acc_empty = acc_full + 1;    // epilogue -> MMA: accumulator has been read out
-    uint64_t* mma_done = acc_empty + 1;    // every MMA issued by this CTA has completed
+    uint64_t* acc_full = empty + STAGES;   // [ACC] MMA -> epilogue: accumulator holds a finished tile
+    uint64_t* acc_empty = acc_full + ACC;  // [ACC] epilogue -> MMA: accumulator has been read out
+    uint64_t* mma_done = acc_empty + ACC;  // every MMA issued by this CTA has completed
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_TMEM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -149,8 +150,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, EPI_WARPS);  // one arrive per epilogue warp
+        for (int a = 0; a < ACC; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], EPI_WARPS);  // one arrive per epilogue warp
+        }
         mbar_init(mma_done, 1);
         fence_mbar_init();
         prefetch_tmap(&p.map_a);
@@ -211,8 +214,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
             uint32_t it = 0, tcount = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++tcount) {
-                if (tcount > 0) {
-                    if (!wait_bounded(acc_empty, (tcount - 1u) & 1u, p.wait_ns, p.status)) break;
+                const uint32_t ab = tcount % ACC;                 // accumulator buffer of this tile
+                const uint32_t acc_t = tmem_base + ab * BN;
+                if (tcount >= ACC) {
+                    if (!wait_bounded(&acc_empty[ab], (tcount / ACC - 1u) & 1u, p.wait_ns, p.status)) break;
                     tc_fence_after();
                 }
                 for (int kt = 0; kt < num_k; ++kt, ++it) {
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + BN + s * Cfg::SF_COLS;
+                    const uint32_t sfa_t = tmem_base + Cfg::ACC_COLS + s * Cfg::SF_COLS;
                     const uint32_t sfb_t = sfa_t + 8;
 #pragma unroll
                     for (int a = 0; a < 2; ++a)
@@ -244,12 +249,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
                         const uint64_t adesc = smem_desc(a_base + k * 32, 16, 1024, kSwizzle128B);
                         const uint64_t bdesc = smem_desc(b_base + k * 32, 16, 1024, kSwizzle128B);
                         const uint32_t sf_id = (uint32_t)(k & 1) * 2u;
-                        tc_mma_mxf4(tmem_base, adesc, bdesc, idesc_with_sf_ids(idesc, sf_id, sf_id),
+                        tc_mma_mxf4(acc_t, adesc, bdesc, idesc_with_sf_ids(idesc, sf_id, sf_id),
                                     sfa_t + (k >> 1) * 4, sfb_t + (k >> 1) * SFB_KSTRIDE, (kt | k) != 0);
                     }
                     tc_commit(&empty[s]);
                 }
-                if (ok) tc_commit(acc_full);
+                if (ok) tc_commit(&acc_full[ab]);
             }
             // Every MMA issued here has completed before TMEM is released.
             tc_commit(mma_done);
@@ -266,18 +271,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
         constexpr int CH = BN / 2 / 32;  // 32-column chunks per thread
         uint32_t tcount = 0;
         for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
-            if (!wait_bounded(acc_full, tcount & 1u, p.wait_ns, p.status)) break;
+            const uint32_t ab = tcount % ACC;
+            if (!wait_bounded(&acc_full[ab], (tcount / ACC) & 1u, p.wait_ns, p.status)) break;
             tc_fence_after();
             const int64_t row_base = (tile / num_n) * BM + q * 32;
             const int64_t c0 = (tile % num_n) * BN + h * (BN / 2);
             uint32_t v[CH][32];
 #pragma unroll
             for (int c = 0; c < CH; ++c)
-                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * (BN / 2) + c * 32), v[c]);
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + ab * BN + (uint32_t)(h * (BN / 2) + c * 32),
+                                   v[c]);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
+            if (lane == 0) mbar_arrive(&acc_empty[ab]);
 #pragma unroll
             for (int c = 0; c < CH; ++c) store_chunk(p, stg, lane, row_base, c0 + c * 32, v[c]);
         }
@@ -291,10 +298,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int ACC>
 cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
-    using Cfg = GemmCfg<BN, STAGES>;
-    auto kern = mxf4_gemm_kernel<BN, STAGES>;
+    using Cfg = GemmCfg<BN, STAGES, ACC>;
+    auto kern = mxf4_gemm_kernel<BN, STAGES, ACC>;
     static bool configured[64] = {};
     static int sm_count[64] = {};
     int dev = 0;
@@ -318,11 +325,11 @@ cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
 // Persistent launch: one CTA per SM walks the 128 x BN output tiles; BN = 256 unless
 // the whole N fits in 128 columns.
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s) {
-    if (p.N <= 128) return launch_cfg<128, 6>(p, s);
+    if (p.N <= 128) return launch_cfg<128, 6, 2>(p, s);
 #ifdef MXG_FORCE_BN128
-    return launch_cfg<128, 6>(p, s);
+    return launch_cfg<128, 6, 2>(p, s);
 #else
-    return launch_cfg<256, MXG_STAGES_256>(p, s);
+    return launch_cfg<256, MXG_STAGES_256, 1>(p, s);
 #endif
 }
 

@@ -59,6 +59,8 @@ struct GemmParams {
 
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s);
 
+cudaError_t run_mma_peak_probe(int kind, int64_t iters, float* ms, uint32_t* status, uint64_t wait_ns);
+
 cudaError_t launch_error_decomposition(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
                                        double* out, cudaStream_t s);
 

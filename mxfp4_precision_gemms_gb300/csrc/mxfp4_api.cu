@@ -396,6 +396,21 @@ mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols
     return ok();
 }
 
+mxfp4_status mxfp4_mma_peak_probe(int kind, int64_t iters, double* tflops) {
+    if (kind < 0 || kind > 2) return fail(MXFP4_ERR_INVALID_ARG, "kind must be 0, 1 or 2");
+    if (iters <= 0 || !tflops) return fail(MXFP4_ERR_INVALID_ARG, "iters must be positive and tflops non-NULL");
+    int dev, sms = 0;
+    mxfp4_status st;
+    if ((st = check_device(&dev))) return st;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    float ms = 0.0f;
+    cudaError_t e = run_mma_peak_probe(kind, iters, &ms, device_status_ptr(), wait_limit());
+    if (e != cudaSuccess) return cuda_fail(e, "mma peak probe");
+    const double k = kind == 2 ? 16.0 : 64.0;  // K per instruction
+    *tflops = (double)sms * (double)iters * 2.0 * 128.0 * 256.0 * k / (ms * 1e-3) / 1e12;
+    return ok();
+}
+
 size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp4_config* cfg) {
     (void)cfg;
     switch (op) {

@@ -279,17 +279,16 @@ __global__ void __launch_bounds__(QTHREADS, 2) rq_kernel(const QuantParams p) {
 }
 
 // ---------------------------------------------------------------------------------
-// TMA-fed variant: one producer warp keeps up to Q_STAGES 128 x 128 tiles in flight
-// (two 64-column boxes each, 128-byte swizzle) and two groups of 8 consumer warps
-// process alternate tiles.  The arithmetic is the same as rq_kernel's.
-constexpr int Q_STAGES = 4;
+// TMA-fed variant: persistent CTAs (two per SM) walk 128 x 128 tiles; thread 0 keeps
+// the next Q_STAGES - 1 tiles of its CTA in flight (two 64-column boxes per tile,
+// 128-byte swizzle) while all 256 threads process the current one.  The arithmetic
+// is the same as rq_kernel's.
+constexpr int Q_STAGES = 3;
 constexpr int Q_TILE_BYTES = TR * TC * 2;  // 32 KB
 constexpr int Q_BOX_BYTES = Q_TILE_BYTES / 2;
-constexpr int Q_GROUPS = 2;
-constexpr int Q_TMA_THREADS = 32 + Q_GROUPS * QTHREADS;
 constexpr int Q_OFF_BAR = Q_STAGES * Q_TILE_BYTES;
-constexpr int Q_OFF_AMAX = Q_OFF_BAR + 2 * Q_STAGES * 8;
-constexpr int Q_TMA_SMEM = Q_OFF_AMAX + Q_GROUPS * TR * 4 * 4 + 1024;
+constexpr int Q_OFF_AMAX = Q_OFF_BAR + Q_STAGES * 8;
+constexpr int Q_TMA_SMEM = Q_OFF_AMAX + TR * 4 * 4 + 1024;
 
 // Word offset (32-bit units) of 16-byte chunk `chunk` (0..15) of tile row r in the
 // swizzled stage: columns 0-63 are box 0, 64-127 box 1; within a box a row is 128 B
@@ -298,61 +297,40 @@ __device__ __forceinline__ int sw_word(int r, int chunk) {
     return ((chunk >> 3) * Q_BOX_BYTES + r * 128 + (((chunk & 7) ^ (r & 7)) << 4)) >> 2;
 }
 
-__device__ __forceinline__ void group_sync(int g) {
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(QTHREADS) : "memory");
-}
-
 template <int HAD, bool ROW, bool COLT, bool TWOD>
-__global__ void __maxnreg__(120) rq_tma_kernel(const __grid_constant__ QuantTmaParams P) {
+__global__ void __launch_bounds__(QTHREADS, 2) rq_tma_kernel(const __grid_constant__ QuantTmaParams P) {
     const QuantParams& p = P.p;
     extern __shared__ uint8_t q_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Q_OFF_BAR);
-    uint64_t* empty = full + Q_STAGES;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float* seg_amax = reinterpret_cast<float*>(smem + Q_OFF_AMAX);
+    const int t = threadIdx.x;
 
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < Q_STAGES; ++st) {
-            mbar_init(&full[st], 1);
-            mbar_init(&empty[st], QTHREADS / 32);
-        }
+    auto issue = [&](uint32_t j) {  // tile j of this CTA's sequence -> stage j % Q_STAGES
+        const int64_t tile = blockIdx.x + (int64_t)j * gridDim.x;
+        if (tile >= P.tiles) return;
+        const int st = (int)(j % Q_STAGES);
+        const int32_t row0 = (int32_t)((tile / P.tiles_c) * TR), col0 = (int32_t)((tile % P.tiles_c) * TC);
+        mbar_arrive_expect_tx(&full[st], Q_TILE_BYTES);
+        uint8_t* dst = smem + st * Q_TILE_BYTES;
+        tma_load_2d(dst, &P.map_x, &full[st], col0, row0);
+        tma_load_2d(dst + Q_BOX_BYTES, &P.map_x, &full[st], col0 + 64, row0);
+    };
+
+    if (t == 0) {
+        for (int st = 0; st < Q_STAGES; ++st) mbar_init(&full[st], 1);
         fence_mbar_init();
         prefetch_tmap(&P.map_x);
+        for (uint32_t j = 0; j + 1 < Q_STAGES; ++j) issue(j);
     }
     __syncthreads();
 
-    if (warp == 0) {
-        if (elect_one()) {
-            uint32_t armed[Q_STAGES];
-#pragma unroll
-            for (int st = 0; st < Q_STAGES; ++st) armed[st] = 0;
-            uint32_t i = 0;
-            for (int64_t tile = blockIdx.x; tile < P.tiles; tile += gridDim.x, ++i) {
-                const int st = (int)(i % Q_STAGES);
-                const uint32_t ph = (i / Q_STAGES) & 1u;
-                if (i >= Q_STAGES && !wait_bounded(&empty[st], ph ^ 1u, P.wait_ns, P.status)) break;
-                const int32_t row0 = (int32_t)((tile / P.tiles_c) * TR), col0 = (int32_t)((tile % P.tiles_c) * TC);
-                mbar_arrive_expect_tx(&full[st], Q_TILE_BYTES);
-                uint8_t* dst = smem + st * Q_TILE_BYTES;
-                tma_load_2d(dst, &P.map_x, &full[st], col0, row0);
-                tma_load_2d(dst + Q_BOX_BYTES, &P.map_x, &full[st], col0 + 64, row0);
-                armed[st] = i / Q_STAGES + 1u;
-            }
-#pragma unroll
-            for (int st = 0; st < Q_STAGES; ++st)
-                if (armed[st]) wait_bounded(&full[st], (armed[st] - 1u) & 1u, P.wait_ns, P.status);
-        }
-        return;
-    }
-
-    const int g = (warp - 1) / (QTHREADS / 32);
-    const int t = (threadIdx.x - 32) % QTHREADS;
-    float* seg_amax = reinterpret_cast<float*>(smem + Q_OFF_AMAX) + g * TR * 4;
-    uint32_t i = g;
-    for (int64_t tile = blockIdx.x + (int64_t)g * gridDim.x; tile < P.tiles; tile += Q_GROUPS * (int64_t)gridDim.x,
-                 i += Q_GROUPS) {
+    uint32_t i = 0;
+    for (int64_t tile = blockIdx.x; tile < P.tiles; tile += gridDim.x, ++i) {
+        // the stage refilled here was released by the __syncthreads ending iteration i - 1
+        if (t == 0) issue(i + Q_STAGES - 1);
         const int st = (int)(i % Q_STAGES);
-        if (!wait_bounded(&full[st], (i / Q_STAGES) & 1u, P.wait_ns, P.status)) break;
+        const bool landed = wait_bounded(&full[st], (i / Q_STAGES) & 1u, P.wait_ns, P.status);
         const uint32_t* buf = reinterpret_cast<const uint32_t*>(smem + st * Q_TILE_BYTES);
         const int64_t row0 = (tile / P.tiles_c) * TR, col0 = (tile % P.tiles_c) * TC;
 
@@ -361,7 +339,7 @@ __global__ void __maxnreg__(120) rq_tma_kernel(const __grid_constant__ QuantTmaP
             const int rx = pr, ry = pr + 64;
             const int64_t gc = col0 + 32 * s;
             const int64_t grx = row0 + rx, gry = row0 + ry;
-            const bool vx = grx < p.R && gc < p.C, vy = gry < p.R && gc < p.C;
+            const bool vx = landed && grx < p.R && gc < p.C, vy = landed && gry < p.R && gc < p.C;
             float2 v[32];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -382,7 +360,7 @@ __global__ void __maxnreg__(120) rq_tma_kernel(const __grid_constant__ QuantTmaP
             if constexpr (TWOD) {
                 seg_amax[rx * 4 + s] = ax;
                 seg_amax[ry * 4 + s] = ay;
-                group_sync(g);
+                __syncthreads();
                 float tx = 0.0f, ty = 0.0f;
                 const int bx = rx & ~31, by = ry & ~31;
 #pragma unroll 8
@@ -390,7 +368,6 @@ __global__ void __maxnreg__(120) rq_tma_kernel(const __grid_constant__ QuantTmaP
                     tx = fmaxf(tx, seg_amax[(bx + k) * 4 + s]);
                     ty = fmaxf(ty, seg_amax[(by + k) * 4 + s]);
                 }
-                group_sync(g);  // seg_amax is rewritten for the group's next tile
                 const uint32_t bytex = scale_byte(tx, p.mode), bytey = scale_byte(ty, p.mode);
                 uint4 qx, qy;
                 quant32x2<HAD>(v, bytex, bytey, qx, qy);
@@ -420,7 +397,7 @@ __global__ void __maxnreg__(120) rq_tma_kernel(const __grid_constant__ QuantTmaP
         if constexpr (COLT) {
             const int cp = t & 63, rb = t >> 6;
             const int64_t gcol = col0 + 2 * cp, grow = row0 + 32 * rb;
-            if (gcol < p.C && grow < p.R) {
+            if (landed && gcol < p.C && grow < p.R) {
                 float2 v[32];
                 const int chunk = cp >> 2, wi = cp & 3;  // 16-byte chunk of the row holding columns 2cp, 2cp+1
 #pragma unroll
@@ -441,9 +418,10 @@ __global__ void __maxnreg__(120) rq_tma_kernel(const __grid_constant__ QuantTmaP
                 store_scale(p.colT, gcol + 1, grow / 32, p.R / 32, bytey);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);  // this warp has finished reading the stage
+        __syncthreads();  // every thread is done with this stage (and with seg_amax)
     }
+    // every copy this CTA issued has been waited for by the loop above (issue only
+    // targets tiles the loop visits), so nothing is in flight at exit.
 }
 
 template <int HAD, bool ROW, bool COLT, bool TWOD>
@@ -461,8 +439,9 @@ cudaError_t launch_tma(const QuantTmaParams& P, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    const unsigned grid = (unsigned)(P.tiles < sms[dev] ? P.tiles : sms[dev]);
-    kern<<<grid, Q_TMA_THREADS, Q_TMA_SMEM, st>>>(P);
+    const int64_t max_grid = 2 * (int64_t)sms[dev];
+    const unsigned grid = (unsigned)(P.tiles < max_grid ? P.tiles : max_grid);
+    kern<<<grid, QTHREADS, Q_TMA_SMEM, st>>>(P);
     return cudaGetLastError();
 }
 

@@ -94,3 +94,13 @@ def test_extreme_scales(torch):
     sb = g.integers(100, 154, size=(N, K // 32), dtype=np.uint8)
     want, S = oracle.gemm(ca, sa, cb, sb)
     assert_within(run(torch, (ca, sa), (cb, sb)), want, S, what="wide scales")
+
+
+def test_many_tiles_narrow_n(torch):
+    """N <= 128 selects the 128-wide tiles with two TMEM accumulators; ~300 tiles make
+    every persistent CTA alternate between them (and the M tail is ragged)."""
+    M, N, K = 37984 + 40, 96, 512
+    qa, qb = oracle_operands(M, N, K, 14)
+    want, S = oracle.gemm(*qa, *qb)
+    assert_within(run(torch, qa, qb), want, S, what="many tiles, N=96")
+    assert_within(run(torch, qa, qb, out_dtype=1), want, S, bf16=True, what="many tiles, N=96, bf16")
