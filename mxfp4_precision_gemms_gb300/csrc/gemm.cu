@@ -24,6 +24,12 @@
 namespace mx {
 namespace {
 
+// 1: the epilogue writes C with TMA tile stores from a swizzled staging buffer;
+// 0: coalesced st.global from a padded staging buffer.
+#ifndef MXG_TMA_STORE
+#define MXG_TMA_STORE 1
+#endif
+
 // Tuning knob (compile-time): pipeline depth of the 256-wide tiles.
 #ifndef MXG_STAGES_256
 #define MXG_STAGES_256 4
@@ -33,7 +39,13 @@ constexpr int BM = 128;
 constexpr int BK_BYTES = 128;  // 256 E2M1 elements per stage
 constexpr int EPI_WARPS = 8;  // two per TMEM lane quadrant, each owning half the columns
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
+#if MXG_TMA_STORE
+constexpr int STG_PITCH = 64;                      // 32 rows x 64 B, 64-byte swizzle (TMA store box)
+constexpr int STG_ALIGN = 1024;
+#else
 constexpr int STG_PITCH = 80;                      // bytes per staged row: 64 B of data + 16 B pad
+constexpr int STG_ALIGN = 128;
+#endif
 constexpr int STG_WARP_BYTES = 32 * STG_PITCH;     // one warp's staging: 32 rows x 64 B
 
 template <int BN, int STAGES, int ACC>
@@ -48,7 +60,7 @@ struct GemmCfg {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
     static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 2 * ACC + 1) * 8;
-    static constexpr int OFF_STG = (OFF_TMEM + 16 + 127) / 128 * 128;  // epilogue staging (16-byte vector access)
+    static constexpr int OFF_STG = (OFF_TMEM + 16 + STG_ALIGN - 1) / STG_ALIGN * STG_ALIGN;  // epilogue staging
     static constexpr int SMEM = OFF_STG + EPI_WARPS * STG_WARP_BYTES + 1024;  // + alignment slack
     static constexpr int TX_BYTES = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
     static constexpr int SF_COLS = 8 + 8 * (BN / 128);  // TMEM columns of scales per stage
@@ -120,6 +132,45 @@ __device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stg, i
     } else {
         stage_and_store(p, stg, lane, row_base, col0, v, 4);
         stage_and_store(p, stg, lane, row_base, col0 + 16, v + 16, 4);
+    }
+}
+
+// TMA-store epilogue: lane i writes its row's 64 bytes into the warp's staging tile
+// (64-byte swizzle: 16-byte chunk j of row r at j ^ ((r >> 1) & 3), conflict-free),
+// then one lane stores the 32-row x 64-byte box with TMA (add-reduce for accumulate).
+// The staging tile is reused only after the previous store has read it.
+__device__ __forceinline__ void tma_store_block(const GemmParams& p, uint8_t* stg, int lane, int64_t row_base,
+                                               int64_t col0, const uint32_t* w) {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0 && row_base < p.M && col0 < p.N) {
+        if (p.accumulate)
+            tma_reduce_add_2d(&p.map_c, stg, (int32_t)col0, (int32_t)row_base);
+        else
+            tma_store_2d(&p.map_c, stg, (int32_t)col0, (int32_t)row_base);
+        bulk_commit();
+    }
+}
+
+__device__ __forceinline__ void store_chunk_tma(const GemmParams& p, uint8_t* stg, int lane, int64_t row_base,
+                                               int64_t col0, const uint32_t (&v)[32]) {
+    if (p.out_bf16) {
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            w[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        tma_store_block(p, stg, lane, row_base, col0, w);
+    } else {
+        tma_store_block(p, stg, lane, row_base, col0, v);
+        tma_store_block(p, stg, lane, row_base, col0 + 16, v + 16);
     }
 }
 
@@ -286,8 +337,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[ab]);
 #pragma unroll
-            for (int c = 0; c < CH; ++c) store_chunk(p, stg, lane, row_base, c0 + c * 32, v[c]);
+            for (int c = 0; c < CH; ++c) {
+#if MXG_TMA_STORE
+                store_chunk_tma(p, stg, lane, row_base, c0 + c * 32, v[c]);
+#else
+                store_chunk(p, stg, lane, row_base, c0 + c * 32, v[c]);
+#endif
+            }
         }
+#if MXG_TMA_STORE
+        if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
+        __syncwarp();
+#endif
     }
 
     tc_fence_before();

@@ -45,6 +45,7 @@ cudaError_t launch_rotate_quantize(const QuantParams& p, int had, unsigned layou
 struct GemmParams {
     CUtensorMap map_a;   // codes of A [M, K/2] bytes, box 128 rows x 128 B, 128B swizzle
     CUtensorMap map_b;   // codes of B [N, K/2] bytes
+    CUtensorMap map_c;   // output C [M, N]: box 64 bytes x 32 rows, 64-byte swizzle
     const uint8_t* sfa;  // MMA-order scales of A
     const uint8_t* sfb;  // MMA-order scales of B
     int64_t M, N, K, kb_pad;
@@ -70,6 +71,7 @@ uint32_t* device_status_ptr();  // for the current device
 mxfp4_status record_error(mxfp4_status st, const char* fmt, ...);
 bool encode_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t cols, uint32_t box_rows);
 bool encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld);
+bool encode_out_map(CUtensorMap* map, void* c, int64_t rows, int64_t cols, int64_t ldc, bool bf16);
 uint64_t quant_wait_ns();  // bounded-wait limit of the calling host thread
 
 }  // namespace mx

@@ -148,6 +148,21 @@ bool encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols
 
 uint64_t quant_wait_ns() { return wait_limit(); }
 
+// 2D tensor map over the GEMM output C [rows, cols] (bf16 or fp32, leading dimension
+// ldc elements): box = 64 bytes of a row x 32 rows, 64-byte swizzle.
+bool encode_out_map(CUtensorMap* map, void* c, int64_t rows, int64_t cols, int64_t ldc, bool bf16) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const int64_t esz = bf16 ? 2 : 4;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ldc * esz)};
+    const cuuint32_t box[2] = {(cuuint32_t)(64 / esz), 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, c, dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mx
 
 using namespace mx;
@@ -350,7 +365,8 @@ mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, i
 
     GemmParams p{};
     if (!encode_codes_map(&p.map_a, A->codes, A->rows, A->cols, 128) ||
-        !encode_codes_map(&p.map_b, B->codes, B->rows, B->cols, 128))
+        !encode_codes_map(&p.map_b, B->codes, B->rows, B->cols, 128) ||
+        !encode_out_map(&p.map_c, C, A->rows, B->rows, ldc, out_dtype == MXFP4_OUT_BF16))
         return fail(MXFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     p.sfa = A->scales;
     p.sfb = B->scales;
