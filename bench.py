@@ -323,7 +323,7 @@ def gpu_arm(args, rank, world, dist):
     traffic = measured_traffic()
     roof_gemm = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1),
                  "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4), "traffic": traffic["gemm"],
-                 "kernel": "mxf4_gemm_kernel", "peak_source": "measured bf16 sustained x 6 (nominal fp4/bf16)",
+                 "kernel": "mxf4_gemm_pair_kernel", "peak_source": "measured bf16 sustained x 6 (nominal fp4/bf16)",
                  "peak_probe_tflops": round(probe, 1), "frac_of_probe": round(gemm_tflops / probe, 4)}
     roof_quant = {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": hbm, "unit": "GB/s",
                   "frac": round(quant_gbs / hbm, 4), "traffic": traffic["quant"], "kernel": "rq_kernel",
@@ -575,8 +575,9 @@ def write_traffic(csv_path):
             per["quant"].append(b)
     rec = {k: {"bytes_per_launch": round(sum(v) / len(v)), "launches": len(v),
                "sources_sha": kernel_sources_sha(KERNEL_SOURCES[k])} for k, v in per.items() if v}
-    rec["command"] = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none --csv "
-                      "--log-file <csv> python bench.py --steps 1 --warmup 3 --skip-e2e --skip-cpu-baseline")
+    rec["command"] = ("ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
+                      "--clock-control none --csv --log-file <csv> python bench.py --steps 1 --warmup 3 "
+                      "--skip-e2e --skip-cpu-baseline --skip-fp8")
     path = os.path.join(ROOT, "profiles", "traffic_llama8b_linears_T8192.json")
     json.dump(rec, open(path, "w"), indent=1)
     print(json.dumps(rec))

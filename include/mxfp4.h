@@ -167,7 +167,9 @@ mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols
  * back-to-back M=128 N=256 tcgen05.mma instructions on operands resident in shared
  * memory, and *tflops receives the dense rate.  kind 0: kind::mxf4 (E2M1, UE8M0 per
  * 32, the GEMM's instruction); 1: kind::mxf4nvf4 with the same 2X UE8M0 scaling;
- * 2: kind::f16 with bf16 operands (calibration).  Allocates no global memory. */
+ * 2: kind::f16 with bf16 operands (calibration); 3: kind::mxf4nvf4 scale_vec::4X with
+ * UE4M3 scales per 16 (the NVFP4 form, for comparison only); 4: kind::mxf4 issued by CTA
+ * pairs (.cta_group::2, M = 256 per pair).  Allocates no global memory. */
 mxfp4_status mxfp4_mma_peak_probe(int kind, int64_t iters, double* tflops);
 
 /* Workspace bytes needed by mxfp4_linear_{fprop,dgrad,wgrad} (op = MXFP4_OP_*). */

@@ -341,7 +341,8 @@ def error_decomposition(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_CE
 
 def mma_peak_tflops(kind: int = 0, iters: int = 1 << 16) -> float:
     """Dense tensor-core rate from mxfp4_mma_peak_probe (0: kind::mxf4, 1: kind::mxf4nvf4
-    2X, 2: bf16 kind::f16), in TFLOP/s."""
+    2X, 2: bf16 kind::f16, 3: kind::mxf4nvf4 4X with UE4M3 scales, 4: kind::mxf4 on CTA pairs),
+    in TFLOP/s."""
     out = ctypes.c_double(0.0)
     _check(lib().mxfp4_mma_peak_probe(kind, iters, ctypes.byref(out)))
     return out.value

@@ -5,7 +5,10 @@
 // The operands are the quantised copies of "Pretraining Large Language Models with
 // MXFP4 on Native FP4 Hardware" (C.1-C.3), already rotated along K.
 //
-// Structure (persistent: one CTA per SM walks 128 x BN output tiles, 320 threads):
+// Two kernels.  The CTA-pair kernel (below the single-CTA one) runs whenever both M
+// and N exceed 128; the single-CTA kernel covers narrow problems.
+//
+// Single-CTA structure (persistent: one CTA per SM walks 128 x BN tiles, 320 threads):
 //   warp 0  TMA producer: 128x128-byte code tiles of A and B (128B swizzle) and the
 //           matching 1 KB scale-factor atoms, into a STAGES-deep shared-memory ring.
 //   warp 1  allocates TMEM; one elected thread copies each stage's scale factors
@@ -28,6 +31,14 @@ namespace {
 // 0: coalesced st.global from a padded staging buffer.
 #ifndef MXG_TMA_STORE
 #define MXG_TMA_STORE 1
+#endif
+
+// 1: problems with M > 128 and N > 128 use the CTA-pair kernel (256 x 256 tiles).
+#ifndef MXG_PAIR
+#define MXG_PAIR 1
+#endif
+#ifndef MXG_PAIR_STAGES
+#define MXG_PAIR_STAGES 5
 #endif
 
 // Tuning knob (compile-time): pipeline depth of the 256-wide tiles.
@@ -359,6 +370,248 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
     }
 }
 
+
+// ---------------------------------------------------------------------------------
+// CTA-pair kernel.  A cluster of two CTAs (on two SMs) computes 256 x 256 output tiles
+// with M = 256 tcgen05.mma.cta_group::2 instructions.  CTA r (r = 0, 1) stages rows
+// m0 + 128r .. +127 of A and rows n0 + 128r .. +127 of B, and its TMEM receives its
+// 128 rows of the tile.  Each CTA thus loads 256 operand rows per K stage for a
+// 128 x 256 share of the output, where a single-CTA 128 x 256 tile loads 384: a third
+// less L2 -> SMEM traffic and shared-memory bandwidth per FLOP.
+//   warp 0 (both CTAs)  TMA producer for the CTA's halves, plus the scale factors
+//           its tensor core needs (its 128 rows of A, all 256 rows of B).  Completion
+//           is counted on the leader's (CTA 0's) full barrier, which the leader arms
+//           with the pair's bytes.
+//   warp 1  allocates the pair's TMEM together with the other CTA; in the leader one
+//           thread copies scale factors (tcgen05.cp.cta_group::2, each CTA's shared
+//           memory -> its own TMEM) and issues the pair's MMAs; its commits arrive on
+//           the barriers of both CTAs (stage free, accumulator full, all done).
+//   warps 2-9 (both CTAs)  epilogue of the CTA's 128 rows; each warp reports the
+//           accumulator read out to the leader's acc_empty barrier.
+// One CTA per SM (shared memory > half the SM's): two pairs never compete for the
+// TMEM of one SM, so the collective TMEM allocation cannot wait on another pair.
+template <int STAGES>
+struct PairCfg {
+    static constexpr int A_STAGE = 128 * BK_BYTES;
+    static constexpr int B_STAGE = 128 * BK_BYTES;
+    static constexpr int SFA_STAGE = 1024;  // this CTA's 128 rows x 8 blocks
+    static constexpr int SFB_STAGE = 2048;  // all 256 B rows x 8 blocks
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
+    static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 3) * 8;
+    static constexpr int OFF_STG = (OFF_TMEM + 16 + STG_ALIGN - 1) / STG_ALIGN * STG_ALIGN;
+    static constexpr int SMEM = OFF_STG + EPI_WARPS * STG_WARP_BYTES + 1024;
+    static constexpr uint32_t TX_PAIR = 2 * (A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE);
+    static constexpr int SF_COLS = 24;  // TMEM columns of scales per stage: 8 for A, 16 for B
+    static constexpr int TMEM_USED = 256 + STAGES * SF_COLS;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(TMEM_USED <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(2 * SMEM > 228 * 1024, "one CTA per SM");
+    static_assert(OFF_BAR % 8 == 0 && OFF_B % 1024 == 0 && OFF_SFA % 1024 == 0 && OFF_STG % 16 == 0, "alignment");
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+    using Cfg = PairCfg<STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem + Cfg::OFF_A;
+    uint8_t* sB = smem + Cfg::OFF_B;
+    uint8_t* sSFA = smem + Cfg::OFF_SFA;
+    uint8_t* sSFB = smem + Cfg::OFF_SFB;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);  // used in the leader
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;
+    uint64_t* acc_empty = acc_full + 1;  // used in the leader: both CTAs' epilogues arrive
+    uint64_t* mma_done = acc_empty + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_TMEM);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int num_k = (int)((p.K + 255) / 256);
+    const int64_t num_n = (p.N + 255) / 256;
+    const int64_t num_tiles = ((p.M + 255) / 256) * num_n;
+    const int64_t cluster = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+    const int64_t atoms_per_row_block = p.kb_pad / 4;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 2 * EPI_WARPS);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+        prefetch_tmap(&p.map_a);
+        prefetch_tmap(&p.map_b);
+        prefetch_tmap(&p.map_sfa);
+        prefetch_tmap(&p.map_sfb);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, Cfg::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before either signals the other's
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs)
+        if (elect_one()) {
+            const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
+            uint32_t armed[STAGES];  // phases issued per stage
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s) armed[s] = 0;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t tile = cluster; ok && tile < num_tiles; tile += num_clusters) {
+                const int64_t m0 = (tile / num_n) * 256, n0 = (tile % num_n) * 256;
+                const int32_t ya = (int32_t)(m0 + rank * 128), yb = (int32_t)(n0 + rank * 128);
+                const int32_t sfa_y = (int32_t)((m0 / 128 + rank) * atoms_per_row_block * 4);
+                const int32_t sfb_y0 = (int32_t)((n0 / 128) * atoms_per_row_block * 4);
+                const int32_t sfb_y1 = (int32_t)((n0 / 128 + 1) * atoms_per_row_block * 4);
+                for (int kt = 0; kt < num_k; ++kt, ++it) {
+                    const int s = (int)(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (it >= STAGES && !wait_bounded(&empty[s], ph ^ 1u, p.wait_ns, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (it == 0 && p.test_drop_first_stage && rank == 0) continue;  // fault injection
+                    if (rank == 0) mbar_arrive_expect_tx(&full[s], Cfg::TX_PAIR);
+                    const uint32_t bar = full_leader + (uint32_t)s * 8u;
+                    tma_load_2d_pair(sA + s * Cfg::A_STAGE, &p.map_a, bar, kt * BK_BYTES, ya);
+                    tma_load_2d_pair(sB + s * Cfg::B_STAGE, &p.map_b, bar, kt * BK_BYTES, yb);
+                    tma_load_2d_pair(sSFA + s * Cfg::SFA_STAGE, &p.map_sfa, bar, 0, sfa_y + kt * 8);
+                    tma_load_2d_pair(sSFB + s * Cfg::SFB_STAGE, &p.map_sfb, bar, 0, sfb_y0 + kt * 8);
+                    tma_load_2d_pair(sSFB + s * Cfg::SFB_STAGE + 1024, &p.map_sfb, bar, 0, sfb_y1 + kt * 8);
+                    armed[s] = it / STAGES + 1u;
+                }
+            }
+            // Drain.  The leader waits until the last armed phase of every stage has
+            // landed (its full barriers count both CTAs' bytes); both CTAs wait until
+            // the MMAs have released every stage they were given, so no commit is
+            // still on its way to this CTA's barriers when it exits.
+#pragma unroll
+            for (int s = 0; s < STAGES; ++s) {
+                if (!armed[s]) continue;
+                if (rank == 0) wait_bounded(&full[s], (armed[s] - 1u) & 1u, p.wait_ns, p.status);
+                wait_bounded(&empty[s], (armed[s] - 1u) & 1u, p.wait_ns, p.status);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- tensor-core issuer (leader CTA)
+        if (elect_one()) {
+            if (rank == 0) {
+                constexpr uint32_t idesc = idesc_mxf4(256, 256);
+                uint32_t it = 0, tcount = 0;
+                bool ok = true;
+                for (int64_t tile = cluster; ok && tile < num_tiles; tile += num_clusters, ++tcount) {
+                    for (int kt = 0; kt < num_k; ++kt, ++it) {
+                        const int s = (int)(it % STAGES);
+                        const uint32_t ph = (it / STAGES) & 1u;
+                        if (!wait_bounded(&full[s], ph, p.wait_ns, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sfa_t = tmem_base + 256 + s * Cfg::SF_COLS;
+                        const uint32_t sfb_t = sfa_t + 8;
+#pragma unroll
+                        for (int a = 0; a < 2; ++a)
+                            tc_cp_32x128b_warpx4_pair(
+                                sfa_t + a * 4,
+                                smem_desc(smem_u32(sSFA + s * Cfg::SFA_STAGE + a * 512), 0, 128, kSwizzleNone));
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+#pragma unroll
+                            for (int a = 0; a < 2; ++a)
+                                tc_cp_32x128b_warpx4_pair(
+                                    sfb_t + a * 8 + j * 4,
+                                    smem_desc(smem_u32(sSFB + s * Cfg::SFB_STAGE + j * 1024 + a * 512), 0, 128,
+                                              kSwizzleNone));
+                        // The scale copies above go to their own TMEM columns, so the
+                        // accumulator is waited for only now: the copies of a tile's first
+                        // stage overlap the epilogue's read-out of the previous tile.
+                        if (kt == 0 && tcount > 0) {
+                            if (!wait_bounded(acc_empty, (tcount - 1u) & 1u, p.wait_ns, p.status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        const uint32_t a_base = smem_u32(sA + s * Cfg::A_STAGE);
+                        const uint32_t b_base = smem_u32(sB + s * Cfg::B_STAGE);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t sf_id = (uint32_t)(k & 1) * 2u;
+                            tc_mma_mxf4_pair(tmem_base, smem_desc(a_base + k * 32, 16, 1024, kSwizzle128B),
+                                             smem_desc(b_base + k * 32, 16, 1024, kSwizzle128B),
+                                             idesc_with_sf_ids(idesc, sf_id, sf_id), sfa_t + (k >> 1) * 4,
+                                             sfb_t + (k >> 1) * 8, (kt | k) != 0);
+                        }
+                        tc_commit_pair(&empty[s], 0x3);
+                    }
+                    if (ok) tc_commit_pair(acc_full, 0x3);
+                }
+                tc_commit_pair(mma_done, 0x3);
+            }
+            // Both CTAs: every MMA of the pair has completed (and this CTA's mma_done
+            // arrival has landed) before TMEM is released.
+            wait_bounded(mma_done, 0, p.wait_ns, p.status);
+        }
+    } else {
+        // ---------------- epilogue (both CTAs): the CTA's 128 rows of the tile
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        uint8_t* stg = smem + Cfg::OFF_STG + (warp - 2) * STG_WARP_BYTES;
+        const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
+        uint32_t tcount = 0;
+        for (int64_t tile = cluster; tile < num_tiles; tile += num_clusters, ++tcount) {
+            if (!wait_bounded(acc_full, tcount & 1u, p.wait_ns, p.status)) break;
+            tc_fence_after();
+            const int64_t row_base = (tile / num_n) * 256 + rank * 128 + q * 32;
+            const int64_t c0 = (tile % num_n) * 256 + h * 128;
+            uint32_t v[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128 + c * 32), v[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            // The TMEM reads above have completed (wait::ld); the arrive only reports it.
+            if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#if MXG_TMA_STORE
+                store_chunk_tma(p, stg, lane, row_base, c0 + c * 32, v[c]);
+#else
+                store_chunk(p, stg, lane, row_base, c0 + c * 32, v[c]);
+#endif
+            }
+        }
+#if MXG_TMA_STORE
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+#endif
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // neither CTA frees TMEM or exits while the pair may still use it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
 template <int BN, int STAGES, int ACC>
 cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
     using Cfg = GemmCfg<BN, STAGES, ACC>;
@@ -381,11 +634,56 @@ cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+
+template <int STAGES>
+cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
+    using Cfg = PairCfg<STAGES>;
+    auto kern = mxf4_gemm_pair_kernel<STAGES>;
+    static bool configured[64] = {};
+    static int max_clusters[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3((unsigned)(sms & ~1));
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        max_clusters[dev] = n;
+        configured[dev] = true;
+    }
+    const int64_t tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
+    const int64_t clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 }  // namespace
 
-// Persistent launch: one CTA per SM walks the 128 x BN output tiles; BN = 256 unless
-// the whole N fits in 128 columns.
+// Persistent launches.  M > 128 and N > 128: clusters of two CTAs walk 256 x 256
+// tiles (as many clusters as fit at once).  Otherwise one CTA per SM walks 128 x BN
+// tiles, BN = 256 unless the whole N fits in 128 columns.
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s) {
+#if MXG_PAIR
+    if (p.M > 128 && p.N > 128) return launch_pair<MXG_PAIR_STAGES>(p, s);
+#endif
     if (p.N <= 128) return launch_cfg<128, 6, 2>(p, s);
 #ifdef MXG_FORCE_BN128
     return launch_cfg<128, 6, 2>(p, s);

@@ -46,6 +46,8 @@ struct GemmParams {
     CUtensorMap map_a;   // codes of A [M, K/2] bytes, box 128 rows x 128 B, 128B swizzle
     CUtensorMap map_b;   // codes of B [N, K/2] bytes
     CUtensorMap map_c;   // output C [M, N]: box 64 bytes x 32 rows, 64-byte swizzle
+    CUtensorMap map_sfa;  // MMA-order scales of A as [atoms * 4, 128] bytes, box 128 B x 8 rows
+    CUtensorMap map_sfb;  // same for B
     const uint8_t* sfa;  // MMA-order scales of A
     const uint8_t* sfb;  // MMA-order scales of B
     int64_t M, N, K, kb_pad;
@@ -60,7 +62,7 @@ struct GemmParams {
 
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s);
 
-cudaError_t run_mma_peak_probe(int kind, int64_t iters, float* ms, uint32_t* status, uint64_t wait_ns);
+cudaError_t run_mma_peak_probe(int kind, int64_t iters, float* ms, int* ctas, uint32_t* status, uint64_t wait_ns);
 
 cudaError_t launch_error_decomposition(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
                                        double* out, cudaStream_t s);
@@ -72,6 +74,7 @@ mxfp4_status record_error(mxfp4_status st, const char* fmt, ...);
 bool encode_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t cols, uint32_t box_rows);
 bool encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld);
 bool encode_out_map(CUtensorMap* map, void* c, int64_t rows, int64_t cols, int64_t ldc, bool bf16);
+bool encode_sf_map(CUtensorMap* map, const void* scales, int64_t rows, int64_t cols);
 uint64_t quant_wait_ns();  // bounded-wait limit of the calling host thread
 
 }  // namespace mx

@@ -163,6 +163,21 @@ bool encode_out_map(CUtensorMap* map, void* c, int64_t rows, int64_t cols, int64
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D tensor map over MMA-order scale factors of a [rows, cols] operand, viewed as
+// [512-byte atoms x 4, 128] bytes: box = 128 bytes x 8 rows, i.e. the two atoms (128
+// rows x 8 blocks) of one 256-element K stage; no swizzle, zero fill out of bounds.
+bool encode_sf_map(CUtensorMap* map, const void* scales, int64_t rows, int64_t cols) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {128, (cuuint64_t)(sf_rows_pad(rows) * sf_kb_pad(cols) / 128)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, 8};
+    const cuuint32_t estr[2] = {1, 1};
+    return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(scales), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mx
 
 using namespace mx;
@@ -366,7 +381,8 @@ mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, i
     GemmParams p{};
     if (!encode_codes_map(&p.map_a, A->codes, A->rows, A->cols, 128) ||
         !encode_codes_map(&p.map_b, B->codes, B->rows, B->cols, 128) ||
-        !encode_out_map(&p.map_c, C, A->rows, B->rows, ldc, out_dtype == MXFP4_OUT_BF16))
+        !encode_out_map(&p.map_c, C, A->rows, B->rows, ldc, out_dtype == MXFP4_OUT_BF16) ||
+        !encode_sf_map(&p.map_sfa, A->scales, A->rows, A->cols) || !encode_sf_map(&p.map_sfb, B->scales, B->rows, B->cols))
         return fail(MXFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     p.sfa = A->scales;
     p.sfb = B->scales;
@@ -413,17 +429,16 @@ mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols
 }
 
 mxfp4_status mxfp4_mma_peak_probe(int kind, int64_t iters, double* tflops) {
-    if (kind < 0 || kind > 2) return fail(MXFP4_ERR_INVALID_ARG, "kind must be 0, 1 or 2");
+    if (kind < 0 || kind > 4) return fail(MXFP4_ERR_INVALID_ARG, "kind must be 0 to 4");
     if (iters <= 0 || !tflops) return fail(MXFP4_ERR_INVALID_ARG, "iters must be positive and tflops non-NULL");
-    int dev, sms = 0;
+    int dev, ctas = 0;
     mxfp4_status st;
     if ((st = check_device(&dev))) return st;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     float ms = 0.0f;
-    cudaError_t e = run_mma_peak_probe(kind, iters, &ms, device_status_ptr(), wait_limit());
+    cudaError_t e = run_mma_peak_probe(kind, iters, &ms, &ctas, device_status_ptr(), wait_limit());
     if (e != cudaSuccess) return cuda_fail(e, "mma peak probe");
     const double k = kind == 2 ? 16.0 : 64.0;  // K per instruction
-    *tflops = (double)sms * (double)iters * 2.0 * 128.0 * 256.0 * k / (ms * 1e-3) / 1e12;
+    *tflops = (double)ctas * (double)iters * 2.0 * 128.0 * 256.0 * k / (ms * 1e-3) / 1e12;
     return ok();
 }
 

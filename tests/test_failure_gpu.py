@@ -11,11 +11,12 @@ from tests.gpu_util import assert_within, gpu_ready
 pytestmark = pytest.mark.gpu
 
 
-def test_bounded_wait_timeout_is_reported(  ):
+@pytest.mark.parametrize("M", [256, 128])  # CTA-pair kernel, single-CTA kernel
+def test_bounded_wait_timeout_is_reported(M):
     torch = gpu_ready()
     from mxfp4_precision_gemms_gb300 import binding as mx
 
-    X, W, _ = synth.linear_inputs(256, 256, 1024, 21)
+    X, W, _ = synth.linear_inputs(M, 256, 1024, 21)
     qa, qb = oracle.quantize(X, 16, 0, "row"), oracle.quantize(W, 16, 0, "row")
     A, B = mx.qtensor_from_host(*qa), mx.qtensor_from_host(*qb)
     assert mx.device_status() == 0

@@ -53,7 +53,23 @@ def test_single_block_scales(torch, N):
     assert_within(got, want, S, what="single block")
 
 
-@pytest.mark.parametrize("shape", [(128, 128, 256), (256, 512, 512), (128, 128, 2048), (384, 256, 1024)])
+def test_single_block_scales_pair(torch):
+    """CTA-pair tiles (M, N > 128): every row of A and of B has its own scale in each of
+    the two K blocks, so a scale read from the wrong CTA, row group or block gives an
+    exact power-of-two error in that quadrant of the 256 x 256 tile."""
+    M, N, K = 512, 512, 64
+    g = np.random.default_rng(1)
+    ca = g.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    cb = g.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = (110 + (np.arange(M)[:, None] * 7 + np.arange(K // 32)[None, :] * 3) % 23).astype(np.uint8)
+    sb = (105 + (np.arange(N)[:, None] * 5 + np.arange(K // 32)[None, :] * 11) % 31).astype(np.uint8)
+    want, S = oracle.gemm(ca, sa, cb, sb)
+    got = run(torch, (ca, sa), (cb, sb))
+    assert_within(got, want, S, what="pair single block")
+
+
+@pytest.mark.parametrize("shape", [(128, 128, 256), (256, 512, 512), (128, 128, 2048), (384, 256, 1024),
+                                   (300, 520, 768)])
 def test_aligned_shapes(torch, shape):
     M, N, K = shape
     qa, qb = oracle_operands(M, N, K, 10)
