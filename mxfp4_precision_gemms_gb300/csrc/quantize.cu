@@ -5,32 +5,50 @@
 //   Hadamard before quantisation), D (1x32 row, 32x1 column-transposed, 32x32 2D).
 // "Decomposing MXFP4 quantization error ...": E8M0 scales, E2M1 grid, ceiling scale.
 //
-// One CTA owns a 128 x 128 tile of the bf16 input and reads it from HBM once.
-//  - Row work: each thread owns two 32-element row segments (rows r and r + 64) in
+// One CTA (2 threads per tile row) owns a TR x 128 tile of the bf16 input and reads it
+// from HBM once.
+//  - Row work: each thread owns two 32-element row segments (rows r and r + TR/2) in
 //    registers and processes them in lockstep with packed f32x2 instructions:
 //    rotation butterfly, block amax, E8M0 byte, 2 x 32 codes -> two 16-byte stores.
-//  - Column work (transposed copy): the tile is staged in shared memory (16-byte
-//    chunks XOR-swizzled so that both the row-wise writes and the column-wise reads
-//    are bank-conflict free); each thread then owns two adjacent columns of one
-//    32-row block (one 32-bit shared load gives both columns' values).
+//  - Column work (transposed copy): the row work also leaves the tile in shared memory
+//    (fp32 or raw bf16, swizzled so that the row-wise writes and the column-wise reads
+//    are bank-conflict free); each thread then owns two adjacent columns of one 32-row
+//    block, one shared load per row giving both columns' values.
 //  - 2D work: row segments as above, the per-segment amax is combined over the 32
-//    rows of the tile through shared memory.
-// The kernel is HBM-bound: 2 B read and 0.53 B (single) or 1.06 B (row + column)
-// written per element.
+//    rows of the block through shared memory.
+// Per element the kernel moves 2 B in and 0.53 B (single) or 1.06 B (row + column)
+// out; the dual pass is bound by instruction issue as much as by HBM.
 #include "internal.h"
 #include "ptx.cuh"
-
-// 1: TMA-fed producer/consumer kernel (rq_tma_kernel); 0: one tile per CTA (rq_kernel).
-#ifndef MXQ_TMA
-#define MXQ_TMA 0
-#endif
 
 namespace mx {
 namespace {
 
-constexpr int TR = 128;  // tile rows
-constexpr int TC = 128;  // tile cols
-constexpr int QTHREADS = 256;
+// Tuning knobs (compile-time): tile rows (32, 64 or 128; 2 threads per tile row) and
+// the type the tile is staged in for the column work (1: fp32, 0: the raw bf16).
+// Measured on GB300 (dual copy, 8192 x 14336): 64 rows / bf16 3.63 TB/s, 64 / fp32
+// 2.81, 128 / bf16 3.31, 128 / fp32 2.72.
+#ifndef MXQ_ROWS
+#define MXQ_ROWS 64
+#endif
+#ifndef MXQ_STAGE_F32
+#define MXQ_STAGE_F32 0
+#endif
+constexpr int TR = MXQ_ROWS;  // tile rows
+constexpr int TC = 128;       // tile cols
+constexpr int QTHREADS = 2 * TR;
+constexpr int QBLOCKS_PER_SM = 512 / QTHREADS;
+constexpr bool STAGE_F32 = MXQ_STAGE_F32 != 0;
+constexpr int TILE_BYTES = STAGE_F32 ? TR * TC * 4 : TR * TC * 2;
+static_assert(TR == 32 || TR == 64 || TR == 128, "tile rows");
+
+// 1: persistent TMA-fed kernel (rq_tma_kernel); 0: one tile per CTA (rq_kernel).
+#ifndef MXQ_TMA
+#define MXQ_TMA 0
+#endif
+#ifndef MXQ_STAGES
+#define MXQ_STAGES 3
+#endif
 
 // Packed fp32 pairs: one instruction performs two independent IEEE fp32 operations
 // (round to nearest even, subnormals kept), so results equal the scalar ones.
@@ -88,15 +106,22 @@ __device__ __forceinline__ void rotate32x2(float2 (&v)[32]) {
     }
 }
 
+// Three-input fp32 maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Block amax of the rotated values (x and y vectors).  For H16 the butterfly output
 // still carries the factor 4, removed exactly here.
 template <int HAD>
 __device__ __forceinline__ void amax32x2(const float2 (&v)[32], float& ax, float& ay) {
     float mx = 0.0f, my = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        mx = fmaxf(mx, fabsf(v[i].x));
-        my = fmaxf(my, fabsf(v[i].y));
+    for (int i = 0; i < 32; i += 2) {
+        mx = fmax3(mx, fabsf(v[i].x), fabsf(v[i + 1].x));
+        my = fmax3(my, fabsf(v[i].y), fabsf(v[i + 1].y));
     }
     if constexpr (HAD == 16) {
         mx *= 0.25f;
@@ -156,49 +181,55 @@ __device__ __forceinline__ void store_scale(const QuantOut& o, int64_t r, int64_
     o.scales[off] = (uint8_t)byte;
 }
 
-// Swizzled position (in 32-bit words) of 16-byte chunk q of tile row r: the row-wise
-// writes (4 threads per row) and the column-wise reads (32 consecutive words of one
-// row per warp) both hit 32 distinct banks.
-[[maybe_unused]] __device__ __forceinline__ int tile_chunk(int r, int q) { return (q ^ ((q >> 2) & 3) ^ ((r & 1) << 2)) * 4; }
+// Staged tile, fp32: float index of 16-byte chunk c (0..31) of row r, stored at
+// c ^ (r % 8).  Row-wise float4 writes (8 rows x 4 segments per warp) and column-wise
+// float2 reads (32 column pairs of one row per warp) are both bank-conflict free.
+__device__ __forceinline__ int f32_chunk(int r, int c) { return r * TC + ((c ^ (r & 7)) << 2); }
+// Staged tile, bf16: 32-bit word index of 16-byte chunk q (0..15) of row r, with the
+// same property for row-wise uint4 writes and column-wise 32-bit reads.
+__device__ __forceinline__ int bf16_chunk(int r, int q) {
+    return r * (TC / 2) + ((q ^ ((q >> 2) & 3) ^ ((r & 1) << 2)) << 2);
+}
 
 template <int HAD, bool ROW, bool COLT, bool TWOD>
-__global__ void __launch_bounds__(QTHREADS, 2) rq_kernel(const QuantParams p) {
-    __shared__ __align__(16) uint32_t tile[COLT ? TR * (TC / 2) : 4];
-    __shared__ float seg_amax[TWOD ? TR * 4 : 1];
+__global__ void __launch_bounds__(QTHREADS, QBLOCKS_PER_SM) rq_kernel(const QuantParams p) {
+    extern __shared__ __align__(16) uint8_t q_smem[];
+    float* tile_f = reinterpret_cast<float*>(q_smem);
+    uint32_t* tile_w = reinterpret_cast<uint32_t*>(q_smem);
+    float* seg_amax = reinterpret_cast<float*>(q_smem + (COLT ? TILE_BYTES : 0));
 
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.y * TR;
     const int64_t col0 = (int64_t)blockIdx.x * TC;
 
-    // ---- two row segments owned by this thread: rows pr and pr + 64, columns 32*s ..
+    // ---- two row segments owned by this thread: rows pr and pr + TR/2, columns 32*s ..
     const int s = t & 3, pr = t >> 2;
-    const int rx = pr, ry = pr + 64;
+    const int rx = pr, ry = pr + TR / 2;
     const int64_t gc = col0 + 32 * s;
     const int64_t grx = row0 + rx, gry = row0 + ry;
     const bool vx = grx < p.R && gc < p.C, vy = gry < p.R && gc < p.C;
-    uint4 raw_x[4], raw_y[4];
+    float2 v[32];
+    {
+        uint4 raw_x[4], raw_y[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) raw_x[j] = raw_y[j] = make_uint4(0, 0, 0, 0);
-    if (vx) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + grx * p.ld + gc);
+        for (int j = 0; j < 4; ++j) raw_x[j] = raw_y[j] = make_uint4(0, 0, 0, 0);
+        if (vx) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.x + grx * p.ld + gc);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) raw_x[j] = __ldcs(src + j);
-    }
-    if (vy) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + gry * p.ld + gc);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) raw_y[j] = __ldcs(src + j);
-    }
-    if constexpr (COLT) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            *reinterpret_cast<uint4*>(&tile[rx * (TC / 2) + tile_chunk(rx, 4 * s + j)]) = raw_x[j];
-            *reinterpret_cast<uint4*>(&tile[ry * (TC / 2) + tile_chunk(ry, 4 * s + j)]) = raw_y[j];
+            for (int j = 0; j < 4; ++j) raw_x[j] = __ldcs(src + j);
         }
-    }
-
-    if constexpr (ROW || TWOD) {
-        float2 v[32];
+        if (vy) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.x + gry * p.ld + gc);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) raw_y[j] = __ldcs(src + j);
+        }
+        if constexpr (COLT && !STAGE_F32) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                *reinterpret_cast<uint4*>(&tile_w[bf16_chunk(rx, 4 * s + j)]) = raw_x[j];
+                *reinterpret_cast<uint4*>(&tile_w[bf16_chunk(ry, 4 * s + j)]) = raw_y[j];
+            }
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t a[4] = {raw_x[j].x, raw_x[j].y, raw_x[j].z, raw_x[j].w};
@@ -210,6 +241,18 @@ __global__ void __launch_bounds__(QTHREADS, 2) rq_kernel(const QuantParams p) {
                     make_float2(__uint_as_float(a[i] & 0xFFFF0000u), __uint_as_float(b[i] & 0xFFFF0000u));
             }
         }
+    }
+    if constexpr (COLT && STAGE_F32) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            *reinterpret_cast<float4*>(&tile_f[f32_chunk(rx, 8 * s + j)]) =
+                make_float4(v[4 * j].x, v[4 * j + 1].x, v[4 * j + 2].x, v[4 * j + 3].x);
+            *reinterpret_cast<float4*>(&tile_f[f32_chunk(ry, 8 * s + j)]) =
+                make_float4(v[4 * j].y, v[4 * j + 1].y, v[4 * j + 2].y, v[4 * j + 3].y);
+        }
+    }
+
+    if constexpr (ROW || TWOD) {
         rotate32x2<HAD>(v);
         float ax, ay;
         amax32x2<HAD>(v, ax, ay);
@@ -256,13 +299,18 @@ __global__ void __launch_bounds__(QTHREADS, 2) rq_kernel(const QuantParams p) {
         const int cp = t & 63, rb = t >> 6;
         const int64_t gcol = col0 + 2 * cp, grow = row0 + 32 * rb;
         if (gcol < p.C && grow < p.R) {
-            float2 v[32];
-            const int q = cp >> 2, wi = cp & 3;
+            if constexpr (STAGE_F32) {
+                const int c = cp >> 1, half = (cp & 1) * 2;  // chunk holding columns 2cp, 2cp + 1
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int rr = 32 * rb + i;
-                const uint32_t w = tile[rr * (TC / 2) + tile_chunk(rr, q) + wi];
-                v[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+                for (int i = 0; i < 32; ++i)
+                    v[i] = *reinterpret_cast<const float2*>(&tile_f[f32_chunk(32 * rb + i, c) + half]);
+            } else {
+                const int q = cp >> 2, wi = cp & 3;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const uint32_t w = tile_w[bf16_chunk(32 * rb + i, q) + wi];
+                    v[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+                }
             }
             rotate32x2<HAD>(v);
             float ax, ay;
@@ -278,27 +326,50 @@ __global__ void __launch_bounds__(QTHREADS, 2) rq_kernel(const QuantParams p) {
     }
 }
 
-// ---------------------------------------------------------------------------------
-// TMA-fed variant: persistent CTAs (two per SM) walk 128 x 128 tiles; thread 0 keeps
-// the next Q_STAGES - 1 tiles of its CTA in flight (two 64-column boxes per tile,
-// 128-byte swizzle) while all 256 threads process the current one.  The arithmetic
-// is the same as rq_kernel's.
-constexpr int Q_STAGES = 3;
-constexpr int Q_TILE_BYTES = TR * TC * 2;  // 32 KB
-constexpr int Q_BOX_BYTES = Q_TILE_BYTES / 2;
-constexpr int Q_OFF_BAR = Q_STAGES * Q_TILE_BYTES;
-constexpr int Q_OFF_AMAX = Q_OFF_BAR + Q_STAGES * 8;
-constexpr int Q_TMA_SMEM = Q_OFF_AMAX + TR * 4 * 4 + 1024;
+template <int HAD, bool ROW, bool COLT, bool TWOD>
+cudaError_t launch_one(const QuantParams& p, cudaStream_t s) {
+    constexpr int smem = (COLT ? TILE_BYTES : 0) + (TWOD ? TR * 4 * 4 : 0);
+    auto kern = rq_kernel<HAD, ROW, COLT, TWOD>;
+    if constexpr (smem > 48 * 1024) {
+        static bool configured[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!configured[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
+    const dim3 grid((unsigned)((p.C + TC - 1) / TC), (unsigned)((p.R + TR - 1) / TR));
+    kern<<<grid, QTHREADS, smem, s>>>(p);
+    return cudaGetLastError();
+}
 
-// Word offset (32-bit units) of 16-byte chunk `chunk` (0..15) of tile row r in the
-// swizzled stage: columns 0-63 are box 0, 64-127 box 1; within a box a row is 128 B
-// with chunk c stored at c ^ (r % 8).
-__device__ __forceinline__ int sw_word(int r, int chunk) {
-    return ((chunk >> 3) * Q_BOX_BYTES + r * 128 + (((chunk & 7) ^ (r & 7)) << 4)) >> 2;
+// ---------------------------------------------------------------------------------
+// Persistent TMA-fed variant.  CTAs (QBLOCKS_PER_SM per SM) walk TR x 128 tiles; thread
+// 0 keeps the next Q_STAGES - 1 tiles of its CTA in flight as two 64-column TMA boxes
+// each (128-byte swizzle), so no thread waits on a global load it has just issued.
+// The row work and the column work both read the staged tile, with the same
+// arithmetic as rq_kernel.
+constexpr int Q_STAGES = MXQ_STAGES;
+constexpr int Q_TILE_BYTES = TR * TC * 2;
+constexpr int Q_BOX_BYTES = Q_TILE_BYTES / 2;  // 64 columns
+constexpr int Q_OFF_BAR = Q_STAGES * Q_TILE_BYTES;
+constexpr int Q_OFF_AMAX = Q_OFF_BAR + 8 * Q_STAGES;
+constexpr int Q_TMA_SMEM = Q_OFF_AMAX + TR * 4 * 4 + 1024;  // + alignment slack
+static_assert(Q_TILE_BYTES % 1024 == 0 && Q_BOX_BYTES % 1024 == 0, "128-byte swizzle atoms");
+
+// 32-bit word index of 16-byte chunk c (0..15) of tile row r in a stage: columns 0-63
+// are box 0, 64-127 box 1; within a box row r is 128 B with chunk c at (c % 8) ^ (r % 8).
+// Row-wise 16-byte reads (8 rows x 4 segments per warp) and column-wise 32-bit reads
+// (32 column pairs of one row per warp) are both bank-conflict free.
+__device__ __forceinline__ int stage_word(int r, int c) {
+    return ((c >> 3) * Q_BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4)) >> 2;
 }
 
 template <int HAD, bool ROW, bool COLT, bool TWOD>
-__global__ void __launch_bounds__(QTHREADS, 2) rq_tma_kernel(const __grid_constant__ QuantTmaParams P) {
+__global__ void __launch_bounds__(QTHREADS, QBLOCKS_PER_SM) rq_tma_kernel(const __grid_constant__ QuantTmaParams P) {
     const QuantParams& p = P.p;
     extern __shared__ uint8_t q_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_raw) + 1023) & ~uintptr_t(1023));
@@ -327,7 +398,8 @@ __global__ void __launch_bounds__(QTHREADS, 2) rq_tma_kernel(const __grid_consta
 
     uint32_t i = 0;
     for (int64_t tile = blockIdx.x; tile < P.tiles; tile += gridDim.x, ++i) {
-        // the stage refilled here was released by the __syncthreads ending iteration i - 1
+        // The stage refilled here held tile i - 1, released by the __syncthreads that
+        // ended the previous iteration.
         if (t == 0) issue(i + Q_STAGES - 1);
         const int st = (int)(i % Q_STAGES);
         const bool landed = wait_bounded(&full[st], (i / Q_STAGES) & 1u, P.wait_ns, P.status);
@@ -336,15 +408,15 @@ __global__ void __launch_bounds__(QTHREADS, 2) rq_tma_kernel(const __grid_consta
 
         if constexpr (ROW || TWOD) {
             const int s = t & 3, pr = t >> 2;
-            const int rx = pr, ry = pr + 64;
+            const int rx = pr, ry = pr + TR / 2;
             const int64_t gc = col0 + 32 * s;
             const int64_t grx = row0 + rx, gry = row0 + ry;
             const bool vx = landed && grx < p.R && gc < p.C, vy = landed && gry < p.R && gc < p.C;
             float2 v[32];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint4 a4 = *reinterpret_cast<const uint4*>(&buf[sw_word(rx, 4 * s + j)]);
-                const uint4 b4 = *reinterpret_cast<const uint4*>(&buf[sw_word(ry, 4 * s + j)]);
+                const uint4 a4 = *reinterpret_cast<const uint4*>(&buf[stage_word(rx, 4 * s + j)]);
+                const uint4 b4 = *reinterpret_cast<const uint4*>(&buf[stage_word(ry, 4 * s + j)]);
                 const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
                 const uint32_t b[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
@@ -399,11 +471,10 @@ __global__ void __launch_bounds__(QTHREADS, 2) rq_tma_kernel(const __grid_consta
             const int64_t gcol = col0 + 2 * cp, grow = row0 + 32 * rb;
             if (landed && gcol < p.C && grow < p.R) {
                 float2 v[32];
-                const int chunk = cp >> 2, wi = cp & 3;  // 16-byte chunk of the row holding columns 2cp, 2cp+1
+                const int chunk = cp >> 2, wi = cp & 3;  // 16-byte chunk holding columns 2cp, 2cp + 1
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    const int rr = 32 * rb + k;
-                    const uint32_t w = buf[sw_word(rr, chunk) + wi];
+                    const uint32_t w = buf[stage_word(32 * rb + k, chunk) + wi];
                     v[k] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
                 }
                 rotate32x2<HAD>(v);
@@ -420,27 +491,31 @@ __global__ void __launch_bounds__(QTHREADS, 2) rq_tma_kernel(const __grid_consta
         }
         __syncthreads();  // every thread is done with this stage (and with seg_amax)
     }
-    // every copy this CTA issued has been waited for by the loop above (issue only
-    // targets tiles the loop visits), so nothing is in flight at exit.
+    // Every copy this CTA issued targets a tile the loop above waited for, so nothing
+    // is in flight at exit.
 }
 
 template <int HAD, bool ROW, bool COLT, bool TWOD>
-cudaError_t launch_tma(const QuantTmaParams& P, cudaStream_t st) {
+cudaError_t launch_tma_one(const QuantTmaParams& P, cudaStream_t st) {
     auto kern = rq_tma_kernel<HAD, ROW, COLT, TWOD>;
     static bool configured[64] = {};
-    static int sms[64] = {};
+    static int grid_max[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_TMA_SMEM);
         if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        int sms = 0, per_sm = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, QTHREADS, Q_TMA_SMEM);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        grid_max[dev] = sms * per_sm;
         configured[dev] = true;
     }
-    const int64_t max_grid = 2 * (int64_t)sms[dev];
-    const unsigned grid = (unsigned)(P.tiles < max_grid ? P.tiles : max_grid);
+    const unsigned grid = (unsigned)(P.tiles < grid_max[dev] ? P.tiles : grid_max[dev]);
     kern<<<grid, QTHREADS, Q_TMA_SMEM, st>>>(P);
     return cudaGetLastError();
 }
@@ -449,13 +524,13 @@ template <int HAD>
 cudaError_t launch_had_tma(const QuantTmaParams& P, unsigned layouts, cudaStream_t s) {
     switch (layouts) {
         case MXFP4_LAYOUT_ROW:
-            return launch_tma<HAD, true, false, false>(P, s);
+            return launch_tma_one<HAD, true, false, false>(P, s);
         case MXFP4_LAYOUT_COLT:
-            return launch_tma<HAD, false, true, false>(P, s);
+            return launch_tma_one<HAD, false, true, false>(P, s);
         case MXFP4_LAYOUT_ROW | MXFP4_LAYOUT_COLT:
-            return launch_tma<HAD, true, true, false>(P, s);
+            return launch_tma_one<HAD, true, true, false>(P, s);
         case MXFP4_LAYOUT_2D:
-            return launch_tma<HAD, false, false, true>(P, s);
+            return launch_tma_one<HAD, false, false, true>(P, s);
         default:
             return cudaErrorInvalidValue;
     }
@@ -463,24 +538,18 @@ cudaError_t launch_had_tma(const QuantTmaParams& P, unsigned layouts, cudaStream
 
 template <int HAD>
 cudaError_t launch_had(const QuantParams& p, unsigned layouts, cudaStream_t s) {
-    const dim3 grid((unsigned)((p.C + TC - 1) / TC), (unsigned)((p.R + TR - 1) / TR));
     switch (layouts) {
         case MXFP4_LAYOUT_ROW:
-            rq_kernel<HAD, true, false, false><<<grid, QTHREADS, 0, s>>>(p);
-            break;
+            return launch_one<HAD, true, false, false>(p, s);
         case MXFP4_LAYOUT_COLT:
-            rq_kernel<HAD, false, true, false><<<grid, QTHREADS, 0, s>>>(p);
-            break;
+            return launch_one<HAD, false, true, false>(p, s);
         case MXFP4_LAYOUT_ROW | MXFP4_LAYOUT_COLT:
-            rq_kernel<HAD, true, true, false><<<grid, QTHREADS, 0, s>>>(p);
-            break;
+            return launch_one<HAD, true, true, false>(p, s);
         case MXFP4_LAYOUT_2D:
-            rq_kernel<HAD, false, false, true><<<grid, QTHREADS, 0, s>>>(p);
-            break;
+            return launch_one<HAD, false, false, true>(p, s);
         default:
             return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -489,7 +558,7 @@ cudaError_t launch_rotate_quantize(const QuantParams& p, int had, unsigned layou
 #if MXQ_TMA
     QuantTmaParams P{};
     P.p = p;
-    if (!encode_bf16_map(&P.map_x, p.x, p.R, p.C, p.ld)) return cudaErrorInvalidValue;
+    if (!encode_bf16_map(&P.map_x, p.x, p.R, p.C, p.ld, TR)) return cudaErrorInvalidValue;
     P.tiles_c = (p.C + TC - 1) / TC;
     P.tiles = P.tiles_c * ((p.R + TR - 1) / TR);
     P.status = device_status_ptr();
