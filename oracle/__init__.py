@@ -70,6 +70,13 @@ def lib():
             L.oracle_gemm.argtypes = [P, P, P, P, I64, I64, I64, P, P]
             L.oracle_dot_pairs.argtypes = [P, P, P, P, I64, I64, P, P]
             L.oracle_error_decomposition.argtypes = [P, I64, I64, I64, I, I, P]
+            L.oracle_quantize_f32_rows.argtypes = [P, I64, I64, I, P, P]
+            L.oracle_quantize_of_row.argtypes = [P, I64, I64, I64, I, I, I, P, P, P, P]
+            L.oracle_quantize_of_row.restype = I64
+            L.oracle_mbs_byte.argtypes = [ctypes.c_float]
+            L.oracle_mbs_byte.restype = I
+            L.oracle_quantize_mbs_row.argtypes = [P, I64, I64, I64, I, I, P, P, P]
+            L.oracle_dequant_mbs_row.argtypes = [P, P, P, I64, I64, P]
             L.oracle_num_threads.restype = I
             L.oracle_set_num_threads.argtypes = [I]
             _lib = L
@@ -270,3 +277,53 @@ def error_decomposition(x_bf16, had, mode):
     lib().oracle_error_decomposition(_p(x), R, C, C, had, mode, _p(out))
     keys = ("e2", "scale2", "dz2", "grid2", "scale_grid", "n_deadzone", "n")
     return dict(zip(keys, out.tolist()))
+
+
+# --------------------------------------------------------------------------- quantiser fixes
+# "Decomposing MXFP4 quantization error ...", the MBS and OF fixes (row layout).
+def quantize_f32_rows(v: np.ndarray, mode: int):
+    """Quantise fp32 values [R, C] in 32-blocks along C, without rotation."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    R, C = v.shape
+    codes = np.zeros((R, C // 2), np.uint8)
+    scales = np.zeros((R, C // 32), np.uint8)
+    lib().oracle_quantize_f32_rows(_p(v), R, C, mode, _p(codes), _p(scales))
+    return codes, scales
+
+
+def quantize_of(x_bf16: np.ndarray, had: int, mode: int, alpha_log2: int = -1):
+    """Outlier fallback: q1 = Q(x), q2 = Q(x - dq(q1)) with alpha = 2^alpha_log2 folded
+    into q2's scale bytes, so x_OF = dq(q1) + dq(q2).  Returns (c1, s1, c2, s2,
+    number of residuals that were not exact in fp32)."""
+    x = _u16(x_bf16)
+    R, C = x.shape
+    c1 = np.zeros((R, C // 2), np.uint8)
+    s1 = np.zeros((R, C // 32), np.uint8)
+    c2 = np.zeros((R, C // 2), np.uint8)
+    s2 = np.zeros((R, C // 32), np.uint8)
+    bad = lib().oracle_quantize_of_row(_p(x), R, C, C, had, mode, int(alpha_log2), _p(c1), _p(s1), _p(c2), _p(s2))
+    return c1, s1, c2, s2, int(bad)
+
+
+def mbs_byte(amax: float) -> int:
+    return lib().oracle_mbs_byte(float(amax))
+
+
+def quantize_mbs(x_bf16: np.ndarray, had: int, mode: int):
+    """Macro-block scaling: returns (codes [R, C/2], scales [R, C/32], mbs [R, C/128])."""
+    x = _u16(x_bf16)
+    R, C = x.shape
+    assert C % 128 == 0
+    codes = np.zeros((R, C // 2), np.uint8)
+    scales = np.zeros((R, C // 32), np.uint8)
+    mbs = np.zeros((R, C // 128), np.uint8)
+    lib().oracle_quantize_mbs_row(_p(x), R, C, C, had, mode, _p(codes), _p(scales), _p(mbs))
+    return codes, scales, mbs
+
+
+def dequant_mbs(codes, scales, mbs) -> np.ndarray:
+    codes, scales, mbs = (np.ascontiguousarray(a) for a in (codes, scales, mbs))
+    R, C = codes.shape[0], codes.shape[1] * 2
+    out = np.empty((R, C), np.float64)
+    lib().oracle_dequant_mbs_row(_p(codes), _p(scales), _p(mbs), R, C, _p(out))
+    return out

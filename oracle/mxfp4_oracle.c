@@ -30,6 +30,7 @@
  * Everything here is written as loops over the definitions; OpenMP only splits
  * independent rows across threads (no reordering inside a computation).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -410,4 +411,130 @@ void oracle_error_decomposition(const uint16_t* x, int64_t R, int64_t C, int64_t
         free(v);
     }
     for (int k = 0; k < 7; ++k) out[k] = acc[k];
+}
+
+/* ------------------------------------------------------------------------- */
+/* Quantiser fixes ([DECOMP] "three fixes": OF and MBS)                       */
+/* ------------------------------------------------------------------------- */
+
+/* Quantise len fp32 values (len % 32 == 0) block by block as they are (no
+ * rotation): codes (packed nibbles) and E8M0 bytes. */
+static void quantize_f32_vec(const float* v, int64_t len, int mode, uint8_t* codes, uint8_t* scales) {
+    for (int64_t b = 0; b < len / 32; ++b) {
+        const float* blk = v + b * 32;
+        int e = oracle_shared_exponent(block_amax(blk, 32), mode);
+        uint8_t q[32];
+        quantize_block(blk, e, q);
+        for (int i = 0; i < 32; ++i) put_nibble(codes, b * 32 + i, q[i]);
+        scales[b] = (uint8_t)(e + 127);
+    }
+}
+
+/* The same for R rows of C fp32 values: codes [R, C/2], scales [R, C/32]. */
+void oracle_quantize_f32_rows(const float* v, int64_t R, int64_t C, int mode, uint8_t* codes, uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) quantize_f32_vec(v + r * C, C, mode, codes + r * (C / 2), scales + r * (C / 32));
+}
+
+static void rotated_row(const uint16_t* x, int64_t len, int had, float* xf, float* v) {
+    for (int64_t i = 0; i < len; ++i) xf[i] = bf16_to_float(x[i]);
+    oracle_rotate_f32(xf, len, had, v);
+}
+
+/* Value of nibble code c of element i of a packed row times 2^e, in fp64. */
+static double dq_elem(const uint8_t* row, int64_t i, int e) {
+    uint8_t b = row[i / 2];
+    int c = (i % 2 == 0) ? (b & 0xF) : (b >> 4);
+    return ldexp(oracle_e2m1_value(c), e);
+}
+
+/* OF ([DECOMP] "OF -- outlier fallback, with residual weight alpha"):
+ *   x1 = Q(x),  x2 = Q(x - x1),  x_OF = x1 + alpha * x2,
+ * with Q the row quantiser acting on the rotated row (1x32 blocks along C).  The
+ * residual x - dq(x1) is formed in fp64; it is exactly representable in fp32 (the
+ * return value counts the values for which it was not, expected 0) and the second
+ * pass quantises it as an fp32 vector.  alpha = 2^alpha_log2 (alpha_log2 <= 0; the
+ * pages settle on 0.5) is carried exactly by the second pass's E8M0 bytes: stored
+ * byte = max(byte + alpha_log2, 0), so a block whose residual amax is below 2^-125
+ * keeps byte 0 (weight 1 instead of alpha).  Then x_OF = dq(q1) + dq(q2). */
+int64_t oracle_quantize_of_row(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                               int alpha_log2, uint8_t* codes1, uint8_t* scales1, uint8_t* codes2,
+                               uint8_t* scales2) {
+    int64_t inexact = 0;
+#pragma omp parallel for schedule(static) reduction(+ : inexact)
+    for (int64_t r = 0; r < R; ++r) {
+        float* xf = (float*)malloc(sizeof(float) * (size_t)C);
+        float* v = (float*)malloc(sizeof(float) * (size_t)C);
+        float* res = (float*)malloc(sizeof(float) * (size_t)C);
+        uint8_t* c1 = codes1 + r * (C / 2);
+        uint8_t* s1 = scales1 + r * (C / 32);
+        rotated_row(x + r * ld, C, had, xf, v);
+        quantize_f32_vec(v, C, mode, c1, s1);
+        for (int64_t i = 0; i < C; ++i) {
+            double d = (double)v[i] - dq_elem(c1, i, (int)s1[i / 32] - 127);
+            res[i] = (float)d;
+            if ((double)res[i] != d) ++inexact;
+        }
+        uint8_t* s2 = scales2 + r * (C / 32);
+        quantize_f32_vec(res, C, mode, codes2 + r * (C / 2), s2);
+        for (int64_t b = 0; b < C / 32; ++b) {
+            int sb = (int)s2[b] + alpha_log2;
+            s2[b] = (uint8_t)(sb < 0 ? 0 : sb);
+        }
+        free(xf);
+        free(v);
+        free(res);
+    }
+    return inexact;
+}
+
+/* MBS byte of a macro block with amax A ([DECOMP] "MBS -- macro block scaling":
+ * scale 2^e_M * (1 + m), m in [0, 1), 8 bits of mantissa).  Reading (the pages do
+ * not say how m is chosen): write A = f * 2^E with f in [1, 2) and let T = 1.5 if
+ * f <= 1.5, else 3; k is the largest value in 0..255 with (1 + k/256) * f <= T, i.e.
+ * the largest 8-bit correction that does not lift the macro-block maximum above the
+ * top grid value 6 of its E8M0 scale.  A == 0 or subnormal: k = 0.  By scanning k. */
+int oracle_mbs_byte(float A) {
+    if (!(A >= FLT_MIN)) return 0;
+    int E;
+    double f = frexp((double)A, &E) * 2.0; /* in [1, 2) */
+    double T = (f <= 1.5) ? 1.5 : 3.0;
+    for (int k = 255; k >= 0; --k)
+        if ((1.0 + k / 256.0) * f <= T) return k;
+    return 0;
+}
+
+/* MBS quantiser, row layout: per macro block of 128 consecutive rotated values (four
+ * 32-blocks) one byte k = oracle_mbs_byte(macro amax); the values are prescaled,
+ * x' = fl32((1 + k/256) * x), and quantised by Q (32-blocks, `mode`); the
+ * reconstruction is dq(q) / (1 + k/256).  codes [R, C/2], scales [R, C/32],
+ * mbs [R, C/128]; C % 128 == 0. */
+void oracle_quantize_mbs_row(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                             uint8_t* codes, uint8_t* scales, uint8_t* mbs) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        float* xf = (float*)malloc(sizeof(float) * (size_t)C);
+        float* v = (float*)malloc(sizeof(float) * (size_t)C);
+        rotated_row(x + r * ld, C, had, xf, v);
+        for (int64_t mb = 0; mb < C / 128; ++mb) {
+            float* blk = v + mb * 128;
+            int k = oracle_mbs_byte(block_amax(blk, 128));
+            float mul = 1.0f + (float)k / 256.0f;
+            for (int i = 0; i < 128; ++i) blk[i] = blk[i] * mul;
+            mbs[r * (C / 128) + mb] = (uint8_t)k;
+        }
+        quantize_f32_vec(v, C, mode, codes + r * (C / 2), scales + r * (C / 32));
+        free(xf);
+        free(v);
+    }
+}
+
+/* MBS reconstruction: out[r][i] = dq(code) / (1 + k/256). */
+void oracle_dequant_mbs_row(const uint8_t* codes, const uint8_t* scales, const uint8_t* mbs, int64_t R, int64_t C,
+                            double* out) {
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t i = 0; i < C; ++i) {
+            double q = dq_elem(codes + r * (C / 2), i, (int)scales[r * (C / 32) + i / 32] - 127);
+            out[r * C + i] = q / (1.0 + mbs[r * (C / 128) + i / 128] / 256.0);
+        }
 }
