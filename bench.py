@@ -359,6 +359,10 @@ def gpu_arm(args, rank, world, dist):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(tot / args.steps, 3)}
         assert mx.device_status() == 0
 
+    fixes = None
+    if not args.skip_fixes:
+        fixes = quant_fixes_leg(flush, hbm)
+
     fp8 = None
     if not args.skip_fp8:
         fp8 = fp8_comparator(layers, flush, args.steps, args.warmup)
@@ -384,7 +388,48 @@ def gpu_arm(args, rank, world, dist):
         "clocks": clk.summary(),
         "device_status": status,
         "fp8_comparator": fp8,
+        "quant_fixes": fixes,
     }
+    return out
+
+
+def quant_fixes_leg(flush, hbm, iters=20):
+    """The quantiser fixes of "Decomposing MXFP4 quantization error ..." (OF, MBS) on the
+    down-projection input of the workload (8192 x 14336 bf16, H16, OCP floor), each
+    launch timed alone with CUDA events after an L2 flush, against the HBM roofline.
+    Algorithmic bytes per element: OF 2 + 2 x (0.5 + 1/32); MBS 2 + 0.5 + 1/32 + 1/128.
+    Not part of the timed step: a measurement of the variants."""
+    import torch
+
+    from mxfp4_precision_gemms_gb300 import binding as mx
+    from mxfp4_precision_gemms_gb300 import synth
+
+    R, C = 8192, 14336
+    x = mx.bf16_tensor(synth.activations(R, C, 11))
+    n = R * C
+    legs = {
+        "of": (lambda: mx.rotate_quantize_of(x, had=16, mode=0, alpha_log2=-1), n * (2 + 2 * (0.5 + 1 / 32))),
+        "mbs": (lambda: mx.rotate_quantize_mbs(x, had=16, mode=0), n * (2 + 0.5 + 1 / 32 + 1 / 128)),
+        "dual": (lambda: mx.rotate_quantize(x, had=16, mode=0, layouts=mx.LAYOUT_ROW | mx.LAYOUT_COLT),
+                 n * (2 + 2 * (0.5 + 1 / 32))),
+        "row": (lambda: mx.rotate_quantize(x, had=16, mode=0, layouts=mx.LAYOUT_ROW), n * (2 + 0.5 + 1 / 32)),
+    }
+    out = {"tensor": f"{R}x{C} bf16 activations, H16, OCP floor", "unit": "GB/s", "peak": hbm}
+    for name, (fn, by) in legs.items():
+        for _ in range(3):
+            fn()
+        tot = 0.0
+        for _ in range(iters):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        gbs = by / (tot / iters * 1e-3) / 1e9
+        out[name] = {"gbs": round(gbs, 1), "frac": round(gbs / hbm, 4), "us": round(tot / iters * 1e3, 1)}
+    assert mx.device_status() == 0
     return out
 
 
@@ -571,13 +616,13 @@ def write_traffic(csv_path):
     for (_, name), b in launches.items():
         if "mxf4_gemm" in name:
             per["gemm"].append(b)
-        elif "rq_" in name:
+        elif "rq_kernel" in name:
             per["quant"].append(b)
     rec = {k: {"bytes_per_launch": round(sum(v) / len(v)), "launches": len(v),
                "sources_sha": kernel_sources_sha(KERNEL_SOURCES[k])} for k, v in per.items() if v}
     rec["command"] = ("ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
                       "--clock-control none --csv --log-file <csv> python bench.py --steps 1 --warmup 3 "
-                      "--skip-e2e --skip-cpu-baseline --skip-fp8")
+                      "--skip-e2e --skip-cpu-baseline --skip-fp8 --skip-fixes")
     path = os.path.join(ROOT, "profiles", "traffic_llama8b_linears_T8192.json")
     json.dump(rec, open(path, "w"), indent=1)
     print(json.dumps(rec))
@@ -590,6 +635,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-fixes", action="store_true", help="skip the OF / MBS quantiser measurement")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-fp8", action="store_true", help="skip the FP8 (torch._scaled_mm) comparator")
     ap.add_argument("--profile-case", action="store_true", help="run the small ncu case and exit")

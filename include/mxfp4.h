@@ -172,6 +172,31 @@ mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols
  * pairs (.cta_group::2, M = 256 per pair).  Allocates no global memory. */
 mxfp4_status mxfp4_mma_peak_probe(int kind, int64_t iters, double* tflops);
 
+/* Quantiser fixes of "Decomposing MXFP4 quantization error for LLM reinforcement
+ * learning" (sections MBS and OF), row layout only: x [rows, cols] bf16 (ld elements per
+ * row, 16-byte aligned, ld % 8 == 0) is rotated along cols exactly as by
+ * mxfp4_rotate_quantize (had, mode as there).  Output descriptors are filled in like
+ * row_out of mxfp4_rotate_quantize (codes, scales, sf_layout set by the caller; the
+ * library writes rows, cols, layout, had, mode).  Asynchronous on `stream`.
+ *
+ * Outlier fallback (OF): q1 = Q(v) and q2 = Q(v - dq(q1)), the residual being exact in
+ * fp32.  The residual weight alpha = 2^alpha_log2 (alpha_log2 in [-8, 0]; the pages use
+ * 0.5) is carried by q2's E8M0 bytes: stored byte = max(byte + alpha_log2, 0), so the
+ * OF value is dq(q1) + dq(q2) and both tensors feed mxfp4_gemm unchanged (a GEMM over
+ * an OF operand is two accumulating GEMMs).  cols % 32 == 0. */
+mxfp4_status mxfp4_rotate_quantize_of(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                      int alpha_log2, mxfp4_tensor* q1, mxfp4_tensor* q2, mxfp4_stream_t stream);
+
+/* Macro-block scaling (MBS): per 128 consecutive rotated values of a row one byte k,
+ * the largest value with (1 + k/256) * f <= T for the macro-block amax A = f * 2^E
+ * (T = 1.5 if f <= 1.5, else 3; A zero or subnormal gives k = 0).  The values are
+ * prescaled to fl32((1 + k/256) v) and quantised to q; the reconstruction is
+ * dq(q) / (1 + k/256).  mbs: device bytes [rows, cols/128], row-major, written by the
+ * call.  The post-scale varies along the contraction, so mxfp4_gemm does not apply it.
+ * cols % 128 == 0. */
+mxfp4_status mxfp4_rotate_quantize_mbs(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                       mxfp4_tensor* q, uint8_t* mbs, mxfp4_stream_t stream);
+
 /* Workspace bytes needed by mxfp4_linear_{fprop,dgrad,wgrad} (op = MXFP4_OP_*). */
 size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp4_config* cfg);
 

@@ -68,6 +68,8 @@ def lib():
                 "mxfp4_scales_bytes": ([I64, I64, I, I], S),
                 "mxfp4_quantized_bytes": ([I64, I64, I, I], S),
                 "mxfp4_rotate_quantize": ([P, I64, I64, I64, I, I, U, T, T, T, P], I),
+                "mxfp4_rotate_quantize_of": ([P, I64, I64, I64, I, I, I, T, T, P], I),
+                "mxfp4_rotate_quantize_mbs": ([P, I64, I64, I64, I, I, T, P, P], I),
                 "mxfp4_gemm": ([T, T, P, I64, I, I, P, S, P], I),
                 "mxfp4_workspace_bytes": ([I, I64, I64, I64, CF], S),
                 "mxfp4_linear_fprop": ([P, P, I64, I64, I64, CF, P, T, T, P, S, P], I),
@@ -195,7 +197,7 @@ def rotate_quantize(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR,
                     sf_layout: int = SF_MMA, outs: dict | None = None, stream=None) -> dict:
     """mxfp4_rotate_quantize on a bf16 CUDA matrix [rows, cols] (row-major, ld = stride(0)).
     Returns {'row': QTensor, 'colT': QTensor, '2d': QTensor} for the requested layouts."""
-    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or (x.numel() and x.stride(1) != 1):
         raise ValueError("x must be a CUDA bf16 matrix with unit column stride")
     R, C = x.shape
     outs = dict(outs or {})
@@ -212,6 +214,42 @@ def rotate_quantize(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR,
     for v in outs.values():
         v.had, v.mode = had, mode
     return outs
+
+
+def _check_bf16_matrix(x: torch.Tensor):
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or (x.numel() and x.stride(1) != 1):
+        raise ValueError("x must be a CUDA bf16 matrix with unit column stride")
+
+
+def rotate_quantize_of(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR, alpha_log2: int = -1,
+                       sf_layout: int = SF_MMA, stream=None) -> tuple[QTensor, QTensor]:
+    """mxfp4_rotate_quantize_of: outlier fallback, row layout.  Returns (q1, q2) with
+    the OF value dq(q1) + dq(q2) (alpha = 2^alpha_log2 carried by q2's scales)."""
+    _check_bf16_matrix(x)
+    R, C = x.shape
+    q1 = empty_qtensor(R, C, LAYOUT_ROW, sf_layout, x.device)
+    q2 = empty_qtensor(R, C, LAYOUT_ROW, sf_layout, x.device)
+    c1, c2 = q1.c(), q2.c()
+    _check(lib().mxfp4_rotate_quantize_of(_ptr(x), R, C, x.stride(0), had, mode, alpha_log2, ctypes.byref(c1),
+                                          ctypes.byref(c2), _stream(stream)))
+    for q in (q1, q2):
+        q.had, q.mode = had, mode
+    return q1, q2
+
+
+def rotate_quantize_mbs(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR, sf_layout: int = SF_MMA,
+                        stream=None) -> tuple[QTensor, torch.Tensor]:
+    """mxfp4_rotate_quantize_mbs: macro-block scaling, row layout.  Returns (q, mbs) with
+    mbs [rows, cols/128] uint8; the reconstruction is dq(q) / (1 + mbs/256)."""
+    _check_bf16_matrix(x)
+    R, C = x.shape
+    q = empty_qtensor(R, C, LAYOUT_ROW, sf_layout, x.device)
+    mbs = torch.empty((R, max(C // 128, 0)), dtype=torch.uint8, device=x.device)
+    c = q.c()
+    _check(lib().mxfp4_rotate_quantize_mbs(_ptr(x), R, C, x.stride(0), had, mode, ctypes.byref(c), _ptr(mbs),
+                                           _stream(stream)))
+    q.had, q.mode = had, mode
+    return q, mbs
 
 
 def gemm(A: QTensor, B: QTensor, out_dtype: int = OUT_F32, accumulate: bool = False,
@@ -331,7 +369,7 @@ DECOMP_KEYS = ("e2", "scale2", "dz2", "grid2", "scale_grid", "n_deadzone", "n")
 def error_decomposition(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_CEIL, stream=None) -> dict:
     """Tensor-wide sums of the MXFP4 error components of a row-quantised bf16 matrix
     (mxfp4_error_decomposition); returns a dict keyed by DECOMP_KEYS."""
-    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or (x.numel() and x.stride(1) != 1):
         raise ValueError("x must be a CUDA bf16 matrix with unit column stride")
     out = torch.empty(7, dtype=torch.float64, device=x.device)
     _check(lib().mxfp4_error_decomposition(_ptr(x), x.shape[0], x.shape[1], x.stride(0), had, mode, _ptr(out),

@@ -43,6 +43,11 @@ struct QuantTmaParams {
 
 // Launches the fused rotate+quantise kernel for the requested layouts.
 cudaError_t launch_rotate_quantize(const QuantParams& p, int had, unsigned layouts, cudaStream_t s);
+// Quantiser fixes (row layout): OF writes Q(v) to p.row and Q(v - dq(Q(v))) to q2;
+// MBS writes Q((1 + k/256) v) to p.row and the bytes k to mbs [R, C/128].
+cudaError_t launch_rotate_quantize_of(const QuantParams& p, const QuantOut& q2, int had, int alpha_log2,
+                                      cudaStream_t s);
+cudaError_t launch_rotate_quantize_mbs(const QuantParams& p, uint8_t* mbs, int had, cudaStream_t s);
 
 struct GemmParams {
     CUtensorMap map_a;   // codes of A [M, K/2] bytes, box 128 rows x 128 B, 128B swizzle

@@ -8,6 +8,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <initializer_list>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -325,7 +327,7 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
     if (ld < cols || ld % 8)
         return fail(MXFP4_ERR_MISALIGNED, "ld (%lld) must be >= cols and a multiple of 8", (long long)ld);
     if (!aligned16(x)) return fail(MXFP4_ERR_MISALIGNED, "x not 16-byte aligned");
-    if ((rows + 127) / 128 > 65535) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "too many rows");
+    if ((rows + 63) / 64 > 65535) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "too many rows");
     mxfp4_status st;
     if (want_row && (st = check_out(row_out, "row_out", true))) return st;
     if (want_colT && (st = check_out(colT_out, "colT_out", true))) return st;
@@ -356,6 +358,97 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
     p.twoD = to_out(want_2d ? twoD_out : nullptr);
     cudaError_t e = launch_rotate_quantize(p, had, layouts, s);
     if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize launch");
+    return ok();
+}
+
+namespace {
+// Shared checks of the row-layout quantiser fixes; fills the descriptors.  Returns
+// MXFP4_OK with *empty set when there is nothing to compute.
+mxfp4_status check_fix_args(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                            int64_t col_multiple, std::initializer_list<mxfp4_tensor*> outs, bool* empty) {
+    *empty = false;
+    if (rows < 0 || cols < 0) return fail(MXFP4_ERR_INVALID_ARG, "negative size");
+    if (!valid_had(had)) return fail(MXFP4_ERR_INVALID_ARG, "hadamard must be 0, 16 or 32 (got %d)", had);
+    if (!valid_mode(mode)) return fail(MXFP4_ERR_INVALID_ARG, "scale mode must be 0 or 1 (got %d)", mode);
+    if (cols % col_multiple)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "cols (%lld) %% %lld != 0", (long long)cols, (long long)col_multiple);
+    for (mxfp4_tensor* t : outs)
+        if (!t) return fail(MXFP4_ERR_INVALID_ARG, "an output descriptor is NULL");
+    for (mxfp4_tensor* t : outs) {
+        t->rows = rows;
+        t->cols = cols;
+        t->layout = MXFP4_LAYOUT_ROW;
+        t->had = had;
+        t->mode = mode;
+    }
+    if (rows == 0 || cols == 0) {
+        *empty = true;
+        return MXFP4_OK;
+    }
+    if (!x) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
+    if (ld < cols || ld % 8)
+        return fail(MXFP4_ERR_MISALIGNED, "ld (%lld) must be >= cols and a multiple of 8", (long long)ld);
+    if (!aligned16(x)) return fail(MXFP4_ERR_MISALIGNED, "x not 16-byte aligned");
+    if ((rows + 63) / 64 > 65535) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "too many rows");
+    mxfp4_status st;
+    for (mxfp4_tensor* t : outs)
+        if ((st = check_out(t, "output", true))) return st;
+    return MXFP4_OK;
+}
+
+mxfp4_status clear_padding(std::initializer_list<mxfp4_tensor*> outs, cudaStream_t s) {
+    for (mxfp4_tensor* t : outs)
+        if (needs_sf_padding(t)) {
+            cudaError_t e =
+                cudaMemsetAsync(t->scales, 0, mxfp4_scales_bytes(t->rows, t->cols, t->layout, t->sf_layout), s);
+            if (e != cudaSuccess) return cuda_fail(e, "clear scale padding");
+        }
+    return MXFP4_OK;
+}
+}  // namespace
+
+mxfp4_status mxfp4_rotate_quantize_of(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                      int alpha_log2, mxfp4_tensor* q1, mxfp4_tensor* q2, mxfp4_stream_t stream) {
+    if (alpha_log2 > 0 || alpha_log2 < -8)
+        return fail(MXFP4_ERR_INVALID_ARG, "alpha_log2 must be in [-8, 0] (got %d)", alpha_log2);
+    bool empty;
+    mxfp4_status st = check_fix_args(x, rows, cols, ld, had, mode, 32, {q1, q2}, &empty);
+    if (st || empty) return st ? st : ok();
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = clear_padding({q1, q2}, s))) return st;
+    QuantParams p{};
+    p.x = static_cast<const uint16_t*>(x);
+    p.R = rows;
+    p.C = cols;
+    p.ld = ld;
+    p.mode = mode;
+    p.row = to_out(q1);
+    cudaError_t e = launch_rotate_quantize_of(p, to_out(q2), had, alpha_log2, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize_of launch");
+    return ok();
+}
+
+mxfp4_status mxfp4_rotate_quantize_mbs(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                       mxfp4_tensor* q, uint8_t* mbs, mxfp4_stream_t stream) {
+    bool empty;
+    mxfp4_status st = check_fix_args(x, rows, cols, ld, had, mode, 128, {q}, &empty);
+    if (st || empty) return st ? st : ok();
+    if (!mbs) return fail(MXFP4_ERR_INVALID_ARG, "mbs is NULL");
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = clear_padding({q}, s))) return st;
+    QuantParams p{};
+    p.x = static_cast<const uint16_t*>(x);
+    p.R = rows;
+    p.C = cols;
+    p.ld = ld;
+    p.mode = mode;
+    p.row = to_out(q);
+    cudaError_t e = launch_rotate_quantize_mbs(p, mbs, had, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize_mbs launch");
     return ok();
 }
 

@@ -1,0 +1,125 @@
+"""GPU quantiser fixes vs the CPU oracle ("Decomposing MXFP4 quantization error for LLM
+reinforcement learning", OF and MBS): codes, E8M0 bytes and MBS bytes bit-exact; the
+GEMM over an OF operand (two accumulating MXFP4 GEMMs) within the GEMM tolerance."""
+import numpy as np
+import pytest
+
+import oracle
+from mxfp4_precision_gemms_gb300 import synth
+from tests.gpu_util import ORACLE_HAD, assert_within, gpu_ready
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return gpu_ready()
+
+
+def same(got, want, what):
+    if not np.array_equal(got, want):
+        i = np.argwhere(got != want)[:4]
+        raise AssertionError(f"{what} differ at {i.tolist()}: gpu {got[tuple(i[0])]} oracle {want[tuple(i[0])]} "
+                             f"({int((got != want).sum())} of {got.size})")
+
+
+SHAPES = [(64, 256), (96, 160), (200, 1056), (1, 32), (130, 384)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("had", [0, 16, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_of_bit_exact(torch, shape, had, mode):
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    R, C = shape
+    xb = synth.heavy_tailed(R, C, 500 + R + C + had + mode)
+    for alpha_log2, sf in ((0, mx.SF_PLAIN), (-1, mx.SF_MMA)):
+        q1, q2 = mx.rotate_quantize_of(mx.bf16_tensor(xb), had=had, mode=mode, alpha_log2=alpha_log2, sf_layout=sf)
+        torch.cuda.synchronize()
+        assert mx.device_status() == 0
+        c1, s1, c2, s2, bad = oracle.quantize_of(xb, ORACLE_HAD[had], mode, alpha_log2)
+        assert bad == 0
+        what = f"OF {shape} had={had} mode={mode} alpha_log2={alpha_log2}"
+        same(q1.plain_scales(), s1, what + " q1 scales")
+        same(q1.codes.cpu().numpy(), c1, what + " q1 codes")
+        same(q2.plain_scales(), s2, what + " q2 scales")
+        same(q2.codes.cpu().numpy(), c2, what + " q2 codes")
+
+
+@pytest.mark.parametrize("shape", [(64, 256), (96, 128), (200, 1024), (1, 128), (130, 384)])
+@pytest.mark.parametrize("had", [0, 16, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_mbs_bit_exact(torch, shape, had, mode):
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    R, C = shape
+    xb = synth.heavy_tailed(R, C, 600 + R + C + had + mode)
+    for sf in (mx.SF_PLAIN, mx.SF_MMA):
+        q, mbs = mx.rotate_quantize_mbs(mx.bf16_tensor(xb), had=had, mode=mode, sf_layout=sf)
+        torch.cuda.synchronize()
+        assert mx.device_status() == 0
+        codes, scales, kb = oracle.quantize_mbs(xb, ORACLE_HAD[had], mode)
+        what = f"MBS {shape} had={had} mode={mode} sf={sf}"
+        same(mbs.cpu().numpy(), kb, what + " mbs bytes")
+        same(q.plain_scales(), scales, what + " scales")
+        same(q.codes.cpu().numpy(), codes, what + " codes")
+
+
+def test_fixes_on_linear_activations_at_scale(torch):
+    """Config-2 sized activations (8192 x 4096, 1% outlier channels), H16, floor: every
+    byte of both fixes against the oracle."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    xb = synth.activations(8192, 4096, 7)
+    x = mx.bf16_tensor(xb)
+    q1, q2 = mx.rotate_quantize_of(x, had=16, mode=0, alpha_log2=-1, sf_layout=mx.SF_MMA)
+    q, mbs = mx.rotate_quantize_mbs(x, had=16, mode=0, sf_layout=mx.SF_MMA)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    c1, s1, c2, s2, _ = oracle.quantize_of(xb, 16, 0, -1)
+    same(q1.codes.cpu().numpy(), c1, "OF q1 codes")
+    same(q1.plain_scales(), s1, "OF q1 scales")
+    same(q2.codes.cpu().numpy(), c2, "OF q2 codes")
+    same(q2.plain_scales(), s2, "OF q2 scales")
+    codes, scales, kb = oracle.quantize_mbs(xb, 16, 0)
+    same(mbs.cpu().numpy(), kb, "MBS bytes")
+    same(q.plain_scales(), scales, "MBS scales")
+    same(q.codes.cpu().numpy(), codes, "MBS codes")
+
+
+def test_gemm_over_an_of_operand(torch):
+    """Y = X_OF W^T as GEMM(q1, Wq) + GEMM(q2, Wq) (fp32, accumulate): within the GEMM
+    tolerance of the oracle's dq(q1) Wq^T + dq(q2) Wq^T."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    X, W, _ = synth.linear_inputs(384, 512, 1024, 8)
+    q1, q2 = mx.rotate_quantize_of(mx.bf16_tensor(X), had=16, mode=0, alpha_log2=-1)
+    wq = mx.rotate_quantize(mx.bf16_tensor(W), had=16, mode=0, layouts=mx.LAYOUT_ROW)["row"]
+    Y = mx.gemm(q1, wq)
+    mx.gemm(q2, wq, accumulate=True, out=Y)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    c1, s1, c2, s2, _ = oracle.quantize_of(X, 16, 0, -1)
+    cw, sw = oracle.quantize(W, 16, 0, "row")
+    C1, S1 = oracle.gemm(c1, s1, cw, sw)
+    C2, S2 = oracle.gemm(c2, s2, cw, sw)
+    assert_within(Y.double().cpu().numpy(), C1 + C2, S1 + S2, what="OF GEMM")
+    # the OF operand is closer to the rotated X than the plain one
+    v = oracle.rotate_f32(synth.bf16_to_f32(X), 16).astype(np.float64)
+    err_of = np.abs(oracle.dequant_row(c1, s1) + oracle.dequant_row(c2, s2) - v).sum()
+    err_q = np.abs(oracle.dequant_row(c1, s1) - v).sum()
+    assert err_of < err_q
+
+
+def test_fix_argument_checks(torch):
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    x = mx.bf16_tensor(synth.heavy_tailed(64, 96, 1))
+    with pytest.raises(RuntimeError):
+        mx.rotate_quantize_mbs(x)  # cols % 128 != 0
+    with pytest.raises(RuntimeError):
+        mx.rotate_quantize_of(x, alpha_log2=1)
+    e = mx.bf16_tensor(np.zeros((0, 128), np.uint16))
+    q, mbs = mx.rotate_quantize_mbs(e)
+    assert q.rows == 0 and mbs.numel() == 0
