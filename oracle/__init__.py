@@ -77,6 +77,10 @@ def lib():
             L.oracle_mbs_byte.restype = I
             L.oracle_quantize_mbs_row.argtypes = [P, I64, I64, I64, I, I, P, P, P]
             L.oracle_dequant_mbs_row.argtypes = [P, P, P, I64, I64, P]
+            L.oracle_e2m1_code_sr.argtypes = [ctypes.c_float, ctypes.c_uint16]
+            L.oracle_e2m1_code_sr.restype = I
+            L.oracle_quantize_row_rand.argtypes = [P, I64, I64, I64, I, I, P, P, P, P]
+            L.oracle_quantize_colT_rand.argtypes = [P, I64, I64, I64, I, I, P, P, P, P]
             L.oracle_num_threads.restype = I
             L.oracle_set_num_threads.argtypes = [I]
             _lib = L
@@ -327,3 +331,41 @@ def dequant_mbs(codes, scales, mbs) -> np.ndarray:
     out = np.empty((R, C), np.float64)
     lib().oracle_dequant_mbs_row(_p(codes), _p(scales), _p(mbs), R, C, _p(out))
     return out
+
+
+# --------------------------------------------------------------------------- randomised baselines
+# "Pretraining ... Native FP4 Hardware", A.2 (random sign flips before the Hadamard)
+# and the ablation of table 1 (stochastic rounding): the random numbers are inputs.
+def e2m1_code_sr(u: float, r: int) -> int:
+    return lib().oracle_e2m1_code_sr(float(np.float32(u)), int(r))
+
+
+def pack_signs(neg: np.ndarray) -> np.ndarray:
+    """Boolean vector (True = negate) -> bitmask bytes, bit i of byte i // 8."""
+    return np.packbits(np.asarray(neg, bool), bitorder="little")
+
+
+def quantize_rand(x_bf16: np.ndarray, had: int, mode: int, layout: str, signs=None, sr=None):
+    """Like quantize() for 'row' ([R, C], signs over C, sr [R, C] uint16) and 'colT'
+    ([C, R] output, signs over R, sr [C, R] uint16); signs is a bitmask (pack_signs)."""
+    x = _u16(x_bf16)
+    R, C = x.shape
+    sg = None if signs is None else np.ascontiguousarray(signs, np.uint8)
+    rr = None if sr is None else np.ascontiguousarray(sr, np.uint16)
+    ps = _p(sg) if sg is not None else None
+    pr = _p(rr) if rr is not None else None
+    if layout == "row":
+        if rr is not None:
+            assert rr.shape == (R, C)
+        codes = np.zeros((R, C // 2), np.uint8)
+        scales = np.zeros((R, C // 32), np.uint8)
+        lib().oracle_quantize_row_rand(_p(x), R, C, C, had, mode, ps, pr, _p(codes), _p(scales))
+    elif layout == "colT":
+        if rr is not None:
+            assert rr.shape == (C, R)
+        codes = np.zeros((C, R // 2), np.uint8)
+        scales = np.zeros((C, R // 32), np.uint8)
+        lib().oracle_quantize_colT_rand(_p(x), R, C, C, had, mode, ps, pr, _p(codes), _p(scales))
+    else:
+        raise ValueError(layout)
+    return codes, scales

@@ -538,3 +538,82 @@ void oracle_dequant_mbs_row(const uint8_t* codes, const uint8_t* scales, const u
             out[r * C + i] = q / (1.0 + mbs[r * (C / 128) + i / 128] / 256.0);
         }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Randomised baselines ([MXFP4-HW] A.2 and "experiments", table 1: random sign */
+/* flips before the Hadamard, stochastic rounding)                             */
+/* ------------------------------------------------------------------------- */
+
+/* Stochastic rounding of u (the fp32 value v * 2^-e, |u| < 8) to the E2M1 grid with
+ * the uniform 16-bit integer r: below 6 the magnitude a lies in [lo, lo + step) with
+ * step 0.5 on [0, 2), 1 on [2, 4), 2 on [4, 6); it rounds up with probability
+ * p = (a - lo) / step, i.e. iff r < p * 65536.  a >= 6 saturates to 6.  The sign is
+ * kept (a zero keeps its sign).  All of lo, a - lo, p and p * 65536 are exact in
+ * fp32, so the decision is the same in any precision.  Returns the 4-bit code. */
+int oracle_e2m1_code_sr(float u, uint16_t r) {
+    float a = fabsf(u);
+    double mag;
+    if (a >= 6.0f) {
+        mag = 6.0;
+    } else {
+        double step = a < 2.0f ? 0.5 : (a < 4.0f ? 1.0 : 2.0);
+        double lo = floor((double)a / step) * step;
+        double p = ((double)a - lo) / step;
+        mag = lo + (((double)r < p * 65536.0) ? step : 0.0);
+    }
+    int code = oracle_e2m1_code(mag); /* mag is a grid value: its own code */
+    if (signbit(u)) code |= 8;
+    return code;
+}
+
+/* Quantise a contiguous vector of len bf16 values (element i at x[i*stride]) along
+ * itself, with optional random signs and stochastic rounding:
+ *   signs: NULL or a bitmask over the vector's indices (bit i set: x_i negated before
+ *          the rotation, the random-sign Hadamard H D x);
+ *   sr:    NULL (round to nearest even) or one uniform 16-bit integer per element.
+ * The E8M0 scale is taken as in oracle_quantize_vec. */
+void oracle_quantize_vec_rand(const uint16_t* x, int64_t stride, int64_t len, int had, int mode, const uint8_t* signs,
+                              const uint16_t* sr, uint8_t* codes, uint8_t* scales) {
+    float* xf = (float*)malloc(sizeof(float) * (size_t)len);
+    float* v = (float*)malloc(sizeof(float) * (size_t)len);
+    for (int64_t i = 0; i < len; ++i) {
+        xf[i] = bf16_to_float(x[i * stride]);
+        if (signs && ((signs[i / 8] >> (i % 8)) & 1)) xf[i] = -xf[i];
+    }
+    oracle_rotate_f32(xf, len, had, v);
+    for (int64_t b = 0; b < len / 32; ++b) {
+        const float* blk = v + b * 32;
+        int e = oracle_shared_exponent(block_amax(blk, 32), mode);
+        for (int i = 0; i < 32; ++i) {
+            int c;
+            if (sr) {
+                float u = (float)ldexp((double)blk[i], -e); /* one rounding: fl32(v * 2^-e) */
+                c = oracle_e2m1_code_sr(u, sr[b * 32 + i]);
+            } else {
+                c = oracle_e2m1_code(ldexp((double)blk[i], -e));
+            }
+            put_nibble(codes, b * 32 + i, (uint8_t)c);
+        }
+        scales[b] = (uint8_t)(e + 127);
+    }
+    free(xf);
+    free(v);
+}
+
+/* Row layout with the randomised options: col_signs over C, sr [R, C] (row-major). */
+void oracle_quantize_row_rand(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                              const uint8_t* col_signs, const uint16_t* sr, uint8_t* codes, uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r)
+        oracle_quantize_vec_rand(x + r * ld, 1, C, had, mode, col_signs, sr ? sr + r * C : 0, codes + r * (C / 2),
+                                 scales + r * (C / 32));
+}
+
+/* Column layout (stored transposed) with row_signs over R and sr [C, R]. */
+void oracle_quantize_colT_rand(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                               const uint8_t* row_signs, const uint16_t* sr, uint8_t* codes, uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < C; ++c)
+        oracle_quantize_vec_rand(x + c, ld, R, had, mode, row_signs, sr ? sr + c * R : 0, codes + c * (R / 2),
+                                 scales + c * (R / 32));
+}
