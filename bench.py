@@ -397,7 +397,9 @@ def quant_fixes_leg(flush, hbm, iters=20):
     """The quantiser fixes of "Decomposing MXFP4 quantization error ..." (OF, MBS) on the
     down-projection input of the workload (8192 x 14336 bf16, H16, OCP floor), each
     launch timed alone with CUDA events after an L2 flush, against the HBM roofline.
-    Algorithmic bytes per element: OF 2 + 2 x (0.5 + 1/32); MBS 2 + 0.5 + 1/32 + 1/128.
+    Algorithmic bytes per element: OF 2 + 2 x (0.5 + 1/32); MBS 2 + 0.5 + 1/32 + 1/128;
+    random signs + stochastic rounding, both copies, 2 + 2 x 2 (random integers) + 2 x
+    (0.5 + 1/32).
     Not part of the timed step: a measurement of the variants."""
     import torch
 
@@ -414,6 +416,15 @@ def quant_fixes_leg(flush, hbm, iters=20):
                  n * (2 + 2 * (0.5 + 1 / 32))),
         "row": (lambda: mx.rotate_quantize(x, had=16, mode=0, layouts=mx.LAYOUT_ROW), n * (2 + 0.5 + 1 / 32)),
     }
+    g = torch.Generator(device="cuda").manual_seed(12)
+    col_signs = torch.randint(0, 256, (C // 8,), dtype=torch.uint8, device="cuda", generator=g)
+    row_signs = torch.randint(0, 256, (R // 8,), dtype=torch.uint8, device="cuda", generator=g)
+    sr_row = torch.randint(-32768, 32768, (R, C), dtype=torch.int16, device="cuda", generator=g)
+    sr_colT = torch.randint(-32768, 32768, (C, R), dtype=torch.int16, device="cuda", generator=g)
+    legs["signs_sr_dual"] = (lambda: mx.rotate_quantize_rand(x, had=16, mode=0, layouts=mx.LAYOUT_ROW | mx.LAYOUT_COLT,
+                                                             col_signs=col_signs, row_signs=row_signs, sr_row=sr_row,
+                                                             sr_colT=sr_colT),
+                             n * (2 + 2 * 2 + 2 * (0.5 + 1 / 32)))
     out = {"tensor": f"{R}x{C} bf16 activations, H16, OCP floor", "unit": "GB/s", "peak": hbm}
     for name, (fn, by) in legs.items():
         for _ in range(3):

@@ -197,6 +197,35 @@ mxfp4_status mxfp4_rotate_quantize_of(const void* x, int64_t rows, int64_t cols,
 mxfp4_status mxfp4_rotate_quantize_mbs(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
                                        mxfp4_tensor* q, uint8_t* mbs, mxfp4_stream_t stream);
 
+/* Randomised quantiser baselines of "Pretraining Large Language Models with MXFP4 on
+ * Native FP4 Hardware" (A.2: random sign flips before the Hadamard; the
+ * stochastic-rounding runs of the ablation).  The random numbers are inputs, owned by
+ * the caller, device memory, 16-byte aligned; NULL disables an option:
+ *   col_signs: bitmask of ceil(cols/8) bytes (bit i of byte i/8 = column i): column i is
+ *              negated before the rotation along cols (row copy).  A GEMM's two
+ *              operands must use the same mask over their shared contraction.
+ *   row_signs: bitmask over rows, for the rotation along rows (transposed copy).
+ *   sr_row:    uint16 [rows, cols] row-major, uniform integers: stochastic rounding of
+ *              the row copy.  A magnitude a in [lo, lo + step) of the E2M1 grid rounds
+ *              up iff r < ((a - lo) / step) * 65536; a >= 6 saturates; the sign is
+ *              kept.  The E8M0 scales are those of `mode`.
+ *   sr_colT:   uint16 [cols, rows] for the transposed copy.
+ * Stochastic rounding is on for a call when any requested layout has its array, and
+ * then every requested layout needs one. */
+typedef struct {
+    const uint8_t* col_signs;
+    const uint8_t* row_signs;
+    const uint16_t* sr_row;
+    const uint16_t* sr_colT;
+} mxfp4_quant_opts;
+
+/* mxfp4_rotate_quantize with the options above (layouts ROW, COLT or both; the 2D
+ * layout returns MXFP4_ERR_UNSUPPORTED_SHAPE when an option is set).  opts == NULL or
+ * all-NULL gives exactly mxfp4_rotate_quantize. */
+mxfp4_status mxfp4_rotate_quantize_ex(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                      unsigned layouts, const mxfp4_quant_opts* opts, mxfp4_tensor* row_out,
+                                      mxfp4_tensor* colT_out, mxfp4_tensor* twoD_out, mxfp4_stream_t stream);
+
 /* Workspace bytes needed by mxfp4_linear_{fprop,dgrad,wgrad} (op = MXFP4_OP_*). */
 size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp4_config* cfg);
 

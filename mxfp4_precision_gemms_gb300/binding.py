@@ -36,6 +36,12 @@ class MxTensorC(ctypes.Structure):
                 ("had", ctypes.c_int32), ("mode", ctypes.c_int32)]
 
 
+class QuantOptsC(ctypes.Structure):
+    """mxfp4_quant_opts: sign bitmasks and random integers (device pointers or NULL)."""
+    _fields_ = [("col_signs", ctypes.c_void_p), ("row_signs", ctypes.c_void_p), ("sr_row", ctypes.c_void_p),
+                ("sr_colT", ctypes.c_void_p)]
+
+
 class MxConfigC(ctypes.Structure):
     _fields_ = [("had", ctypes.c_int32), ("mode", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
                 ("accumulate", ctypes.c_int32)]
@@ -69,6 +75,7 @@ def lib():
                 "mxfp4_quantized_bytes": ([I64, I64, I, I], S),
                 "mxfp4_rotate_quantize": ([P, I64, I64, I64, I, I, U, T, T, T, P], I),
                 "mxfp4_rotate_quantize_of": ([P, I64, I64, I64, I, I, I, T, T, P], I),
+                "mxfp4_rotate_quantize_ex": ([P, I64, I64, I64, I, I, U, ctypes.POINTER(QuantOptsC), T, T, T, P], I),
                 "mxfp4_rotate_quantize_mbs": ([P, I64, I64, I64, I, I, T, P, P], I),
                 "mxfp4_gemm": ([T, T, P, I64, I, I, P, S, P], I),
                 "mxfp4_workspace_bytes": ([I, I64, I64, I64, CF], S),
@@ -235,6 +242,31 @@ def rotate_quantize_of(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLO
     for q in (q1, q2):
         q.had, q.mode = had, mode
     return q1, q2
+
+
+def rotate_quantize_rand(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR, layouts: int = LAYOUT_ROW,
+                         col_signs: torch.Tensor | None = None, row_signs: torch.Tensor | None = None,
+                         sr_row: torch.Tensor | None = None, sr_colT: torch.Tensor | None = None,
+                         sf_layout: int = SF_MMA, stream=None) -> dict:
+    """mxfp4_rotate_quantize_ex: random sign flips (uint8 bitmask tensors) and stochastic
+    rounding (int16/uint16 tensors of uniform 16-bit integers, [rows, cols] for the row
+    copy and [cols, rows] for the transposed copy).  Returns {'row': ..., 'colT': ...}."""
+    _check_bf16_matrix(x)
+    R, C = x.shape
+    outs = {}
+    if layouts & LAYOUT_ROW:
+        outs["row"] = empty_qtensor(R, C, LAYOUT_ROW, sf_layout, x.device)
+    if layouts & LAYOUT_COLT:
+        outs["colT"] = empty_qtensor(C, R, LAYOUT_COLT, sf_layout, x.device)
+    ptr = lambda t: None if t is None else t.data_ptr()
+    opts = QuantOptsC(ptr(col_signs), ptr(row_signs), ptr(sr_row), ptr(sr_colT))
+    cs = {k: v.c() for k, v in outs.items()}
+    ref = lambda k: ctypes.byref(cs[k]) if (k in cs) else None
+    _check(lib().mxfp4_rotate_quantize_ex(_ptr(x), R, C, x.stride(0), had, mode, layouts, ctypes.byref(opts),
+                                          ref("row"), ref("colT"), None, _stream(stream)))
+    for v in outs.values():
+        v.had, v.mode = had, mode
+    return outs
 
 
 def rotate_quantize_mbs(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR, sf_layout: int = SF_MMA,

@@ -49,6 +49,17 @@ cudaError_t launch_rotate_quantize_of(const QuantParams& p, const QuantOut& q2, 
                                       cudaStream_t s);
 cudaError_t launch_rotate_quantize_mbs(const QuantParams& p, uint8_t* mbs, int had, cudaStream_t s);
 
+// Randomised baselines (row / transposed layouts): sign bitmasks and 16-bit random
+// integers supplied by the caller (NULL: not used).
+struct RandOpts {
+    const uint8_t* col_signs;  // over C, for the row copy
+    const uint8_t* row_signs;  // over R, for the transposed copy
+    const uint16_t* sr_row;    // [R, C]
+    const uint16_t* sr_colT;   // [C, R]
+};
+cudaError_t launch_rotate_quantize_rand(const QuantParams& p, const RandOpts& o, int had, unsigned layouts,
+                                        cudaStream_t s);
+
 struct GemmParams {
     CUtensorMap map_a;   // codes of A [M, K/2] bytes, box 128 rows x 128 B, 128B swizzle
     CUtensorMap map_b;   // codes of B [N, K/2] bytes

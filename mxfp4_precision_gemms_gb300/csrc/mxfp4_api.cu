@@ -398,7 +398,7 @@ mxfp4_status check_fix_args(const void* x, int64_t rows, int64_t cols, int64_t l
 
 mxfp4_status clear_padding(std::initializer_list<mxfp4_tensor*> outs, cudaStream_t s) {
     for (mxfp4_tensor* t : outs)
-        if (needs_sf_padding(t)) {
+        if (t && needs_sf_padding(t)) {
             cudaError_t e =
                 cudaMemsetAsync(t->scales, 0, mxfp4_scales_bytes(t->rows, t->cols, t->layout, t->sf_layout), s);
             if (e != cudaSuccess) return cuda_fail(e, "clear scale padding");
@@ -449,6 +449,67 @@ mxfp4_status mxfp4_rotate_quantize_mbs(const void* x, int64_t rows, int64_t cols
     p.row = to_out(q);
     cudaError_t e = launch_rotate_quantize_mbs(p, mbs, had, s);
     if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize_mbs launch");
+    return ok();
+}
+
+mxfp4_status mxfp4_rotate_quantize_ex(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                      unsigned layouts, const mxfp4_quant_opts* opts, mxfp4_tensor* row_out,
+                                      mxfp4_tensor* colT_out, mxfp4_tensor* twoD_out, mxfp4_stream_t stream) {
+    const bool any = opts && (opts->col_signs || opts->row_signs || opts->sr_row || opts->sr_colT);
+    if (!any) return mxfp4_rotate_quantize(x, rows, cols, ld, had, mode, layouts, row_out, colT_out, twoD_out, stream);
+    if (layouts & MXFP4_LAYOUT_2D)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "random signs / stochastic rounding: row and column layouts only");
+    const bool want_row = layouts & MXFP4_LAYOUT_ROW, want_colT = layouts & MXFP4_LAYOUT_COLT;
+    const bool sr = (want_row && opts->sr_row) || (want_colT && opts->sr_colT);
+    if (sr && ((want_row && !opts->sr_row) || (want_colT && !opts->sr_colT)))
+        return fail(MXFP4_ERR_INVALID_ARG, "stochastic rounding needs random integers for every requested layout");
+    for (const void* q : {(const void*)opts->col_signs, (const void*)opts->row_signs, (const void*)opts->sr_row,
+                          (const void*)opts->sr_colT})
+        if (q && !aligned16(q)) return fail(MXFP4_ERR_MISALIGNED, "option arrays must be 16-byte aligned");
+    // Validation of shapes, descriptors and x exactly as the plain entry point; an empty
+    // problem touches nothing.
+    if (rows < 0 || cols < 0) return fail(MXFP4_ERR_INVALID_ARG, "negative size");
+    if (!valid_had(had)) return fail(MXFP4_ERR_INVALID_ARG, "hadamard must be 0, 16 or 32 (got %d)", had);
+    if (!valid_mode(mode)) return fail(MXFP4_ERR_INVALID_ARG, "scale mode must be 0 or 1 (got %d)", mode);
+    if (!layouts || (layouts & ~3u)) return fail(MXFP4_ERR_INVALID_ARG, "bad layout mask 0x%x", layouts);
+    if (cols % 32) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "cols (%lld) %% 32 != 0", (long long)cols);
+    if (want_colT && rows % 32)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "rows (%lld) %% 32 != 0 for the column layout", (long long)rows);
+    if ((want_row && !row_out) || (want_colT && !colT_out))
+        return fail(MXFP4_ERR_INVALID_ARG, "a requested output descriptor is NULL");
+    auto fill = [&](mxfp4_tensor* t, int64_t r, int64_t c, int layout) {
+        t->rows = r;
+        t->cols = c;
+        t->layout = layout;
+        t->had = had;
+        t->mode = mode;
+    };
+    if (want_row) fill(row_out, rows, cols, MXFP4_LAYOUT_ROW);
+    if (want_colT) fill(colT_out, cols, rows, MXFP4_LAYOUT_COLT);
+    if (rows == 0 || cols == 0) return ok();
+    if (!x) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
+    if (ld < cols || ld % 8)
+        return fail(MXFP4_ERR_MISALIGNED, "ld (%lld) must be >= cols and a multiple of 8", (long long)ld);
+    if (!aligned16(x)) return fail(MXFP4_ERR_MISALIGNED, "x not 16-byte aligned");
+    if ((rows + 63) / 64 > 65535) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "too many rows");
+    mxfp4_status st;
+    if (want_row && (st = check_out(row_out, "row_out", true))) return st;
+    if (want_colT && (st = check_out(colT_out, "colT_out", true))) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = clear_padding({want_row ? row_out : nullptr, want_colT ? colT_out : nullptr}, s))) return st;
+    QuantParams p{};
+    p.x = static_cast<const uint16_t*>(x);
+    p.R = rows;
+    p.C = cols;
+    p.ld = ld;
+    p.mode = mode;
+    p.row = to_out(want_row ? row_out : nullptr);
+    p.colT = to_out(want_colT ? colT_out : nullptr);
+    RandOpts o{opts->col_signs, opts->row_signs, opts->sr_row, opts->sr_colT};
+    cudaError_t e = launch_rotate_quantize_rand(p, o, had, layouts, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize_ex launch");
     return ok();
 }
 
