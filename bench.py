@@ -137,7 +137,7 @@ def kernel_sources_sha(files):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"gemm": ("gemm.cu", "ptx.cuh", "internal.h"), "quant": ("quantize.cu", "ptx.cuh", "internal.h")}
+KERNEL_SOURCES = {"gemm": ("gemm.cu", "ptx.cuh", "internal.h"), "quant": ("quantize.cu", "quant_math.cuh", "ptx.cuh", "internal.h")}
 
 
 def measured_traffic():
@@ -223,8 +223,9 @@ LAUNCHES_PER_LAYER = 6  # 3 rotate+quantise + 3 GEMM kernels
 def run_e2e_step(layers, ws, streams):
     """The same step through the public linear-layer API with host buffers: H2D of
     X, W, dY from pinned memory, fprop/dgrad/wgrad, D2H of Y, dX, dW.  Three streams
-    (copy-in, compute, copy-out) ordered per layer by events, so layer i+1's inputs
-    upload and layer i-1's outputs download while layer i computes."""
+    (copy-in, compute, copy-out) ordered by events at the finest grain the data allows:
+    Fprop starts once X and W have landed (dY still uploading), and each output starts
+    downloading as soon as the GEMM that writes it has finished."""
     import torch
 
     from mxfp4_precision_gemms_gb300 import binding as mx
@@ -235,27 +236,66 @@ def run_e2e_step(layers, ws, streams):
     start = torch.cuda.current_stream()
     for st in streams:
         st.wait_stream(start)
+
+    def mark(stream):
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        return ev
+
     for L in layers:
         with torch.cuda.stream(s_in):
             L.x.copy_(L.host["x"], non_blocking=True)
             L.w.copy_(L.host["w"], non_blocking=True)
+            ev_xw = mark(s_in)
             L.dy.copy_(L.host["dy"], non_blocking=True)
-            ev_in = torch.cuda.Event()
-            ev_in.record(s_in)
-        s_comp.wait_event(ev_in)
+            ev_dy = mark(s_in)
         with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev_xw)
             mx.linear_fprop(L.x, L.w, cfg, y=L.y, xT=L.xT, wT=L.wT, ws=ws, stream=s_comp)
+            ev_y = mark(s_comp)
+            s_comp.wait_event(ev_dy)
             mx.linear_dgrad(L.dy, L.wT, cfg, dx=L.dx, dyT=L.dyT, ws=ws, stream=s_comp)
+            ev_dx = mark(s_comp)
             mx.linear_wgrad(L.dyT, L.xT, wcfg, dw=L.dw, stream=s_comp)
-            ev_c = torch.cuda.Event()
-            ev_c.record(s_comp)
-        s_out.wait_event(ev_c)
+            ev_dw = mark(s_comp)
         with torch.cuda.stream(s_out):
-            L.out_host["y"].copy_(L.y, non_blocking=True)
-            L.out_host["dx"].copy_(L.dx, non_blocking=True)
-            L.out_host["dw"].copy_(L.dw, non_blocking=True)
+            for ev, src, dst in ((ev_y, L.y, "y"), (ev_dx, L.dx, "dx"), (ev_dw, L.dw, "dw")):
+                s_out.wait_event(ev)
+                L.out_host[dst].copy_(src, non_blocking=True)
     for st in streams:
         start.wait_stream(st)
+
+
+def link_bandwidth(nbytes=256 << 20, reps=3):
+    """Pinned host <-> device copy rates on this machine (GB/s): H2D alone, D2H alone and the
+    two directions at once (total), for the end-to-end copy bound."""
+    import torch
+
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t) / reps
+
+    def both():
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_b, non_blocking=True)
+
+    h2d = nbytes / timed(lambda: d_a.copy_(h_in, non_blocking=True)) / 1e9
+    d2h = nbytes / timed(lambda: h_out.copy_(d_b, non_blocking=True)) / 1e9
+    bi = 2 * nbytes / timed(both) / 1e9
+    return {"h2d_gbs": round(h2d, 1), "d2h_gbs": round(d2h, 1), "concurrent_total_gbs": round(bi, 1)}
 
 
 def gpu_arm(args, rank, world, dist):
@@ -355,8 +395,13 @@ def gpu_arm(args, rank, world, dist):
         tot = max_over_ranks(sum(e2e_ms), dist, dev)
         h2d = sum(L.x.numel() * 2 + L.w.numel() * 2 + L.dy.numel() * 2 for L in layers)
         d2h = sum(L.y.numel() * 2 + L.dx.numel() * 2 + L.dw.numel() * 4 for L in layers)
+        link = link_bandwidth()
+        # copy bound: both directions share the link; the larger direction at half the
+        # concurrent rate, or the total at the concurrent rate, whichever is longer
+        bound_ms = max(max(h2d, d2h) / (link["concurrent_total_gbs"] / 2), (h2d + d2h) / link["concurrent_total_gbs"]) / 1e6
         e2e = {"value": round(world * fl * args.steps / (tot * 1e-3) / 1e12, 2), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(tot / args.steps, 3)}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(tot / args.steps, 3),
+               "link": link, "copy_bound_ms_per_step": round(bound_ms, 3)}
         assert mx.device_status() == 0
 
     fixes = None

@@ -49,7 +49,7 @@ def test_traffic_record_parser(tmp_path, monkeypatch):
     out_dir.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     os.makedirs(tmp_path / "mxfp4_precision_gemms_gb300" / "csrc")
-    for f in ("gemm.cu", "ptx.cuh", "internal.h", "quantize.cu"):
+    for f in {f for files in bench.KERNEL_SOURCES.values() for f in files}:
         (tmp_path / "mxfp4_precision_gemms_gb300" / "csrc" / f).write_text(f)
     bench.write_traffic(str(src))
     rec = json.load(open(out_dir / "traffic_llama8b_linears_T8192.json"))
