@@ -124,7 +124,7 @@ __device__ __forceinline__ uint32_t mbs_byte(float A) {
 }
 
 template <int HAD>
-__global__ void __launch_bounds__(FX_THREADS, 4) rq_mbs_kernel(const QuantParams p, uint8_t* mbs) {
+__global__ void __launch_bounds__(FX_THREADS, 5) rq_mbs_kernel(const QuantParams p, uint8_t* mbs) {
     const int t = threadIdx.x;
     const int s = t & 3, pr = t >> 2;
     const int64_t row0 = (int64_t)blockIdx.y * FX_TR, col0 = (int64_t)blockIdx.x * FX_TC;
