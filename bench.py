@@ -485,6 +485,27 @@ def quant_fixes_leg(flush, hbm, iters=20):
             tot += a.elapsed_time(b)
         gbs = by / (tot / iters * 1e-3) / 1e9
         out[name] = {"gbs": round(gbs, 1), "frac": round(gbs / hbm, 4), "us": round(tot / iters * 1e3, 1)}
+    # the quantiser sweep of the heavy-tailed tensors (0.1 t(3) + 0.1% entries x100):
+    # {none, H16, H32} x {row, colT, 2D} x {floor, ceil}, GB/s
+    xs = mx.bf16_tensor(synth.heavy_tailed(R, C, 13))
+    sweep = {}
+    for had in (mx.HAD_NONE, mx.HAD_16, mx.HAD_32):
+        for lay, lname, by in ((mx.LAYOUT_ROW, "row", 2 + 0.5 + 1 / 32), (mx.LAYOUT_COLT, "colT", 2 + 0.5 + 1 / 32),
+                               (mx.LAYOUT_2D, "2d", 2 + 0.5 + 1 / 1024)):
+            for mode, mname in ((mx.SCALE_FLOOR, "floor"), (mx.SCALE_CEIL, "ceil")):
+                fn = lambda: mx.rotate_quantize(xs, had, mode, lay, sf_layout=mx.SF_PLAIN)
+                fn()
+                tot = 0.0
+                for _ in range(5):
+                    flush.fill_(1.0)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    fn()
+                    b.record()
+                    b.synchronize()
+                    tot += a.elapsed_time(b)
+                sweep[f"h{had}_{lname}_{mname}"] = round(n * by / (tot / 5 * 1e-3) / 1e9, 1)
+    out["sweep_gbs"] = sweep
     assert mx.device_status() == 0
     return out
 
@@ -627,9 +648,11 @@ def reference_arm(args, rank, world):
 
 
 def profile_case():
-    """Small case for ncu captures: the down-proj X quantiser (8192x14336 bf16, 235 MB,
-    row + transposed copies) and the gate/up Fprop GEMM (8192x14336x4096, bf16 out),
-    each launched twice (capture the second launch with -s 1 -c 1)."""
+    """Small case for ncu captures, each kernel launched twice (capture the second):
+    the down-proj X quantiser (8192x14336 bf16, 235 MB, row + transposed copies; rq_kernel
+    -s 1), and three GEMM shape classes (mxf4_gemm): gate/up Fprop 8192x14336x4096 bf16 out
+    (-s 1), gate/up Wgrad 14336x4096x8192 fp32 out (-s 3), k/v Dgrad 8192x4096x1024 bf16
+    out (-s 5)."""
     import torch
 
     from mxfp4_precision_gemms_gb300 import binding as mx
@@ -646,6 +669,20 @@ def profile_case():
     wq = mx.rotate_quantize(w, mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW)["row"]
     for _ in range(2):
         mx.gemm(xq, wq, mx.OUT_BF16)
+    # Wgrad: dW [14336, 4096] = dY^T X, contraction over the 8192 tokens, fp32 out
+    dyt = mx.rotate_quantize(mx.bf16_tensor(synth.output_grads(14336, 8192, 4)), mx.HAD_16, mx.SCALE_FLOOR,
+                             mx.LAYOUT_ROW)["row"]
+    xt = mx.rotate_quantize(mx.bf16_tensor(synth.activations(4096, 8192, 5)), mx.HAD_16, mx.SCALE_FLOOR,
+                            mx.LAYOUT_ROW)["row"]
+    for _ in range(2):
+        mx.gemm(dyt, xt, mx.OUT_F32)
+    # k/v Dgrad: dX [8192, 4096] = dY W, contraction over N = 1024
+    dy = mx.rotate_quantize(mx.bf16_tensor(synth.output_grads(8192, 1024, 6)), mx.HAD_16, mx.SCALE_FLOOR,
+                            mx.LAYOUT_ROW)["row"]
+    wt = mx.rotate_quantize(mx.bf16_tensor(synth.weights(4096, 1024, 7)), mx.HAD_16, mx.SCALE_FLOOR,
+                            mx.LAYOUT_ROW)["row"]
+    for _ in range(2):
+        mx.gemm(dy, wt, mx.OUT_BF16)
     torch.cuda.synchronize()
     assert mx.device_status() == 0
     print("profile case ok")
