@@ -49,6 +49,15 @@ constexpr bool STAGE_F32 = MXQ_STAGE_F32 != 0;
 constexpr int TILE_BYTES = STAGE_F32 ? TR * TC * 4 : TR * TC * 2;
 static_assert(TR == 32 || TR == 64 || TR == 128, "tile rows");
 
+// 1: the row copy's scale bytes (MMA order) leave as one 32-bit store per row, gathered
+// by warp shuffles, and the transposed copy's codes and scale bytes are staged in shared
+// memory so that each output row's piece leaves as one 32-byte (or two 16-byte) store
+// and one 16-bit scale store; 0: every thread stores its own 16-byte pieces and bytes.
+#ifndef MXQ_COALESCE
+#define MXQ_COALESCE 1
+#endif
+static_assert(!MXQ_COALESCE || MXQ_ROWS == 64, "the transposed-copy staging is laid out for 64-row tiles");
+
 // 1: persistent TMA-fed kernel (rq_tma_kernel); 0: one tile per CTA (rq_kernel).
 #ifndef MXQ_TMA
 #define MXQ_TMA 0
@@ -67,12 +76,31 @@ __device__ __forceinline__ int bf16_chunk(int r, int q) {
     return r * (TC / 2) + ((q ^ ((q >> 2) & 3) ^ ((r & 1) << 2)) << 2);
 }
 
+// One 32-byte global store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_32B(void* dst, uint4 a, uint4 b) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a.x), "r"(a.y),
+                 "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
+// Staging of the transposed codes: 16-byte chunk (column pair cp, row block rb, column
+// h of the pair) at chunk 4 cp + ((2 rb + h) ^ ((cp >> 1) & 3)).  The column work's
+// writes (32 consecutive pairs, fixed rb and h) and the per-output-row reads (16 pairs,
+// both h) each spread over all eight 16-byte bank groups.
+__device__ __forceinline__ int colt_stage_chunk(int cp, int rb, int h) {
+    return 4 * cp + ((2 * rb + h) ^ ((cp >> 1) & 3));
+}
+
 template <int HAD, bool ROW, bool COLT, bool TWOD>
 __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel(const QuantParams p) {
     extern __shared__ __align__(16) uint8_t q_smem[];
     float* tile_f = reinterpret_cast<float*>(q_smem);
     uint32_t* tile_w = reinterpret_cast<uint32_t*>(q_smem);
     float* seg_amax = reinterpret_cast<float*>(q_smem + (COLT ? TILE_BYTES : 0));
+    // transposed-copy staging (MXQ_COALESCE): codes of the tile's 128 output rows x 2
+    // row blocks (4 KB), then their scale bytes
+    [[maybe_unused]] uint8_t* colt_codes = q_smem + TILE_BYTES;
+    [[maybe_unused]] uint8_t* colt_scales = colt_codes + TC * (TR / 2);
 
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.y * TR;
@@ -158,14 +186,37 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
             const uint32_t bytex = scale_byte(ax, p.mode), bytey = scale_byte(ay, p.mode);
             uint4 qx, qy;
             quant32x2<HAD>(v, bytex, bytey, qx, qy);
-            if (vx) {
-                *reinterpret_cast<uint4*>(p.row.codes + grx * (p.C / 2) + gc / 2) = qx;
-                store_scale(p.row, grx, gc / 32, p.C / 32, bytex);
+            if (vx) *reinterpret_cast<uint4*>(p.row.codes + grx * (p.C / 2) + gc / 2) = qx;
+            if (vy) *reinterpret_cast<uint4*>(p.row.codes + gry * (p.C / 2) + gc / 2) = qy;
+#if MXQ_COALESCE
+            // The four segments of a row are lanes 4 pr .. 4 pr + 3 and their four bytes are
+            // consecutive (k = col0/32 + s, col0/32 a multiple of 4) in both scale orders.
+            // MMA order: one 32-bit store, rows past R and columns past C carrying byte 0
+            // into the zeroed padding.  Plain order: one 32-bit store when the row exists,
+            // all four blocks exist and the offset is 4-byte aligned, else byte stores.
+            uint32_t wx = bytex << (8 * s), wy = bytey << (8 * s);
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                wx |= __shfl_xor_sync(0xffffffffu, wx, o);
+                wy |= __shfl_xor_sync(0xffffffffu, wy, o);
             }
-            if (vy) {
-                *reinterpret_cast<uint4*>(p.row.codes + gry * (p.C / 2) + gc / 2) = qy;
-                store_scale(p.row, gry, gc / 32, p.C / 32, bytey);
+            const int64_t k0 = col0 / 32, kb = p.C / 32;
+            if (p.row.sf_mma) {
+                if (s == 0) {
+                    *reinterpret_cast<uint32_t*>(p.row.scales + sf_mma_offset(grx, k0, p.row.kb_pad)) = wx;
+                    *reinterpret_cast<uint32_t*>(p.row.scales + sf_mma_offset(gry, k0, p.row.kb_pad)) = wy;
+                }
+            } else if (k0 + 4 <= kb && (kb & 3) == 0) {
+                if (s == 0 && grx < p.R) *reinterpret_cast<uint32_t*>(p.row.scales + grx * kb + k0) = wx;
+                if (s == 0 && gry < p.R) *reinterpret_cast<uint32_t*>(p.row.scales + gry * kb + k0) = wy;
+            } else {
+                if (vx) store_scale(p.row, grx, gc / 32, p.C / 32, bytex);
+                if (vy) store_scale(p.row, gry, gc / 32, p.C / 32, bytey);
             }
+#else
+            if (vx) store_scale(p.row, grx, gc / 32, p.C / 32, bytex);
+            if (vy) store_scale(p.row, gry, gc / 32, p.C / 32, bytey);
+#endif
         }
     }
 
@@ -194,17 +245,61 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
             const uint32_t bytex = scale_byte(ax, p.mode), bytey = scale_byte(ay, p.mode);
             uint4 qx, qy;
             quant32x2<HAD>(v, bytex, bytey, qx, qy);
+#if MXQ_COALESCE
+            uint4* cst = reinterpret_cast<uint4*>(colt_codes);
+            cst[colt_stage_chunk(cp, rb, 0)] = qx;
+            cst[colt_stage_chunk(cp, rb, 1)] = qy;
+            colt_scales[(2 * cp) * 2 + rb] = (uint8_t)bytex;
+            colt_scales[(2 * cp + 1) * 2 + rb] = (uint8_t)bytey;
+#else
             *reinterpret_cast<uint4*>(p.colT.codes + gcol * (p.R / 2) + grow / 2) = qx;
             *reinterpret_cast<uint4*>(p.colT.codes + (gcol + 1) * (p.R / 2) + grow / 2) = qy;
             store_scale(p.colT, gcol, grow / 32, p.R / 32, bytex);
             store_scale(p.colT, gcol + 1, grow / 32, p.R / 32, bytey);
+#endif
         }
+#if MXQ_COALESCE
+        __syncthreads();
+        // one thread per output row c: the tile's rows give it 16 bytes per valid 32-row block
+        for (int c = t; c < TC; c += QTHREADS) {
+            const int64_t orow = col0 + c;
+            const int64_t left = (p.R - row0) / 32;
+            const int nrb = left >= 2 ? 2 : (int)left;  // valid 32-row blocks of the tile
+            if (orow >= p.C || nrb <= 0) continue;
+            const uint4* cst = reinterpret_cast<const uint4*>(colt_codes);
+            const int cp = c >> 1, h = c & 1;
+            uint8_t* dst = p.colT.codes + orow * (p.R / 2) + row0 / 2;
+            const uint4 a = cst[colt_stage_chunk(cp, 0, h)];
+            if (nrb == 2) {
+                const uint4 b = cst[colt_stage_chunk(cp, 1, h)];
+                if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+                    st_global_32B(dst, a, b);
+                } else {
+                    reinterpret_cast<uint4*>(dst)[0] = a;
+                    reinterpret_cast<uint4*>(dst)[1] = b;
+                }
+            } else {
+                *reinterpret_cast<uint4*>(dst) = a;
+            }
+            const uint8_t b0 = colt_scales[c * 2], b1 = colt_scales[c * 2 + 1];
+            // k = row0/32 (even) and k + 1 are adjacent bytes in both scale orders
+            const int64_t off = p.colT.sf_mma ? sf_mma_offset(orow, row0 / 32, p.colT.kb_pad)
+                                              : orow * (p.R / 32) + row0 / 32;
+            if (nrb == 2 && (off & 1) == 0) {
+                *reinterpret_cast<uint16_t*>(p.colT.scales + off) = (uint16_t)(b0 | (b1 << 8));
+            } else {
+                store_scale(p.colT, orow, row0 / 32, p.R / 32, b0);
+                if (nrb == 2) store_scale(p.colT, orow, row0 / 32 + 1, p.R / 32, b1);
+            }
+        }
+#endif
     }
 }
 
 template <int HAD, bool ROW, bool COLT, bool TWOD>
 cudaError_t launch_one(const QuantParams& p, cudaStream_t s) {
-    constexpr int smem = (COLT ? TILE_BYTES : 0) + (TWOD ? TR * 4 * 4 : 0);
+    constexpr int smem = (COLT ? TILE_BYTES + (MXQ_COALESCE ? TC * (TR / 2) + TC * (TR / 32) : 0) : 0) +
+                         (TWOD ? TR * 4 * 4 : 0);
     auto kern = rq_kernel<HAD, ROW, COLT, TWOD>;
     if constexpr (smem > 48 * 1024) {
         static bool configured[64] = {};
@@ -233,14 +328,14 @@ constexpr int Q_TILE_BYTES = TR * TC * 2;
 constexpr int Q_BOX_BYTES = Q_TILE_BYTES / 2;  // 64 columns
 constexpr int Q_OFF_BAR = Q_STAGES * Q_TILE_BYTES;
 constexpr int Q_OFF_AMAX = Q_OFF_BAR + 8 * Q_STAGES;
-constexpr int Q_TMA_SMEM = Q_OFF_AMAX + TR * 4 * 4 + 1024;  // + alignment slack
+[[maybe_unused]] constexpr int Q_TMA_SMEM = Q_OFF_AMAX + TR * 4 * 4 + 1024;  // + alignment slack
 static_assert(Q_TILE_BYTES % 1024 == 0 && Q_BOX_BYTES % 1024 == 0, "128-byte swizzle atoms");
 
 // 32-bit word index of 16-byte chunk c (0..15) of tile row r in a stage: columns 0-63
 // are box 0, 64-127 box 1; within a box row r is 128 B with chunk c at (c % 8) ^ (r % 8).
 // Row-wise 16-byte reads (8 rows x 4 segments per warp) and column-wise 32-bit reads
 // (32 column pairs of one row per warp) are both bank-conflict free.
-__device__ __forceinline__ int stage_word(int r, int c) {
+[[maybe_unused]] __device__ __forceinline__ int stage_word(int r, int c) {
     return ((c >> 3) * Q_BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4)) >> 2;
 }
 
