@@ -77,7 +77,7 @@ __device__ __forceinline__ void store_row(const QuantOut& o, const QuantParams& 
 }
 
 template <int HAD>
-__global__ void __launch_bounds__(FX_THREADS, 4) rq_of_kernel(const QuantParams p, const QuantOut q2, int alpha_log2) {
+__global__ void __launch_bounds__(FX_THREADS, 5) rq_of_kernel(const QuantParams p, const QuantOut q2, int alpha_log2) {
     const int t = threadIdx.x;
     const int s = t & 3, pr = t >> 2;
     const int64_t row0 = (int64_t)blockIdx.y * FX_TR, col0 = (int64_t)blockIdx.x * FX_TC;

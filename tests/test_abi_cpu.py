@@ -69,6 +69,48 @@ def test_rotate_quantize_rejects_bad_arguments(L):
     assert _rq(L, layouts=4, twoD=_tensor(sf=1)) == 1    # 2D has plain scales only
 
 
+def test_quantiser_row_limit(L):
+    t = _tensor()
+    assert _rq(L, rows=65535 * 64 + 1, row=t) == 2        # grid limit of the 64-row tiles
+    assert b"rows" in L.mxfp4_last_error()
+
+
+def test_quantiser_fixes_reject_bad_arguments(L):
+    P = ctypes.c_void_p
+    t1, t2 = _tensor(), _tensor()
+    of = lambda x=0x1000, rows=64, cols=256, ld=256, had=16, mode=0, a=-1, q1=t1, q2=t2: L.mxfp4_rotate_quantize_of(
+        P(x), rows, cols, ld, had, mode, a, ctypes.byref(q1) if q1 else None, ctypes.byref(q2) if q2 else None, None)
+    assert of(a=1) == 1 and of(a=-9) == 1                 # alpha = 2^a with a in [-8, 0]
+    assert of(had=8) == 1 and of(mode=3) == 1
+    assert of(cols=48, ld=48) == 2                        # cols % 32
+    assert of(q2=None) == 1                               # missing output
+    assert of(x=0) == 1                                   # NULL input
+    assert of(rows=0) == 0                                # empty: nothing touched
+    assert of(ld=100) == 3 and of(x=0x1008) == 3          # ld % 8, misaligned x
+    assert of(q1=_tensor(codes=0x1004)) == 3              # misaligned codes
+    mbs = lambda cols=256, ld=256, m=0x5000, q=t1: L.mxfp4_rotate_quantize_mbs(
+        P(0x1000), 64, cols, ld, 16, 0, ctypes.byref(q) if q else None, P(m) if m else None, None)
+    assert mbs(cols=96, ld=96) == 2                       # cols % 128
+    assert mbs(m=0) == 1                                  # mbs bytes missing
+    assert mbs(q=None) == 1
+
+
+def test_randomised_options_reject_bad_arguments(L):
+    P = ctypes.c_void_p
+    t1, t2 = _tensor(), _tensor()
+
+    def ex(layouts=3, cs=0, rs=0, srr=0, src=0, rows=64, cols=256, twoD=None):
+        o = mx.QuantOptsC(cs or None, rs or None, srr or None, src or None)
+        return L.mxfp4_rotate_quantize_ex(P(0x1000), rows, cols, cols, 16, 0, layouts, ctypes.byref(o),
+                                          ctypes.byref(t1), ctypes.byref(t2), ctypes.byref(twoD) if twoD else None,
+                                          None)
+    assert ex(srr=0x8000) == 1                            # stochastic rounding for one of two copies
+    assert ex(layouts=4, cs=0x8000, twoD=_tensor(layout=4, sf=0)) == 2  # 2D with an option
+    assert ex(cs=0x8008) == 3                             # option arrays 16-byte aligned
+    assert ex(rows=40, cs=0x8000) == 2                    # rows % 32 for the column copy
+    assert ex(rows=0, srr=0x8000, src=0x9000) == 0        # empty: nothing touched
+
+
 def test_gemm_rejects_bad_arguments(L):
     a, b = _tensor(), _tensor()
     c = ctypes.c_void_p(0x4000)
