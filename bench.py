@@ -494,7 +494,8 @@ def quant_fixes_leg(flush, hbm, iters=20):
                                (mx.LAYOUT_2D, "2d", 2 + 0.5 + 1 / 1024)):
             for mode, mname in ((mx.SCALE_FLOOR, "floor"), (mx.SCALE_CEIL, "ceil")):
                 fn = lambda: mx.rotate_quantize(xs, had, mode, lay, sf_layout=mx.SF_PLAIN)
-                fn()
+                for _ in range(3):
+                    fn()
                 tot = 0.0
                 for _ in range(5):
                     flush.fill_(1.0)
