@@ -84,7 +84,8 @@ def _sampled_checks(torch, X, W, dY, had, mode, y, dx, dw, n=256, seed=0):
     assert_within(dw[r, c].double().cpu().numpy(), want, S, what="wgrad sampled")
 
 
-@pytest.mark.parametrize("name,N,K", [("qkv", 6144, 4096), ("down", 4096, 14336), ("k", 1024, 4096)])
+@pytest.mark.parametrize("name,N,K", [("qkv", 6144, 4096), ("o", 4096, 4096), ("gate_up", 14336, 4096),
+                                    ("down", 4096, 14336), ("k", 1024, 4096)])
 def test_llama8b_linears_sampled(torch, name, N, K):
     """Config 2 shapes at T = 8192 in the launch configuration the benchmark times
     (bf16 Fprop/Dgrad outputs, fp32 Wgrad)."""
