@@ -130,7 +130,7 @@ __device__ __forceinline__ void stage_and_store(const GemmParams& p, uint8_t* st
 }
 
 // One TMEM chunk (32 fp32 columns of this lane's row) -> bf16 or fp32 global output.
-__device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stg, int lane, int64_t row_base,
+[[maybe_unused]] __device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stg, int lane, int64_t row_base,
                                            int64_t col0, const uint32_t (&v)[32]) {
     if (p.out_bf16) {
         uint32_t w[16];
@@ -635,6 +635,8 @@ cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
 }
 
 
+// Returns cudaErrorNotSupported (nothing launched) when no cluster of two CTAs can be
+// resident on this device, so the caller can fall back to the single-CTA kernel.
 template <int STAGES>
 cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
     using Cfg = PairCfg<STAGES>;
@@ -665,10 +667,10 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
         int n = 0;
         e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
         if (e != cudaSuccess) return e;
-        if (n < 1) return cudaErrorInvalidConfiguration;
         max_clusters[dev] = n;
         configured[dev] = true;
     }
+    if (max_clusters[dev] < 1) return cudaErrorNotSupported;
     const int64_t tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
     const int64_t clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
     cfg.gridDim = dim3((unsigned)(2 * clusters));
@@ -682,7 +684,10 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
 // tiles, BN = 256 unless the whole N fits in 128 columns.
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s) {
 #if MXG_PAIR
-    if (p.M > 128 && p.N > 128) return launch_pair<MXG_PAIR_STAGES>(p, s);
+    if (p.M > 128 && p.N > 128) {
+        const cudaError_t e = launch_pair<MXG_PAIR_STAGES>(p, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
 #endif
     if (p.N <= 128) return launch_cfg<128, 6, 2>(p, s);
 #ifdef MXG_FORCE_BN128
