@@ -616,20 +616,15 @@ template <int BN, int STAGES, int ACC>
 cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
     using Cfg = GemmCfg<BN, STAGES, ACC>;
     auto kern = mxf4_gemm_kernel<BN, STAGES, ACC>;
-    static bool configured[64] = {};
-    static int sm_count[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
+    static DeviceSlots sm_slots;
+    int sm_count = 0;
+    cudaError_t e = per_device_setting(sm_slots, &sm_count, [&](int dev, int* n) {
+        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        return r != cudaSuccess ? r : cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+    });
+    if (e != cudaSuccess) return e;
     const int64_t tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
-    const unsigned grid = (unsigned)(tiles < sm_count[dev] ? tiles : sm_count[dev]);
+    const unsigned grid = (unsigned)(tiles < sm_count ? tiles : sm_count);
     kern<<<grid, GEMM_THREADS, Cfg::SMEM, s>>>(p);
     return cudaGetLastError();
 }
@@ -641,11 +636,7 @@ template <int STAGES>
 cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
     using Cfg = PairCfg<STAGES>;
     auto kern = mxf4_gemm_pair_kernel<STAGES>;
-    static bool configured[64] = {};
-    static int max_clusters[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static DeviceSlots cluster_slots;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -657,22 +648,21 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-        if (e != cudaSuccess) return e;
+    int max_clusters = 0;
+    cudaError_t e = per_device_setting(cluster_slots, &max_clusters, [&](int dev, int* n) {
+        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        if (r != cudaSuccess) return r;
         int sms = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        cfg.gridDim = dim3((unsigned)(sms & ~1));
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        max_clusters[dev] = n;
-        configured[dev] = true;
-    }
-    if (max_clusters[dev] < 1) return cudaErrorNotSupported;
+        r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (r != cudaSuccess) return r;
+        cudaLaunchConfig_t probe = cfg;
+        probe.gridDim = dim3((unsigned)(sms & ~1));
+        return cudaOccupancyMaxActiveClusters(n, kern, &probe);
+    });
+    if (e != cudaSuccess) return e;
+    if (max_clusters < 1) return cudaErrorNotSupported;
     const int64_t tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
-    const int64_t clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
+    const int64_t clusters = tiles < max_clusters ? tiles : max_clusters;
     cfg.gridDim = dim3((unsigned)(2 * clusters));
     return cudaLaunchKernelEx(&cfg, kern, p);
 }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/mxfp4.h"
 
 namespace mx {
@@ -84,6 +86,31 @@ cudaError_t run_mma_peak_probe(int kind, int64_t iters, float* ms, int* ctas, ui
 
 cudaError_t launch_error_decomposition(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
                                        double* out, cudaStream_t s);
+
+// A launch setting computed once per device (a kernel's shared-memory opt-in, its grid
+// limit).  Thread-safe: concurrent first calls may both run compute(dev, &value); the
+// value is the same for both and is published with release / acquire ordering.  Values
+// must be >= 0; a slot holds value + 1, so 0 means "not computed yet".
+constexpr int kMaxCachedDevices = 64;
+using DeviceSlots = std::atomic<int>[kMaxCachedDevices];
+template <class F>
+cudaError_t per_device_setting(DeviceSlots& slots, int* value, F&& compute) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxCachedDevices) return cudaErrorInvalidDevice;
+    int v = slots[dev].load(std::memory_order_acquire);
+    if (v == 0) {
+        int r = 0;
+        e = compute(dev, &r);
+        if (e != cudaSuccess) return e;
+        if (r < 0) return cudaErrorInvalidValue;
+        v = r + 1;
+        slots[dev].store(v, std::memory_order_release);
+    }
+    *value = v - 1;
+    return cudaSuccess;
+}
 
 // Host helpers implemented in mxfp4_api.cu.
 uint32_t* device_status_ptr();  // for the current device

@@ -302,15 +302,12 @@ cudaError_t launch_one(const QuantParams& p, cudaStream_t s) {
                          (TWOD ? TR * 4 * 4 : 0);
     auto kern = rq_kernel<HAD, ROW, COLT, TWOD>;
     if constexpr (smem > 48 * 1024) {
-        static bool configured[64] = {};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!configured[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess) return e;
-            configured[dev] = true;
-        }
+        static DeviceSlots opted_in;
+        int unused = 0;
+        const cudaError_t e = per_device_setting(opted_in, &unused, [&](int, int*) {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        });
+        if (e != cudaSuccess) return e;
     }
     const dim3 grid((unsigned)((p.C + TC - 1) / TC), (unsigned)((p.R + TR - 1) / TR));
     kern<<<grid, QTHREADS, smem, s>>>(p);
@@ -469,24 +466,22 @@ __global__ void __launch_bounds__(QTHREADS, QBLOCKS_PER_SM) rq_tma_kernel(const 
 template <int HAD, bool ROW, bool COLT, bool TWOD>
 cudaError_t launch_tma_one(const QuantTmaParams& P, cudaStream_t st) {
     auto kern = rq_tma_kernel<HAD, ROW, COLT, TWOD>;
-    static bool configured[64] = {};
-    static int grid_max[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_TMA_SMEM);
-        if (e != cudaSuccess) return e;
+    static DeviceSlots grid_slots;
+    int grid_max = 0;
+    const cudaError_t e = per_device_setting(grid_slots, &grid_max, [&](int dev, int* g) {
+        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_TMA_SMEM);
+        if (r != cudaSuccess) return r;
         int sms = 0, per_sm = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, QTHREADS, Q_TMA_SMEM);
-        if (e != cudaSuccess) return e;
+        r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (r != cudaSuccess) return r;
+        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, QTHREADS, Q_TMA_SMEM);
+        if (r != cudaSuccess) return r;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        grid_max[dev] = sms * per_sm;
-        configured[dev] = true;
-    }
-    const unsigned grid = (unsigned)(P.tiles < grid_max[dev] ? P.tiles : grid_max[dev]);
+        *g = sms * per_sm;
+        return cudaSuccess;
+    });
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(P.tiles < grid_max ? P.tiles : grid_max);
     kern<<<grid, QTHREADS, Q_TMA_SMEM, st>>>(P);
     return cudaGetLastError();
 }
