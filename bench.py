@@ -75,6 +75,14 @@ def barrier(dist):
         dist.barrier()
 
 
+def job_throughput(local_ms, work_per_step, steps, world, dist, device):
+    """Whole-job throughput of `steps` timed steps on every rank: each rank did
+    `work_per_step` units per step in `local_ms` milliseconds in total; the job's time
+    is the slowest rank's.  Returns (units per second over all ranks, ms per step)."""
+    total_ms = max_over_ranks(local_ms, dist, device)
+    return world * work_per_step * steps / (total_ms * 1e-3), total_ms / steps
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -369,10 +377,9 @@ def gpu_arm(args, rank, world, dist):
     barrier(dist)
     status = mx.device_status()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    total_ms = max_over_ranks(sum(step_ms), dist, dev)
-    ms_per_step = total_ms / args.steps
     fl = flops_per_step()
-    value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
+    value, ms_per_step = job_throughput(sum(step_ms), fl, args.steps, world, dist, dev)
+    value /= 1e12
 
     # ---- per-kernel rooflines from the events of the timed region
     agg = {}
@@ -426,7 +433,7 @@ def gpu_arm(args, rank, world, dist):
             b.record()
             b.synchronize()
             e2e_ms.append(a.elapsed_time(b))
-        tot = max_over_ranks(sum(e2e_ms), dist, dev)
+        e2e_value, e2e_ms_per_step = job_throughput(sum(e2e_ms), fl, args.steps, world, dist, dev)
         h2d = sum(L.x.numel() * 2 + L.w.numel() * 2 + L.dy.numel() * 2 for L in layers)
         d2h = sum(L.y.numel() * 2 + L.dx.numel() * 2 + L.dw.numel() * 4 for L in layers)
         link = link_bandwidth()
@@ -434,8 +441,8 @@ def gpu_arm(args, rank, world, dist):
         # together at the concurrent rate (a lower bound on any schedule of these copies)
         bound_ms = max(h2d / link["h2d_gbs"], d2h / link["d2h_gbs"], (h2d + d2h) / link["concurrent_total_gbs"]) / 1e6
         copies_ms = copy_only_step_ms(layers, streams, args.steps, max(1, args.warmup))
-        e2e = {"value": round(world * fl * args.steps / (tot * 1e-3) / 1e12, 2), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(tot / args.steps, 3),
+        e2e = {"value": round(e2e_value / 1e12, 2), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_per_step, 3),
                "link": link, "copy_bound_ms_per_step": round(bound_ms, 3),
                "copies_alone_ms_per_step": round(copies_ms, 3)}
         assert mx.device_status() == 0
@@ -643,11 +650,20 @@ def oracle_sample(tokens: int, linears):
     return fl, sec
 
 
-def cpu_baseline_leg():
+def oracle_on_host_cores():
+    """Loads the oracle with one OpenMP thread per core this process may run on.  Under
+    torchrun OMP_NUM_THREADS is 1 for every rank, but only rank 0 runs the oracle."""
     import oracle
-    from mxfp4_precision_gemms_gb300 import synth
 
     oracle.lib()
+    oracle.set_num_threads(len(os.sched_getaffinity(0)))
+    return oracle
+
+
+def cpu_baseline_leg():
+    from mxfp4_precision_gemms_gb300 import synth
+
+    oracle = oracle_on_host_cores()
     tokens = 256  # about 10-20 s of CPU work on a 16-core host
     fl, sec = oracle_sample(tokens, synth.LLAMA8B_LINEARS)
     return {"value": round(fl / sec / 1e12, 6), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
@@ -659,10 +675,9 @@ def reference_arm(args, rank, world):
     """The CPU oracle as the reference arm, on a bounded slab of the same workload."""
     if rank != 0:
         return None
-    import oracle
     from mxfp4_precision_gemms_gb300 import synth
 
-    oracle.lib()
+    oracle = oracle_on_host_cores()
     tokens = 32  # the transposed (Wgrad) copies quantise blocks of 32 tokens
     lin = synth.LLAMA8B_LINEARS[:1]
     for _ in range(args.warmup):
