@@ -281,8 +281,9 @@ mxfp4_status mxfp4_linear_fprop_noalloc(const void* x, const void* w, int64_t M,
 size_t mxfp4_noalloc_scratch_bytes(void);
 
 /* Synchronises `stream`, then returns and clears the current device's status word:
- * MXFP4_OK, or MXFP4_ERR_TIMEOUT if a kernel's bounded wait expired since the last
- * call (that kernel returned early and its output is invalid). */
+ * MXFP4_OK, MXFP4_ERR_TIMEOUT if a kernel's bounded wait expired since the last call,
+ * or MXFP4_ERR_CUDA if a GEMM kernel found its shared memory misaligned for its tile
+ * layout.  In both error cases that kernel returned early and its output is invalid. */
 mxfp4_status mxfp4_device_status(mxfp4_stream_t stream);
 
 /* Bounded-wait limit in nanoseconds for kernels launched afterwards by this host

@@ -38,7 +38,7 @@ namespace {
 #define MXG_PAIR 1
 #endif
 #ifndef MXG_PAIR_STAGES
-#define MXG_PAIR_STAGES 5
+#define MXG_PAIR_STAGES 6
 #endif
 
 // Tuning knob (compile-time): pipeline depth of the 256-wide tiles.
@@ -402,8 +402,11 @@ struct PairCfg {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
     static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 3) * 8;
-    static constexpr int OFF_STG = (OFF_TMEM + 16 + STG_ALIGN - 1) / STG_ALIGN * STG_ALIGN;
-    static constexpr int SMEM = OFF_STG + EPI_WARPS * STG_WARP_BYTES + 1024;
+    // The 64-byte-swizzled staging tiles repeat every 512 bytes.  No alignment slack:
+    // the kernel checks that dynamic shared memory starts on a 1024-byte boundary.
+    static constexpr int PAIR_STG_ALIGN = MXG_TMA_STORE ? 512 : STG_ALIGN;
+    static constexpr int OFF_STG = (OFF_TMEM + 16 + PAIR_STG_ALIGN - 1) / PAIR_STG_ALIGN * PAIR_STG_ALIGN;
+    static constexpr int SMEM = OFF_STG + EPI_WARPS * STG_WARP_BYTES;
     static constexpr uint32_t TX_PAIR = 2 * (A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE);
     static constexpr int SF_COLS = 24;  // TMEM columns of scales per stage: 8 for A, 16 for B
     static constexpr int TMEM_USED = 256 + STAGES * SF_COLS;
@@ -418,7 +421,13 @@ template <int STAGES>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
     using Cfg = PairCfg<STAGES>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // The layout has no slack for aligning the 128-byte-swizzled operand tiles.  Both
+    // CTAs see the same base, so both return here, before any cluster barrier.
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(p.status, kStatusSmemLayout);
+        return;
+    }
+    uint8_t* smem = smem_raw;
     uint8_t* sA = smem + Cfg::OFF_A;
     uint8_t* sB = smem + Cfg::OFF_B;
     uint8_t* sSFA = smem + Cfg::OFF_SFA;

@@ -290,6 +290,9 @@ mxfp4_status mxfp4_device_status(mxfp4_stream_t stream) {
     e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
     if (e != cudaSuccess) return cuda_fail(e, "clear status word");
     if (word & kStatusTimeout) return fail(MXFP4_ERR_TIMEOUT, "a bounded device wait expired (status 0x%x)", word);
+    if (word & kStatusSmemLayout)
+        return fail(MXFP4_ERR_CUDA, "a kernel's shared memory was not 1024-byte aligned; it returned early (status 0x%x)",
+                    word);
     return ok();
 }
 

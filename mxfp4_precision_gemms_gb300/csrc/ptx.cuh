@@ -11,6 +11,9 @@ namespace mx {
 
 // Status bits OR-ed into the device status word.
 constexpr uint32_t kStatusTimeout = 1u;
+// A kernel found its dynamic shared memory misaligned for its layout and returned
+// without touching memory.
+constexpr uint32_t kStatusSmemLayout = 2u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
