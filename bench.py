@@ -99,7 +99,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "25"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -361,7 +361,12 @@ def gpu_arm(args, rank, world, dist):
     torch.cuda.synchronize()
     assert mx.device_status() == 0, "device status after warm-up"
 
-    # ---- timed region: K steps, L2 flushed before each, device-timed with events
+    # ---- timed region: K steps, L2 flushed before each, device-timed with events around
+    # each step; the kernels of a step run back to back (a GEMM starts its set-up while
+    # the previous kernel drains).  Then, for the per-kernel rooflines, the same K steps
+    # again with an event pair around every launch: an event between two kernels keeps
+    # them from overlapping, so that pass gives each kernel's own duration and is kept
+    # out of the step's time.  Clocks are sampled through both passes.
     step_ev, kern_ev = [], []
     barrier(dist)
     torch.cuda.synchronize()
@@ -370,9 +375,14 @@ def gpu_arm(args, rank, world, dist):
             flush.fill_(1.0)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            run_step(layers, kern_ev)
+            run_step(layers)
             b.record()
             step_ev.append((a, b))
+        torch.cuda.synchronize()
+        barrier(dist)
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            run_step(layers, kern_ev)
         torch.cuda.synchronize()
     barrier(dist)
     status = mx.device_status()
@@ -380,8 +390,6 @@ def gpu_arm(args, rank, world, dist):
     fl = flops_per_step()
     value, ms_per_step = job_throughput(sum(step_ms), fl, args.steps, world, dist, dev)
     value /= 1e12
-
-    # ---- per-kernel rooflines from the events of the timed region
     agg = {}
     for kind, a, b, work in kern_ev:
         d = agg.setdefault(kind, [0.0, 0.0, 0])

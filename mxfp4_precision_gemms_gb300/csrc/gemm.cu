@@ -229,6 +229,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+#if MXF_PDL_GEMM
+    // The set-up above touches no global memory, so it overlaps the previous kernel.
+    grid_dependency_wait();
+    allow_dependent_launch();
+#endif
 
     if (warp == 0) {
         // ---------------- TMA producer
@@ -470,6 +475,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
     cluster_sync();  // both CTAs' barriers exist before either signals the other's
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+#if MXF_PDL_GEMM
+    // The set-up above touches no global memory, so it overlaps the previous kernel.
+    grid_dependency_wait();
+    allow_dependent_launch();
+#endif
 
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs)
@@ -634,8 +644,7 @@ cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int64_t tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
     const unsigned grid = (unsigned)(tiles < sm_count ? tiles : sm_count);
-    kern<<<grid, GEMM_THREADS, Cfg::SMEM, s>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(kern, dim3(grid), dim3(GEMM_THREADS), Cfg::SMEM, s, 1, MXF_PDL_GEMM != 0, p);
 }
 
 
@@ -672,8 +681,8 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
     if (max_clusters < 1) return cudaErrorNotSupported;
     const int64_t tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
     const int64_t clusters = tiles < max_clusters ? tiles : max_clusters;
-    cfg.gridDim = dim3((unsigned)(2 * clusters));
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    return launch_overlapped(kern, dim3((unsigned)(2 * clusters)), dim3(GEMM_THREADS), Cfg::SMEM, s, 2,
+                             MXF_PDL_GEMM != 0, p);
 }
 
 }  // namespace

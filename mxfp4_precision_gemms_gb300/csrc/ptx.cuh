@@ -36,6 +36,16 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Programmatic dependent launch (griddepcontrol).  A kernel launched with programmatic
+// stream serialization may start while the previous kernel in its stream is finishing;
+// it must call grid_dependency_wait() before its first global-memory access, which
+// returns once the grids it depends on have completed and their writes are visible (at
+// once when the launch allowed no overlap).  allow_dependent_launch() lets the next
+// kernel start once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

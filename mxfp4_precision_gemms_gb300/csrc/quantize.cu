@@ -105,6 +105,12 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.y * TR;
     const int64_t col0 = (int64_t)blockIdx.x * TC;
+#if MXF_PDL_QUANT
+    grid_dependency_wait();  // x may come from the previous kernel in the stream
+#endif
+#if MXF_QUANT_TRIGGER
+    allow_dependent_launch();
+#endif
 
     // ---- two row segments owned by this thread: rows pr and pr + TR/2, columns 32*s ..
     const int s = t & 3, pr = t >> 2;
@@ -310,8 +316,7 @@ cudaError_t launch_one(const QuantParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     const dim3 grid((unsigned)((p.C + TC - 1) / TC), (unsigned)((p.R + TR - 1) / TR));
-    kern<<<grid, QTHREADS, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(kern, grid, dim3(QTHREADS), smem, s, 1, MXF_PDL_QUANT != 0, p);
 }
 
 // ---------------------------------------------------------------------------------
