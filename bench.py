@@ -360,6 +360,21 @@ def gpu_arm(args, rank, world, dist):
         run_step(layers)
     torch.cuda.synchronize()
     assert mx.device_status() == 0, "device status after warm-up"
+    # The step's 24 launches captured once as a CUDA graph (the library makes no host
+    # syncs or allocations inside a call) and replayed for the timed steps.
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            run_step(layers)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert mx.device_status() == 0, "device status after graph warm-up"
+    step = graph.replay if graph is not None else (lambda: run_step(layers))
 
     # ---- timed region: K steps, L2 flushed before each, device-timed with events around
     # each step; the kernels of a step run back to back (a GEMM starts its set-up while
@@ -375,7 +390,7 @@ def gpu_arm(args, rank, world, dist):
             flush.fill_(1.0)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            run_step(layers)
+            step()
             b.record()
             step_ev.append((a, b))
         torch.cuda.synchronize()
@@ -472,7 +487,9 @@ def gpu_arm(args, rank, world, dist):
         "data": "synthetic (seeded: X N(0,1)+1% channels x50, W N(0,0.02), dY N(0,1e-4)+2% tokens x20)",
         "config": {"workload": WORKLOAD, "tokens": T_TOKENS, "flops_per_step": fl,
                    "l2": "flushed (256 MB write) before every timed step; per-step events exclude the flush",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "launch": ("CUDA graph of the step's 24 launches, replayed" if graph is not None
+                              else "stream launches")},
         "roofline": dominant,
         "kernels": {"gemm": {**roof_gemm, "launches": g_n, "ms_total": round(g_ms, 3), "share": round(gemm_share, 3)},
                     "quant": {**roof_quant, "launches": q_n, "ms_total": round(q_ms, 3),
@@ -788,6 +805,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time the step as stream launches, not a CUDA graph")
     ap.add_argument("--skip-fixes", action="store_true", help="skip the OF / MBS quantiser measurement")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-fp8", action="store_true", help="skip the FP8 (torch._scaled_mm) comparator")

@@ -112,3 +112,51 @@ def test_wgrad_stress_sampled(torch, had):
     r, c = sample_pairs(N, K, 48, 7, edge=2)
     want, S = oracle.wgrad_sample(dY, X, ORACLE_HAD[had], 0, r, c)
     assert_within(dw[r, c].double().cpu().numpy(), want, S, what=f"wgrad T=32768 had={had}")
+
+
+def test_cuda_graph_replay_matches_eager(torch):
+    """Every launch of the linear-layer API can be held in a CUDA graph: no host syncs,
+    no allocations once buffers exist, per-device launch settings cached on first use.
+    Fprop, Dgrad and Wgrad captured once and replayed twice (ragged M, the CTA-pair GEMM
+    and the single-CTA one) give the same bytes as eager calls."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    M, N, K = 640, 384, 128  # Dgrad and Wgrad outputs 128 wide: the single-CTA GEMM
+    X, W, dY = synth.linear_inputs(M, N, K, 21)
+    x, w, dy = (mx.bf16_tensor(a) for a in (X, W, dY))
+    cfg = mx.Config(had=16, mode=0, out_dtype=mx.OUT_BF16)
+    wcfg = mx.Config(had=16, mode=0, out_dtype=mx.OUT_F32)
+    ws = mx.Workspace()
+
+    def buffers():
+        return {"y": torch.empty((M, N), dtype=torch.bfloat16, device="cuda"),
+                "dx": torch.empty((M, K), dtype=torch.bfloat16, device="cuda"),
+                "dw": torch.empty((N, K), dtype=torch.float32, device="cuda"),
+                "xT": mx.empty_qtensor(K, M, mx.LAYOUT_COLT, mx.SF_MMA),
+                "wT": mx.empty_qtensor(K, N, mx.LAYOUT_COLT, mx.SF_MMA),
+                "dyT": mx.empty_qtensor(N, M, mx.LAYOUT_COLT, mx.SF_MMA)}
+
+    def step(b):
+        mx.linear_fprop(x, w, cfg, y=b["y"], xT=b["xT"], wT=b["wT"], ws=ws)
+        mx.linear_dgrad(dy, b["wT"], cfg, dx=b["dx"], dyT=b["dyT"], ws=ws)
+        mx.linear_wgrad(b["dyT"], b["xT"], wcfg, dw=b["dw"])
+
+    eager, cap = buffers(), buffers()
+    step(eager)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step(cap)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for k in ("y", "dx", "dw"):
+            cap[k].zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    for k in ("y", "dx", "dw"):
+        assert torch.equal(eager[k], cap[k]), k
+    for k in ("xT", "wT", "dyT"):
+        assert torch.equal(eager[k].codes, cap[k].codes) and torch.equal(eager[k].scales, cap[k].scales), k
