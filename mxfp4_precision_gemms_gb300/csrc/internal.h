@@ -34,15 +34,6 @@ struct QuantParams {
 };
 
 
-// Persistent TMA-fed quantiser: the parameters plus the input's tensor map.
-struct QuantTmaParams {
-    QuantParams p;
-    CUtensorMap map_x;  // bf16 input, box 64 columns x TR rows, 128-byte swizzle
-    int64_t tiles_c, tiles;
-    uint32_t* status;
-    uint64_t wait_ns;
-};
-
 // Launches the fused rotate+quantise kernel for the requested layouts.
 cudaError_t launch_rotate_quantize(const QuantParams& p, int had, unsigned layouts, cudaStream_t s);
 // Quantiser fixes (row layout): OF writes Q(v) to p.row and Q(v - dq(Q(v))) to q2;
@@ -164,9 +155,7 @@ uint32_t* device_status_ptr();  // for the current device
 // Records the thread-local message returned by mxfp4_last_error() and returns st.
 mxfp4_status record_error(mxfp4_status st, const char* fmt, ...);
 bool encode_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t cols, uint32_t box_rows);
-bool encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows);
 bool encode_out_map(CUtensorMap* map, void* c, int64_t rows, int64_t cols, int64_t ldc, bool bf16);
 bool encode_sf_map(CUtensorMap* map, const void* scales, int64_t rows, int64_t cols);
-uint64_t quant_wait_ns();  // bounded-wait limit of the calling host thread
 
 }  // namespace mx

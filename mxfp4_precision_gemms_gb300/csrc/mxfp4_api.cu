@@ -134,22 +134,6 @@ bool encode_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2D tensor map over a bf16 matrix [rows, cols] (leading dimension ld elements): box
-// = 64 columns (128 bytes) x box_rows rows, 128-byte swizzle, zero fill out of bounds.
-bool encode_bf16_map(CUtensorMap* map, const void* x, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows) {
-    EncodeTiledFn f = encode_fn();
-    if (!f) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(x), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-uint64_t quant_wait_ns() { return wait_limit(); }
-
 // 2D tensor map over the GEMM output C [rows, cols] (bf16 or fp32, leading dimension
 // ldc elements): box = 64 bytes of a row x 32 rows, 64-byte swizzle.
 bool encode_out_map(CUtensorMap* map, void* c, int64_t rows, int64_t cols, int64_t ldc, bool bf16) {

@@ -58,14 +58,6 @@ static_assert(TR == 32 || TR == 64 || TR == 128, "tile rows");
 #endif
 static_assert(!MXQ_COALESCE || MXQ_ROWS == 64, "the transposed-copy staging is laid out for 64-row tiles");
 
-// 1: persistent TMA-fed kernel (rq_tma_kernel); 0: one tile per CTA (rq_kernel).
-#ifndef MXQ_TMA
-#define MXQ_TMA 0
-#endif
-#ifndef MXQ_STAGES
-#define MXQ_STAGES 3
-#endif
-
 // Staged tile, fp32: float index of 16-byte chunk c (0..31) of row r, stored at
 // c ^ (r % 8).  Row-wise float4 writes (8 rows x 4 segments per warp) and column-wise
 // float2 reads (32 column pairs of one row per warp) are both bank-conflict free.
@@ -319,194 +311,6 @@ cudaError_t launch_one(const QuantParams& p, cudaStream_t s) {
     return launch_overlapped(kern, grid, dim3(QTHREADS), smem, s, 1, MXF_PDL_QUANT != 0, p);
 }
 
-// ---------------------------------------------------------------------------------
-// Persistent TMA-fed variant.  CTAs (QBLOCKS_PER_SM per SM) walk TR x 128 tiles; thread
-// 0 keeps the next Q_STAGES - 1 tiles of its CTA in flight as two 64-column TMA boxes
-// each (128-byte swizzle), so no thread waits on a global load it has just issued.
-// The row work and the column work both read the staged tile, with the same
-// arithmetic as rq_kernel.
-constexpr int Q_STAGES = MXQ_STAGES;
-constexpr int Q_TILE_BYTES = TR * TC * 2;
-constexpr int Q_BOX_BYTES = Q_TILE_BYTES / 2;  // 64 columns
-constexpr int Q_OFF_BAR = Q_STAGES * Q_TILE_BYTES;
-constexpr int Q_OFF_AMAX = Q_OFF_BAR + 8 * Q_STAGES;
-[[maybe_unused]] constexpr int Q_TMA_SMEM = Q_OFF_AMAX + TR * 4 * 4 + 1024;  // + alignment slack
-static_assert(Q_TILE_BYTES % 1024 == 0 && Q_BOX_BYTES % 1024 == 0, "128-byte swizzle atoms");
-
-// 32-bit word index of 16-byte chunk c (0..15) of tile row r in a stage: columns 0-63
-// are box 0, 64-127 box 1; within a box row r is 128 B with chunk c at (c % 8) ^ (r % 8).
-// Row-wise 16-byte reads (8 rows x 4 segments per warp) and column-wise 32-bit reads
-// (32 column pairs of one row per warp) are both bank-conflict free.
-[[maybe_unused]] __device__ __forceinline__ int stage_word(int r, int c) {
-    return ((c >> 3) * Q_BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4)) >> 2;
-}
-
-template <int HAD, bool ROW, bool COLT, bool TWOD>
-__global__ void __launch_bounds__(QTHREADS, QBLOCKS_PER_SM) rq_tma_kernel(const __grid_constant__ QuantTmaParams P) {
-    const QuantParams& p = P.p;
-    extern __shared__ uint8_t q_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Q_OFF_BAR);
-    float* seg_amax = reinterpret_cast<float*>(smem + Q_OFF_AMAX);
-    const int t = threadIdx.x;
-
-    auto issue = [&](uint32_t j) {  // tile j of this CTA's sequence -> stage j % Q_STAGES
-        const int64_t tile = blockIdx.x + (int64_t)j * gridDim.x;
-        if (tile >= P.tiles) return;
-        const int st = (int)(j % Q_STAGES);
-        const int32_t row0 = (int32_t)((tile / P.tiles_c) * TR), col0 = (int32_t)((tile % P.tiles_c) * TC);
-        mbar_arrive_expect_tx(&full[st], Q_TILE_BYTES);
-        uint8_t* dst = smem + st * Q_TILE_BYTES;
-        tma_load_2d(dst, &P.map_x, &full[st], col0, row0);
-        tma_load_2d(dst + Q_BOX_BYTES, &P.map_x, &full[st], col0 + 64, row0);
-    };
-
-    if (t == 0) {
-        for (int st = 0; st < Q_STAGES; ++st) mbar_init(&full[st], 1);
-        fence_mbar_init();
-        prefetch_tmap(&P.map_x);
-        for (uint32_t j = 0; j + 1 < Q_STAGES; ++j) issue(j);
-    }
-    __syncthreads();
-
-    uint32_t i = 0;
-    for (int64_t tile = blockIdx.x; tile < P.tiles; tile += gridDim.x, ++i) {
-        // The stage refilled here held tile i - 1, released by the __syncthreads that
-        // ended the previous iteration.
-        if (t == 0) issue(i + Q_STAGES - 1);
-        const int st = (int)(i % Q_STAGES);
-        const bool landed = wait_bounded(&full[st], (i / Q_STAGES) & 1u, P.wait_ns, P.status);
-        const uint32_t* buf = reinterpret_cast<const uint32_t*>(smem + st * Q_TILE_BYTES);
-        const int64_t row0 = (tile / P.tiles_c) * TR, col0 = (tile % P.tiles_c) * TC;
-
-        if constexpr (ROW || TWOD) {
-            const int s = t & 3, pr = t >> 2;
-            const int rx = pr, ry = pr + TR / 2;
-            const int64_t gc = col0 + 32 * s;
-            const int64_t grx = row0 + rx, gry = row0 + ry;
-            const bool vx = landed && grx < p.R && gc < p.C, vy = landed && gry < p.R && gc < p.C;
-            float2 v[32];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 a4 = *reinterpret_cast<const uint4*>(&buf[stage_word(rx, 4 * s + j)]);
-                const uint4 b4 = *reinterpret_cast<const uint4*>(&buf[stage_word(ry, 4 * s + j)]);
-                const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
-                const uint32_t b[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    v[8 * j + 2 * k] = make_float2(__uint_as_float(a[k] << 16), __uint_as_float(b[k] << 16));
-                    v[8 * j + 2 * k + 1] =
-                        make_float2(__uint_as_float(a[k] & 0xFFFF0000u), __uint_as_float(b[k] & 0xFFFF0000u));
-                }
-            }
-            rotate32x2<HAD>(v);
-            float ax, ay;
-            amax32x2<HAD>(v, ax, ay);
-            if constexpr (TWOD) {
-                seg_amax[rx * 4 + s] = ax;
-                seg_amax[ry * 4 + s] = ay;
-                __syncthreads();
-                float tx = 0.0f, ty = 0.0f;
-                const int bx = rx & ~31, by = ry & ~31;
-#pragma unroll 8
-                for (int k = 0; k < 32; ++k) {
-                    tx = fmaxf(tx, seg_amax[(bx + k) * 4 + s]);
-                    ty = fmaxf(ty, seg_amax[(by + k) * 4 + s]);
-                }
-                const uint32_t bytex = scale_byte(tx, p.mode), bytey = scale_byte(ty, p.mode);
-                uint4 qx, qy;
-                quant32x2<HAD>(v, bytex, bytey, qx, qy);
-                if (vx) {
-                    *reinterpret_cast<uint4*>(p.twoD.codes + grx * (p.C / 2) + gc / 2) = qx;
-                    if ((rx & 31) == 0) p.twoD.scales[(grx / 32) * (p.C / 32) + gc / 32] = (uint8_t)bytex;
-                }
-                if (vy) {
-                    *reinterpret_cast<uint4*>(p.twoD.codes + gry * (p.C / 2) + gc / 2) = qy;
-                    if ((ry & 31) == 0) p.twoD.scales[(gry / 32) * (p.C / 32) + gc / 32] = (uint8_t)bytey;
-                }
-            } else {
-                const uint32_t bytex = scale_byte(ax, p.mode), bytey = scale_byte(ay, p.mode);
-                uint4 qx, qy;
-                quant32x2<HAD>(v, bytex, bytey, qx, qy);
-                if (vx) {
-                    *reinterpret_cast<uint4*>(p.row.codes + grx * (p.C / 2) + gc / 2) = qx;
-                    store_scale(p.row, grx, gc / 32, p.C / 32, bytex);
-                }
-                if (vy) {
-                    *reinterpret_cast<uint4*>(p.row.codes + gry * (p.C / 2) + gc / 2) = qy;
-                    store_scale(p.row, gry, gc / 32, p.C / 32, bytey);
-                }
-            }
-        }
-
-        if constexpr (COLT) {
-            const int cp = t & 63, rb = t >> 6;
-            const int64_t gcol = col0 + 2 * cp, grow = row0 + 32 * rb;
-            if (landed && gcol < p.C && grow < p.R) {
-                float2 v[32];
-                const int chunk = cp >> 2, wi = cp & 3;  // 16-byte chunk holding columns 2cp, 2cp + 1
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const uint32_t w = buf[stage_word(32 * rb + k, chunk) + wi];
-                    v[k] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-                }
-                rotate32x2<HAD>(v);
-                float ax, ay;
-                amax32x2<HAD>(v, ax, ay);
-                const uint32_t bytex = scale_byte(ax, p.mode), bytey = scale_byte(ay, p.mode);
-                uint4 qx, qy;
-                quant32x2<HAD>(v, bytex, bytey, qx, qy);
-                *reinterpret_cast<uint4*>(p.colT.codes + gcol * (p.R / 2) + grow / 2) = qx;
-                *reinterpret_cast<uint4*>(p.colT.codes + (gcol + 1) * (p.R / 2) + grow / 2) = qy;
-                store_scale(p.colT, gcol, grow / 32, p.R / 32, bytex);
-                store_scale(p.colT, gcol + 1, grow / 32, p.R / 32, bytey);
-            }
-        }
-        __syncthreads();  // every thread is done with this stage (and with seg_amax)
-    }
-    // Every copy this CTA issued targets a tile the loop above waited for, so nothing
-    // is in flight at exit.
-}
-
-template <int HAD, bool ROW, bool COLT, bool TWOD>
-cudaError_t launch_tma_one(const QuantTmaParams& P, cudaStream_t st) {
-    auto kern = rq_tma_kernel<HAD, ROW, COLT, TWOD>;
-    static DeviceSlots grid_slots;
-    int grid_max = 0;
-    const cudaError_t e = per_device_setting(grid_slots, &grid_max, [&](int dev, int* g) {
-        cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_TMA_SMEM);
-        if (r != cudaSuccess) return r;
-        int sms = 0, per_sm = 0;
-        r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (r != cudaSuccess) return r;
-        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, QTHREADS, Q_TMA_SMEM);
-        if (r != cudaSuccess) return r;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        *g = sms * per_sm;
-        return cudaSuccess;
-    });
-    if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(P.tiles < grid_max ? P.tiles : grid_max);
-    kern<<<grid, QTHREADS, Q_TMA_SMEM, st>>>(P);
-    return cudaGetLastError();
-}
-
-template <int HAD>
-cudaError_t launch_had_tma(const QuantTmaParams& P, unsigned layouts, cudaStream_t s) {
-    switch (layouts) {
-        case MXFP4_LAYOUT_ROW:
-            return launch_tma_one<HAD, true, false, false>(P, s);
-        case MXFP4_LAYOUT_COLT:
-            return launch_tma_one<HAD, false, true, false>(P, s);
-        case MXFP4_LAYOUT_ROW | MXFP4_LAYOUT_COLT:
-            return launch_tma_one<HAD, true, true, false>(P, s);
-        case MXFP4_LAYOUT_2D:
-            return launch_tma_one<HAD, false, false, true>(P, s);
-        default:
-            return cudaErrorInvalidValue;
-    }
-}
-
 template <int HAD>
 cudaError_t launch_had(const QuantParams& p, unsigned layouts, cudaStream_t s) {
     switch (layouts) {
@@ -526,25 +330,6 @@ cudaError_t launch_had(const QuantParams& p, unsigned layouts, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_rotate_quantize(const QuantParams& p, int had, unsigned layouts, cudaStream_t s) {
-#if MXQ_TMA
-    QuantTmaParams P{};
-    P.p = p;
-    if (!encode_bf16_map(&P.map_x, p.x, p.R, p.C, p.ld, TR)) return cudaErrorInvalidValue;
-    P.tiles_c = (p.C + TC - 1) / TC;
-    P.tiles = P.tiles_c * ((p.R + TR - 1) / TR);
-    P.status = device_status_ptr();
-    P.wait_ns = quant_wait_ns();
-    switch (had) {
-        case 0:
-            return launch_had_tma<1>(P, layouts, s);
-        case 16:
-            return launch_had_tma<16>(P, layouts, s);
-        case 32:
-            return launch_had_tma<32>(P, layouts, s);
-        default:
-            return cudaErrorInvalidValue;
-    }
-#else
     switch (had) {
         case 0:
             return launch_had<1>(p, layouts, s);
@@ -555,7 +340,6 @@ cudaError_t launch_rotate_quantize(const QuantParams& p, int had, unsigned layou
         default:
             return cudaErrorInvalidValue;
     }
-#endif
 }
 
 }  // namespace mx
