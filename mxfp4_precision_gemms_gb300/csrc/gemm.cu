@@ -27,12 +27,6 @@
 namespace mx {
 namespace {
 
-// 1: the epilogue writes C with TMA tile stores from a swizzled staging buffer;
-// 0: coalesced st.global from a padded staging buffer.
-#ifndef MXG_TMA_STORE
-#define MXG_TMA_STORE 1
-#endif
-
 // 1: problems with M > 128 and N > 128 use the CTA-pair kernel (256 x 256 tiles).
 #ifndef MXG_PAIR
 #define MXG_PAIR 1
@@ -50,13 +44,8 @@ constexpr int BM = 128;
 constexpr int BK_BYTES = 128;  // 256 E2M1 elements per stage
 constexpr int EPI_WARPS = 8;  // two per TMEM lane quadrant, each owning half the columns
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
-#if MXG_TMA_STORE
 constexpr int STG_PITCH = 64;                      // 32 rows x 64 B, 64-byte swizzle (TMA store box)
 constexpr int STG_ALIGN = 1024;
-#else
-constexpr int STG_PITCH = 80;                      // bytes per staged row: 64 B of data + 16 B pad
-constexpr int STG_ALIGN = 128;
-#endif
 constexpr int STG_WARP_BYTES = 32 * STG_PITCH;     // one warp's staging: 32 rows x 64 B
 
 template <int BN, int STAGES, int ACC>
@@ -84,67 +73,6 @@ struct GemmCfg {
     static_assert(OFF_STG % 16 == 0 && STG_PITCH % 16 == 0, "staging rows are accessed as 16-byte vectors");
     static_assert(OFF_BAR % 8 == 0 && OFF_A % 1024 == 0 && OFF_B % 1024 == 0, "barrier / swizzle-atom alignment");
 };
-
-// Writes 64 bytes per row for the 32 rows of one epilogue warp (lane i holds row
-// row_base + i): the rows are staged in shared memory and written back with four
-// lanes per row, so each store instruction covers 8 rows x 64 contiguous bytes
-// instead of 32 scattered 16-byte pieces.  esz is the output element size (2 or 4).
-__device__ __forceinline__ void stage_and_store(const GemmParams& p, uint8_t* stg, int lane, int64_t row_base,
-                                                int64_t col0, const uint32_t* w, int esz) {
-    __syncwarp();
-    uint4* mine = reinterpret_cast<uint4*>(stg + lane * STG_PITCH);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) mine[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-    __syncwarp();
-    const int epc = 16 / esz;  // elements per 16-byte piece
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int r = it * 8 + (lane >> 2), c = lane & 3;
-        const int64_t grow = row_base + r;
-        const int64_t gcol = col0 + c * epc;
-        if (grow >= p.M || gcol >= p.N) continue;
-        const uint4 val = *reinterpret_cast<const uint4*>(stg + r * STG_PITCH + c * 16);
-        uint8_t* dst = reinterpret_cast<uint8_t*>(p.C) + (grow * p.ldc + gcol) * esz;
-        if (gcol + epc <= p.N) {
-            if (p.accumulate) {  // fp32 only
-                const float4 o = *reinterpret_cast<const float4*>(dst);
-                *reinterpret_cast<float4*>(dst) =
-                    make_float4(o.x + __uint_as_float(val.x), o.y + __uint_as_float(val.y),
-                                o.z + __uint_as_float(val.z), o.w + __uint_as_float(val.w));
-            } else {
-                *reinterpret_cast<uint4*>(dst) = val;
-            }
-        } else {
-            const uint32_t vw[4] = {val.x, val.y, val.z, val.w};
-            for (int e = 0; e < p.N - gcol; ++e) {
-                if (esz == 4) {
-                    float* d = reinterpret_cast<float*>(dst) + e;
-                    *d = (p.accumulate ? *d : 0.0f) + __uint_as_float(vw[e]);
-                } else {
-                    const uint32_t hw = (vw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-                    reinterpret_cast<uint16_t*>(dst)[e] = (uint16_t)hw;
-                }
-            }
-        }
-    }
-}
-
-// One TMEM chunk (32 fp32 columns of this lane's row) -> bf16 or fp32 global output.
-[[maybe_unused]] __device__ __forceinline__ void store_chunk(const GemmParams& p, uint8_t* stg, int lane, int64_t row_base,
-                                           int64_t col0, const uint32_t (&v)[32]) {
-    if (p.out_bf16) {
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            w[j] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        stage_and_store(p, stg, lane, row_base, col0, w, 2);
-    } else {
-        stage_and_store(p, stg, lane, row_base, col0, v, 4);
-        stage_and_store(p, stg, lane, row_base, col0 + 16, v + 16, 4);
-    }
-}
 
 // TMA-store epilogue: lane i writes its row's 64 bytes into the warp's staging tile
 // (64-byte swizzle: 16-byte chunk j of row r at j ^ ((r >> 1) & 3), conflict-free),
@@ -354,17 +282,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_kernel(const __grid
             if (lane == 0) mbar_arrive(&acc_empty[ab]);
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
-#if MXG_TMA_STORE
                 store_chunk_tma(p, stg, lane, row_base, c0 + c * 32, v[c]);
-#else
-                store_chunk(p, stg, lane, row_base, c0 + c * 32, v[c]);
-#endif
             }
         }
-#if MXG_TMA_STORE
         if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
         __syncwarp();
-#endif
     }
 
     tc_fence_before();
@@ -409,7 +331,7 @@ struct PairCfg {
     static constexpr int OFF_TMEM = OFF_BAR + (2 * STAGES + 3) * 8;
     // The 64-byte-swizzled staging tiles repeat every 512 bytes.  No alignment slack:
     // the kernel checks that dynamic shared memory starts on a 1024-byte boundary.
-    static constexpr int PAIR_STG_ALIGN = MXG_TMA_STORE ? 512 : STG_ALIGN;
+    static constexpr int PAIR_STG_ALIGN = 512;
     static constexpr int OFF_STG = (OFF_TMEM + 16 + PAIR_STG_ALIGN - 1) / PAIR_STG_ALIGN * PAIR_STG_ALIGN;
     static constexpr int SMEM = OFF_STG + EPI_WARPS * STG_WARP_BYTES;
     static constexpr uint32_t TX_PAIR = 2 * (A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE);
@@ -609,17 +531,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
             if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-#if MXG_TMA_STORE
                 store_chunk_tma(p, stg, lane, row_base, c0 + c * 32, v[c]);
-#else
-                store_chunk(p, stg, lane, row_base, c0 + c * 32, v[c]);
-#endif
             }
         }
-#if MXG_TMA_STORE
         if (lane == 0) bulk_wait_all();
         __syncwarp();
-#endif
     }
 
     tc_fence_before();
