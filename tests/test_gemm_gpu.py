@@ -120,3 +120,26 @@ def test_many_tiles_narrow_n(torch):
     want, S = oracle.gemm(*qa, *qb)
     assert_within(run(torch, qa, qb), want, S, what="many tiles, N=96")
     assert_within(run(torch, qa, qb, out_dtype=1), want, S, bf16=True, what="many tiles, N=96, bf16")
+
+
+def test_back_to_back_accumulate_chain(torch):
+    """GEMMs overlap the previous kernel's drain (programmatic dependent launch) and wait
+    for it before touching memory: C = A1 B1^T, then C += A2 B2^T launched right after
+    on the same stream (CTA-pair tiles), must equal the sum of the two products."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    M, N, K = 1024, 768, 512
+    qa1, qb1 = oracle_operands(M, N, K, 15)
+    qa2, qb2 = oracle_operands(M, N, K, 16)
+    w1, S1 = oracle.gemm(*qa1, *qb1)
+    w2, S2 = oracle.gemm(*qa2, *qb2)
+    A1, B1, A2, B2 = (mx.qtensor_from_host(*q) for q in (qa1, qb1, qa2, qb2))
+    C = mx.gemm(A1, B1, out_dtype=mx.OUT_F32)
+    for _ in range(3):  # the accumulating launches follow one another with no sync between
+        C = mx.gemm(A2, B2, out_dtype=mx.OUT_F32, accumulate=True, out=C)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    got = C.double().cpu().numpy()
+    # each fp32 add of the running value rounds once more: allow 2^-22 of the magnitudes
+    assert_within(got, w1 + 3 * w2, S1 + 3 * S2 + 2.4e-7 * (np.abs(w1) + 3 * np.abs(w2)) / 1e-5,
+                  what="accumulate chain")
