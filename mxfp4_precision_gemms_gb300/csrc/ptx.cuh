@@ -292,10 +292,11 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 
 // ------------------------------------------------------------------ conversions
 // Eight fp32 -> eight E2M1 codes packed in 32 bits (value i in nibble i), round to
-// nearest even, saturating.
+// nearest even, saturating.  A pure conversion (no side effects), so not volatile: the
+// compiler may schedule it among the surrounding arithmetic.
 __device__ __forceinline__ uint32_t cvt_e2m1x8(const float* v) {
     uint32_t out;
-    asm volatile(
+    asm(
         "{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
         "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
         "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
