@@ -75,6 +75,13 @@ __device__ __forceinline__ void st_global_32B(void* dst, uint4 a, uint4 b) {
                  : "memory");
 }
 
+// One 32-byte streaming global load (the address must be 32-byte aligned).
+__device__ __forceinline__ void ld_global_cs_32B(const void* src, uint4& a, uint4& b) {
+    asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(src));
+}
+
 // Staging of the transposed codes: 16-byte chunk (column pair cp, row block rb, column
 // h of the pair) at chunk 4 cp + ((2 rb + h) ^ ((cp >> 1) & 3)).  The column work's
 // writes (32 consecutive pairs, fixed rb and h) and the per-output-row reads (16 pairs,
@@ -115,15 +122,31 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
         uint4 raw_x[4], raw_y[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) raw_x[j] = raw_y[j] = make_uint4(0, 0, 0, 0);
+        // Row + transposed pass: 32-byte loads when every row segment starts on a 32-byte
+        // boundary, so that each load instruction uses whole 32-byte sectors (measured
+        // 5-20% faster on 8192 x {4096, 14336}).  The single-layout passes keep 16-byte
+        // loads: the row pass measured 13% slower with 32-byte ones, the transposed pass
+        // unchanged.
+        const bool a32 = (ROW && COLT) && ((reinterpret_cast<uintptr_t>(p.x) | (uintptr_t)(p.ld * 2)) & 31u) == 0;
         if (vx) {
             const uint4* src = reinterpret_cast<const uint4*>(p.x + grx * p.ld + gc);
+            if (a32) {
+                ld_global_cs_32B(src, raw_x[0], raw_x[1]);
+                ld_global_cs_32B(src + 2, raw_x[2], raw_x[3]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) raw_x[j] = __ldcs(src + j);
+                for (int j = 0; j < 4; ++j) raw_x[j] = __ldcs(src + j);
+            }
         }
         if (vy) {
             const uint4* src = reinterpret_cast<const uint4*>(p.x + gry * p.ld + gc);
+            if (a32) {
+                ld_global_cs_32B(src, raw_y[0], raw_y[1]);
+                ld_global_cs_32B(src + 2, raw_y[2], raw_y[3]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) raw_y[j] = __ldcs(src + j);
+                for (int j = 0; j < 4; ++j) raw_y[j] = __ldcs(src + j);
+            }
         }
         if constexpr (COLT && !STAGE_F32) {
 #pragma unroll
