@@ -194,12 +194,35 @@ class Layer:
         self.gemm_flops = 3 * 2 * M * N * K
 
 
-def run_step(layers, ev=None):
+def run_step(layers, ev=None, aux=None):
     """One pass of the hot path.  If `ev` is a list, CUDA events are recorded around
-    every kernel launch: ev gets (kind, start, end, work) tuples."""
+    every kernel launch: ev gets (kind, start, end, work) tuples.  If `aux` is a second
+    CUDA stream, each linear layer's independent launches run on two branches: the X
+    and W quantisations (both feed Fprop), then Dgrad and Wgrad (both need only the dY
+    quantisation and the saved transposed copies).  The layers stay in order: a layer
+    starts once both branches of the previous one have finished."""
     import torch
 
     from mxfp4_precision_gemms_gb300 import binding as mx
+
+    if aux is not None:
+        main = torch.cuda.current_stream()
+        RC = mx.LAYOUT_ROW | mx.LAYOUT_COLT
+        for L in layers:
+            M, N, K = T_TOKENS, L.N, L.K
+            aux.wait_stream(main)
+            mx.rotate_quantize(L.x, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.xq, "colT": L.xT})
+            with torch.cuda.stream(aux):
+                mx.rotate_quantize(L.w, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.wq, "colT": L.wT})
+            main.wait_stream(aux)
+            mx.gemm(L.xq, L.wq, mx.OUT_BF16, out=L.y)
+            mx.rotate_quantize(L.dy, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.dyq, "colT": L.dyT})
+            aux.wait_stream(main)
+            with torch.cuda.stream(aux):
+                mx.gemm(L.dyT, L.xT, mx.OUT_F32, out=L.dw)
+            mx.gemm(L.dyq, L.wT, mx.OUT_BF16, out=L.dx)
+            main.wait_stream(aux)
+        return
 
     def timed(kind, work, fn):
         if ev is None:
@@ -383,19 +406,21 @@ def gpu_arm(args, rank, world, dist):
     assert mx.device_status() == 0, "device status after warm-up"
     # The step's 24 launches captured once as a CUDA graph (the library makes no host
     # syncs or allocations inside a call) and replayed for the timed steps.
+    # Unless --serial-step, each linear's independent launches sit on two branches.
     graph = None
+    aux = None if args.serial_step else torch.cuda.Stream()
     if not args.no_graph:
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side):
-            run_step(layers)
+            run_step(layers, aux=aux)
         torch.cuda.synchronize()
         for _ in range(args.warmup):
             graph.replay()
         torch.cuda.synchronize()
         assert mx.device_status() == 0, "device status after graph warm-up"
-    step = graph.replay if graph is not None else (lambda: run_step(layers))
+    step = graph.replay if graph is not None else (lambda: run_step(layers, aux=aux))
 
     # ---- timed region: K steps, L2 flushed before each, device-timed with events around
     # each step; the kernels of a step run back to back (a GEMM starts its set-up while
@@ -509,8 +534,10 @@ def gpu_arm(args, rank, world, dist):
         "config": {"workload": WORKLOAD, "tokens": T_TOKENS, "flops_per_step": fl,
                    "l2": "flushed before every timed step (256 MB write, then a 256 MB read of another buffer); per-step events exclude the flush",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": ("CUDA graph of the step's 24 launches, replayed" if graph is not None
-                              else "stream launches")},
+                   "launch": (("CUDA graph of the step's 24 launches, replayed" if graph is not None
+                               else "stream launches")
+                              + ("" if aux is None else "; per linear, X and W quantisations on two branches "
+                                 "before Fprop, Dgrad and Wgrad on two branches after the dY quantisation"))},
         "roofline": dominant,
         "kernels": {"gemm": {**roof_gemm, "launches": g_n, "ms_total": round(g_ms, 3), "share": round(gemm_share, 3)},
                     "quant": {**roof_quant, "launches": q_n, "ms_total": round(q_ms, 3),
@@ -830,6 +857,8 @@ def main():
     ap.add_argument("--skip-fixes", action="store_true", help="skip the OF / MBS quantiser measurement")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-fp8", action="store_true", help="skip the FP8 (torch._scaled_mm) comparator")
+    ap.add_argument("--serial-step", action="store_true",
+                    help="launch the timed step's 24 kernels on one stream (default: two branches per linear)")
     ap.add_argument("--profile-case", action="store_true", help="run the small ncu case and exit")
     ap.add_argument("--traffic-from", metavar="CSV", help="turn an ncu CSV of dram bytes for this benchmark "
                     "into profiles/traffic_llama8b_linears_T8192.json and exit")
