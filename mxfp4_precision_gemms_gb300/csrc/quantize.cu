@@ -5,15 +5,17 @@
 //   Hadamard before quantisation), D (1x32 row, 32x1 column-transposed, 32x32 2D).
 // "Decomposing MXFP4 quantization error ...": E8M0 scales, E2M1 grid, ceiling scale.
 //
-// One CTA (2 threads per tile row) owns a TR x 128 tile of the bf16 input and reads it
+// One CTA of 128 threads (4 warps) owns a 64 x 128 tile of the bf16 input and reads it
 // from HBM once.
-//  - Row work: each thread owns two 32-element row segments (rows r and r + TR/2) in
+//  - Row work: each thread owns two 32-element row segments (rows r and r + 32) in
 //    registers and processes them in lockstep with packed f32x2 instructions:
 //    rotation butterfly, block amax, E8M0 byte, 2 x 32 codes -> two 16-byte stores.
-//  - Column work (transposed copy): the row work also leaves the tile in shared memory
-//    (fp32 or raw bf16, swizzled so that the row-wise writes and the column-wise reads
-//    are bank-conflict free); each thread then owns two adjacent columns of one 32-row
-//    block, one shared load per row giving both columns' values.
+//  - Column work (transposed copy): the load also leaves the raw bf16 tile in shared
+//    memory, swizzled so that the row-wise writes and the column-wise reads are
+//    bank-conflict free.  Each thread then owns two adjacent columns of one 32-row block
+//    (one 32-bit shared load per row gives both columns' values); a warp holds both row
+//    blocks of its 16 column pairs, so each output row's two 16-byte halves meet in one
+//    warp and leave, after one shuffle exchange, as one 32-byte store.
 //  - 2D work: row segments as above, the per-segment amax is combined over the 32
 //    rows of the block through shared memory.
 // Per element the kernel moves 2 B in and 0.53 B (single) or 1.06 B (row + column)
@@ -25,47 +27,20 @@
 namespace mx {
 namespace {
 
-// Tuning knobs (compile-time): tile rows (32, 64 or 128; 2 threads per tile row) and
-// the type the tile is staged in for the column work (1: fp32, 0: the raw bf16).
-// Measured on GB300 (dual copy, 8192 x 14336): 64 rows / bf16 3.63 TB/s, 64 / fp32
-// 2.81, 128 / bf16 3.31, 128 / fp32 2.72.
-#ifndef MXQ_ROWS
-#define MXQ_ROWS 64
-#endif
-#ifndef MXQ_STAGE_F32
-#define MXQ_STAGE_F32 0
-#endif
-constexpr int TR = MXQ_ROWS;  // tile rows
+constexpr int TR = 64;        // tile rows
 constexpr int TC = 128;       // tile cols
 constexpr int QTHREADS = 2 * TR;
-// Launch bound: CTAs per SM the register allocation must allow.  With 64-row tiles, 6
-// (80 registers, no spills) beats 4 (122 registers) by 7-9% on the dual pass; 7 and 8
-// spill.
-#ifndef MXQ_MINB
-#define MXQ_MINB (MXQ_ROWS == 64 ? 6 : 512 / (2 * MXQ_ROWS))
-#endif
-constexpr int QBLOCKS_PER_SM = MXQ_MINB;
-constexpr bool STAGE_F32 = MXQ_STAGE_F32 != 0;
-constexpr int TILE_BYTES = STAGE_F32 ? TR * TC * 4 : TR * TC * 2;
-static_assert(TR == 32 || TR == 64 || TR == 128, "tile rows");
+// Launch bound: CTAs per SM the register allocation must allow.  Six (80 registers, no
+// spills) beat four (122 registers) by 7-9% on the dual pass; seven and eight spill.
+constexpr int QBLOCKS_PER_SM = 6;
+constexpr int TILE_BYTES = TR * TC * 2;  // the raw bf16 tile
 
-// 1: the row copy's scale bytes (MMA order) leave as one 32-bit store per row, gathered
-// by warp shuffles, and the transposed copy's codes and scale bytes are staged in shared
-// memory so that each output row's piece leaves as one 32-byte (or two 16-byte) store
-// and one 16-bit scale store; 0: every thread stores its own 16-byte pieces and bytes.
-#ifndef MXQ_COALESCE
-#define MXQ_COALESCE 1
-#endif
-static_assert(!MXQ_COALESCE || MXQ_ROWS == 64, "the transposed-copy staging is laid out for 64-row tiles");
-
-// Staged tile, fp32: float index of 16-byte chunk c (0..31) of row r, stored at
-// c ^ (r % 8).  Row-wise float4 writes (8 rows x 4 segments per warp) and column-wise
-// float2 reads (32 column pairs of one row per warp) are both bank-conflict free.
-__device__ __forceinline__ int f32_chunk(int r, int c) { return r * TC + ((c ^ (r & 7)) << 2); }
-// Staged tile, bf16: 32-bit word index of 16-byte chunk q (0..15) of row r, with the
-// same property for row-wise uint4 writes and column-wise 32-bit reads.
+// Staged tile: 32-bit word index of 16-byte chunk q (0..15) of row r.  The XOR on the
+// chunk index (by q bits 2-3, row bit 0 and row bit 5) keeps the row-wise 16-byte writes
+// (8 rows x 4 segments per warp) and the column-wise 32-bit reads (rows i and 32 + i,
+// 16 column pairs each, per warp) bank-conflict free.
 __device__ __forceinline__ int bf16_chunk(int r, int q) {
-    return r * (TC / 2) + ((q ^ ((q >> 2) & 3) ^ ((r & 1) << 2)) << 2);
+    return r * (TC / 2) + ((q ^ ((q >> 2) & 3) ^ (((r ^ (r >> 5)) & 1) << 2)) << 2);
 }
 
 // One 32-byte global store (the address must be 32-byte aligned).
@@ -82,24 +57,11 @@ __device__ __forceinline__ void ld_global_cs_32B(const void* src, uint4& a, uint
                  : "l"(src));
 }
 
-// Staging of the transposed codes: 16-byte chunk (column pair cp, row block rb, column
-// h of the pair) at chunk 4 cp + ((2 rb + h) ^ ((cp >> 1) & 3)).  The column work's
-// writes (32 consecutive pairs, fixed rb and h) and the per-output-row reads (16 pairs,
-// both h) each spread over all eight 16-byte bank groups.
-__device__ __forceinline__ int colt_stage_chunk(int cp, int rb, int h) {
-    return 4 * cp + ((2 * rb + h) ^ ((cp >> 1) & 3));
-}
-
 template <int HAD, bool ROW, bool COLT, bool TWOD>
 __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel(const QuantParams p) {
     extern __shared__ __align__(16) uint8_t q_smem[];
-    float* tile_f = reinterpret_cast<float*>(q_smem);
     uint32_t* tile_w = reinterpret_cast<uint32_t*>(q_smem);
     float* seg_amax = reinterpret_cast<float*>(q_smem + (COLT ? TILE_BYTES : 0));
-    // transposed-copy staging (MXQ_COALESCE): codes of the tile's 128 output rows x 2
-    // row blocks (4 KB), then their scale bytes
-    [[maybe_unused]] uint8_t* colt_codes = q_smem + TILE_BYTES;
-    [[maybe_unused]] uint8_t* colt_scales = colt_codes + TC * (TR / 2);
 
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.y * TR;
@@ -148,7 +110,7 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
                 for (int j = 0; j < 4; ++j) raw_y[j] = __ldcs(src + j);
             }
         }
-        if constexpr (COLT && !STAGE_F32) {
+        if constexpr (COLT) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 *reinterpret_cast<uint4*>(&tile_w[bf16_chunk(rx, 4 * s + j)]) = raw_x[j];
@@ -167,16 +129,6 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
             }
         }
     }
-    if constexpr (COLT && STAGE_F32) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            *reinterpret_cast<float4*>(&tile_f[f32_chunk(rx, 8 * s + j)]) =
-                make_float4(v[4 * j].x, v[4 * j + 1].x, v[4 * j + 2].x, v[4 * j + 3].x);
-            *reinterpret_cast<float4*>(&tile_f[f32_chunk(ry, 8 * s + j)]) =
-                make_float4(v[4 * j].y, v[4 * j + 1].y, v[4 * j + 2].y, v[4 * j + 3].y);
-        }
-    }
-
     if constexpr (ROW || TWOD) {
         rotate32x2<HAD>(v);
         float ax, ay;
@@ -209,7 +161,6 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
             quant32x2<HAD>(v, bytex, bytey, qx, qy);
             if (vx) *reinterpret_cast<uint4*>(p.row.codes + grx * (p.C / 2) + gc / 2) = qx;
             if (vy) *reinterpret_cast<uint4*>(p.row.codes + gry * (p.C / 2) + gc / 2) = qy;
-#if MXQ_COALESCE
             // The four segments of a row are lanes 4 pr .. 4 pr + 3 and their four bytes are
             // consecutive (k = col0/32 + s, col0/32 a multiple of 4) in both scale orders.
             // MMA order: one 32-bit store, rows past R and columns past C carrying byte 0
@@ -234,75 +185,55 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
                 if (vx) store_scale(p.row, grx, gc / 32, p.C / 32, bytex);
                 if (vy) store_scale(p.row, gry, gc / 32, p.C / 32, bytey);
             }
-#else
-            if (vx) store_scale(p.row, grx, gc / 32, p.C / 32, bytex);
-            if (vy) store_scale(p.row, gry, gc / 32, p.C / 32, bytey);
-#endif
         }
     }
 
     if constexpr (COLT) {
         __syncthreads();
-        // two adjacent columns (2*cp, 2*cp + 1) x one 32-row block per thread
-        const int cp = t & 63, rb = t >> 6;
-        const int64_t gcol = col0 + 2 * cp, grow = row0 + 32 * rb;
-        if (gcol < p.C && grow < p.R) {
-            if constexpr (STAGE_F32) {
-                const int c = cp >> 1, half = (cp & 1) * 2;  // chunk holding columns 2cp, 2cp + 1
+        // Two adjacent columns (2 cp, 2 cp + 1) x one 32-row block per thread.  A warp
+        // holds both row blocks of 16 column pairs (lanes l and l ^ 16 share cp), so the
+        // two 16-byte halves of each output row meet in one warp: one shuffle exchange,
+        // then every lane writes one output row's 32 bytes and two scale bytes.
+        const int lane = t & 31;
+        const int rb = lane >> 4, cp = 16 * (t >> 5) + (lane & 15);
+        const int q = cp >> 2, wi = cp & 3;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    v[i] = *reinterpret_cast<const float2*>(&tile_f[f32_chunk(32 * rb + i, c) + half]);
-            } else {
-                const int q = cp >> 2, wi = cp & 3;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const uint32_t w = tile_w[bf16_chunk(32 * rb + i, q) + wi];
-                    v[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-                }
-            }
-            rotate32x2<HAD>(v);
-            float ax, ay;
-            amax32x2<HAD>(v, ax, ay);
-            const uint32_t bytex = scale_byte(ax, p.mode), bytey = scale_byte(ay, p.mode);
-            uint4 qx, qy;
-            quant32x2<HAD>(v, bytex, bytey, qx, qy);
-#if MXQ_COALESCE
-            uint4* cst = reinterpret_cast<uint4*>(colt_codes);
-            cst[colt_stage_chunk(cp, rb, 0)] = qx;
-            cst[colt_stage_chunk(cp, rb, 1)] = qy;
-            colt_scales[(2 * cp) * 2 + rb] = (uint8_t)bytex;
-            colt_scales[(2 * cp + 1) * 2 + rb] = (uint8_t)bytey;
-#else
-            *reinterpret_cast<uint4*>(p.colT.codes + gcol * (p.R / 2) + grow / 2) = qx;
-            *reinterpret_cast<uint4*>(p.colT.codes + (gcol + 1) * (p.R / 2) + grow / 2) = qy;
-            store_scale(p.colT, gcol, grow / 32, p.R / 32, bytex);
-            store_scale(p.colT, gcol + 1, grow / 32, p.R / 32, bytey);
-#endif
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t w = tile_w[bf16_chunk(32 * rb + i, q) + wi];
+            v[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
         }
-#if MXQ_COALESCE
-        __syncthreads();
-        // one thread per output row c: the tile's rows give it 16 bytes per valid 32-row block
-        for (int c = t; c < TC; c += QTHREADS) {
-            const int64_t orow = col0 + c;
-            const int64_t left = (p.R - row0) / 32;
-            const int nrb = left >= 2 ? 2 : (int)left;  // valid 32-row blocks of the tile
-            if (orow >= p.C || nrb <= 0) continue;
-            const uint4* cst = reinterpret_cast<const uint4*>(colt_codes);
-            const int cp = c >> 1, h = c & 1;
+        rotate32x2<HAD>(v);
+        float ax, ay;
+        amax32x2<HAD>(v, ax, ay);
+        const uint32_t bytex = scale_byte(ax, p.mode), bytey = scale_byte(ay, p.mode);
+        uint4 qx, qy;
+        quant32x2<HAD>(v, bytex, bytey, qx, qy);
+        // row block 0 keeps output row 2 cp (its qx) and takes block 1's qx; row block 1
+        // keeps output row 2 cp + 1 (its qy) and takes block 0's qy
+        const uint4 send = rb == 0 ? qy : qx;
+        uint4 recv;
+        recv.x = __shfl_xor_sync(0xffffffffu, send.x, 16);
+        recv.y = __shfl_xor_sync(0xffffffffu, send.y, 16);
+        recv.z = __shfl_xor_sync(0xffffffffu, send.z, 16);
+        recv.w = __shfl_xor_sync(0xffffffffu, send.w, 16);
+        const uint32_t recv_b = __shfl_xor_sync(0xffffffffu, rb == 0 ? bytey : bytex, 16);
+        const uint4 lo = rb == 0 ? qx : recv, hi = rb == 0 ? recv : qy;
+        const uint32_t b0 = rb == 0 ? bytex : recv_b, b1 = rb == 0 ? recv_b : bytey;
+        const int64_t orow = col0 + 2 * cp + rb;
+        const int64_t left = (p.R - row0) / 32;
+        const int nrb = left >= 2 ? 2 : (int)left;  // valid 32-row blocks of the tile
+        if (orow < p.C && nrb > 0) {
             uint8_t* dst = p.colT.codes + orow * (p.R / 2) + row0 / 2;
-            const uint4 a = cst[colt_stage_chunk(cp, 0, h)];
             if (nrb == 2) {
-                const uint4 b = cst[colt_stage_chunk(cp, 1, h)];
                 if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
-                    st_global_32B(dst, a, b);
+                    st_global_32B(dst, lo, hi);
                 } else {
-                    reinterpret_cast<uint4*>(dst)[0] = a;
-                    reinterpret_cast<uint4*>(dst)[1] = b;
+                    reinterpret_cast<uint4*>(dst)[0] = lo;
+                    reinterpret_cast<uint4*>(dst)[1] = hi;
                 }
             } else {
-                *reinterpret_cast<uint4*>(dst) = a;
+                *reinterpret_cast<uint4*>(dst) = lo;
             }
-            const uint8_t b0 = colt_scales[c * 2], b1 = colt_scales[c * 2 + 1];
             // k = row0/32 (even) and k + 1 are adjacent bytes in both scale orders
             const int64_t off = p.colT.sf_mma ? sf_mma_offset(orow, row0 / 32, p.colT.kb_pad)
                                               : orow * (p.R / 32) + row0 / 32;
@@ -313,14 +244,12 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
                 if (nrb == 2) store_scale(p.colT, orow, row0 / 32 + 1, p.R / 32, b1);
             }
         }
-#endif
     }
 }
 
 template <int HAD, bool ROW, bool COLT, bool TWOD>
 cudaError_t launch_one(const QuantParams& p, cudaStream_t s) {
-    constexpr int smem = (COLT ? TILE_BYTES + (MXQ_COALESCE ? TC * (TR / 2) + TC * (TR / 32) : 0) : 0) +
-                         (TWOD ? TR * 4 * 4 : 0);
+    constexpr int smem = (COLT ? TILE_BYTES : 0) + (TWOD ? TR * 4 * 4 : 0);
     auto kern = rq_kernel<HAD, ROW, COLT, TWOD>;
     if constexpr (smem > 48 * 1024) {
         static DeviceSlots opted_in;
