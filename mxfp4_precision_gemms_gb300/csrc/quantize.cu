@@ -84,12 +84,11 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
         uint4 raw_x[4], raw_y[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) raw_x[j] = raw_y[j] = make_uint4(0, 0, 0, 0);
-        // Row + transposed pass: 32-byte loads when every row segment starts on a 32-byte
-        // boundary, so that each load instruction uses whole 32-byte sectors (measured
-        // 5-20% faster on 8192 x {4096, 14336}).  The single-layout passes keep 16-byte
-        // loads: the row pass measured 13% slower with 32-byte ones, the transposed pass
-        // unchanged.
-        const bool a32 = (ROW && COLT) && ((reinterpret_cast<uintptr_t>(p.x) | (uintptr_t)(p.ld * 2)) & 31u) == 0;
+        // 32-byte loads when every row segment starts on a 32-byte boundary, so that each
+        // load instruction uses whole 32-byte sectors.  Measured on 8192 x {4096, 14336}:
+        // row + transposed 5-20% faster, transposed only 2-14%, 2D unchanged; the
+        // row-only pass was 13% slower with them and keeps 16-byte loads.
+        const bool a32 = (COLT || TWOD) && ((reinterpret_cast<uintptr_t>(p.x) | (uintptr_t)(p.ld * 2)) & 31u) == 0;
         if (vx) {
             const uint4* src = reinterpret_cast<const uint4*>(p.x + grx * p.ld + gc);
             if (a32) {
