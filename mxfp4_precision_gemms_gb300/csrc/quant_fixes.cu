@@ -12,6 +12,8 @@
 //  MBS: per 128 values (one tile row) one byte k, the largest value with
 //       (1 + k/256) f <= T for the macro amax A = f 2^E (T = 1.5 if f <= 1.5, else 3);
 //       v' = fl32((1 + k/256) v), q = Q(v'); reconstruction dq(q) / (1 + k/256).
+#include <cuda_fp16.h>
+
 #include "quant_math.cuh"
 
 namespace mx {
@@ -57,11 +59,34 @@ __device__ __forceinline__ void rotate_normalised(float2 (&v)[32]) {
     }
 }
 
-// Value of a 4-bit E2M1 code (sign in bit 3): 0, 0.5, 1, 1.5, 2, 3, 4, 6.
-__device__ __forceinline__ float e2m1_value(uint32_t c) {
-    const uint32_t m = c & 7u;
-    const uint32_t mag = m >= 2u ? (((125u + (m >> 1)) + 1u) << 23) | ((m & 1u) << 22) : (m == 1u ? 0x3F000000u : 0u);
-    return __uint_as_float(mag | ((c & 8u) << 28));
+// Values of E2M1 codes 2B and 2B + 1 of a packed word (code i in nibble i): the hardware
+// conversion of byte B to an f16 pair {nibble 2B, nibble 2B + 1}, widened to fp32.  Exact:
+// every E2M1 value (0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives, -0 included) is an f16.
+template <int B>
+__device__ __forceinline__ float2 e2m1x2_value(uint32_t w) {
+    uint32_t h;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b%2;\n\t}"
+        : "=r"(h)
+        : "r"(w), "n"(B));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Packed fused multiply-add of two independent fp32 pairs: a * b + c, one rounding each.
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// Elements 2B, 2B + 1 of both vectors: v - dq(q1) = v + d * (-2^e).
+template <int B>
+__device__ __forceinline__ void residual_pair(uint32_t wx, uint32_t wy, float2 npx, float2& v0, float2& v1) {
+    const float2 dx = e2m1x2_value<B>(wx), dy = e2m1x2_value<B>(wy);
+    v0 = f2_fma(make_float2(dx.x, dy.x), npx, v0);
+    v1 = f2_fma(make_float2(dx.y, dy.y), npx, v1);
 }
 
 // 2^e for e = byte - 127 in [-127, 127] (2^-127 is subnormal; exact).
@@ -96,13 +121,17 @@ __global__ void __launch_bounds__(FX_THREADS, 5) rq_of_kernel(const QuantParams 
     store_row(p.row, p, grx, gc, vx, qx, b1x);
     store_row(p.row, p, gry, gc, vy, qy, b1y);
 
-    // residual v - dq(q1), exact in fp32
-    const float2 px = make_float2(pow2_of_byte(b1x), pow2_of_byte(b1y));
+    // residual v - dq(q1), exact in fp32: the product d * 2^e is exact (a power-of-two
+    // scaling of an E2M1 value, at worst a subnormal well above 2^-149), so the fused
+    // v + d * (-2^e) rounds once, to the exact difference
+    const float2 npx = make_float2(-pow2_of_byte(b1x), -pow2_of_byte(b1y));
     const uint32_t wx[4] = {qx.x, qx.y, qx.z, qx.w}, wy[4] = {qy.x, qy.y, qy.z, qy.w};
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const float2 d = make_float2(e2m1_value(wx[i >> 3] >> (4 * (i & 7))), e2m1_value(wy[i >> 3] >> (4 * (i & 7))));
-        v[i] = f2_sub(v[i], f2_mul(d, px));
+    for (int j = 0; j < 4; ++j) {
+        residual_pair<0>(wx[j], wy[j], npx, v[8 * j], v[8 * j + 1]);
+        residual_pair<1>(wx[j], wy[j], npx, v[8 * j + 2], v[8 * j + 3]);
+        residual_pair<2>(wx[j], wy[j], npx, v[8 * j + 4], v[8 * j + 5]);
+        residual_pair<3>(wx[j], wy[j], npx, v[8 * j + 6], v[8 * j + 7]);
     }
 
     // second pass; alpha carried by the scale byte
