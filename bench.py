@@ -520,6 +520,10 @@ def gpu_arm(args, rank, world, dist):
     if not args.skip_fixes:
         fixes = quant_fixes_leg(flush, hbm)
 
+    block = None
+    if not args.skip_block:
+        block = decoder_block_leg(flush, args.steps, args.warmup, dev)
+
     fp8 = None
     if not args.skip_fp8:
         fp8 = fp8_comparator(layers, flush, args.steps, args.warmup)
@@ -550,7 +554,70 @@ def gpu_arm(args, rank, world, dist):
         "device_status": status,
         "fp8_comparator": fp8,
         "quant_fixes": fixes,
+        "decoder_block": block,
     }
+    return out
+
+
+def decoder_block_leg(flush, steps, warmup, dev):
+    """One Llama-3.1-8B-shaped decoder block at T = 8192: the seven linear layers (q, k, v,
+    o, gate, up, down; k and v have N = 1024), each with Fprop, Dgrad and Wgrad under H16 +
+    MXFP4, quantisation included -- 42 launches, 10.72 TFLOP.  Each linear's X, W and dY
+    are drawn from the block's distributions (seed base 4000 + 10 i); the block's non-GEMM
+    ops (RMSNorm, SiLU, attention core) lie outside the timed GEMM path and are not run.
+    Total: the block's launches as one two-branch CUDA graph, events around each replay.
+    Per layer: the same launches on one stream with events around each layer's six.  L2 is
+    emptied before every timed block."""
+    import torch
+
+    from mxfp4_precision_gemms_gb300 import binding as mx
+    from mxfp4_precision_gemms_gb300 import synth
+
+    layers = [Layer(n, N, K, 4000 + 10 * i, dev) for i, (n, N, K) in enumerate(synth.LLAMA8B_BLOCK_LINEARS)]
+    fl = flops_per_step(synth.LLAMA8B_BLOCK_LINEARS)
+    for _ in range(warmup):
+        run_step(layers)
+    side, aux = torch.cuda.Stream(), torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        run_step(layers, aux=aux)
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    tot = []
+    for _ in range(steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        tot.append((a, b))
+    per = {L.name: 0.0 for L in layers}
+    for _ in range(steps):
+        flush()
+        for L in layers:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run_step([L])
+            b.record()
+            L.ev = (a, b)
+        torch.cuda.synchronize()
+        for L in layers:
+            per[L.name] += L.ev[0].elapsed_time(L.ev[1])
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0, "device status after the decoder-block leg"
+    ms = sum(a.elapsed_time(b) for a, b in tot) / steps
+    out = {"workload": "one Llama-3.1-8B decoder block, T=8192: q, k, v, o, gate, up, down; fprop+dgrad+wgrad, "
+                       "H16, OCP floor, quantisation included",
+           "tflop_per_block": round(fl / 1e12, 3), "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+           "launch": "CUDA graph of the block's 42 launches, two branches per linear", "per_layer": {}}
+    for L in layers:
+        lms = per[L.name] / steps
+        out["per_layer"][L.name] = {"N": L.N, "K": L.K, "ms": round(lms, 4),
+                                    "tflops": round(L.gemm_flops / (lms * 1e-3) / 1e12, 1)}
+    out["per_layer_note"] = "each layer's six launches on one stream, events around them"
     return out
 
 
@@ -843,7 +910,7 @@ def write_traffic(csv_path):
                "sources_sha": kernel_sources_sha(KERNEL_SOURCES[k])} for k, v in per.items() if v}
     rec["command"] = ("ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
                       "--clock-control none --csv --log-file <csv> python bench.py --steps 1 --warmup 3 "
-                      "--skip-e2e --skip-cpu-baseline --skip-fp8 --skip-fixes")
+                      "--skip-e2e --skip-cpu-baseline --skip-fp8 --skip-fixes --skip-block")
     path = os.path.join(ROOT, "profiles", "traffic_llama8b_linears_T8192.json")
     json.dump(rec, open(path, "w"), indent=1)
     print(json.dumps(rec))
@@ -858,6 +925,7 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time the step as stream launches, not a CUDA graph")
     ap.add_argument("--skip-fixes", action="store_true", help="skip the OF / MBS quantiser measurement")
+    ap.add_argument("--skip-block", action="store_true", help="skip the decoder-block (seven linears) measurement")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-fp8", action="store_true", help="skip the FP8 (torch._scaled_mm) comparator")
     ap.add_argument("--serial-step", action="store_true",
