@@ -43,6 +43,15 @@ def flops_per_step(linears=None):
     return sum(3 * 2 * T_TOKENS * N * K for _, N, K in linears)
 
 
+def step_stats(ms):
+    """Median and 10th / 90th percentiles of the timed steps' durations (ms)."""
+    v = sorted(ms)
+    if not v:
+        return None
+    q = lambda f: v[min(len(v) - 1, int(round(f * (len(v) - 1))))]
+    return {"median": round(statistics.median(v), 4), "p10": round(q(0.1), 4), "p90": round(q(0.9), 4)}
+
+
 def quant_bytes(R, C, dual):
     """Algorithmic bytes of one rotate+quantise pass: bf16 read + codes + scales per copy."""
     return R * C * 2 + (2 if dual else 1) * (R * C // 2 + R * C // 32)
@@ -87,7 +96,7 @@ def job_throughput(local_ms, work_per_step, steps, world, dist, device):
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
@@ -117,7 +126,7 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, mx, reasons = [], None, set()
+        sm, mem, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             p = [x.strip() for x in line.split(",")]
@@ -131,8 +140,13 @@ class ClockSampler:
             for n, v in zip(names, p[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+            if len(p) > 9:
+                try:
+                    mem.append(float(p[9]))
+                except ValueError:
+                    pass
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "mem_mhz": statistics.median(mem) if mem else None, "samples": len(sm)}
 
 
 # --------------------------------------------------------------------------- ncu traffic
@@ -551,6 +565,8 @@ def gpu_arm(args, rank, world, dist):
         "e2e": e2e,
         "gpu_launches": args.steps * LAUNCHES_PER_LAYER * len(layers),
         "clocks": clk.summary(),
+        "gpu": torch.cuda.get_device_name(dev),
+        "step_ms_stats": step_stats(step_ms),
         "device_status": status,
         "fp8_comparator": fp8,
         "quant_fixes": fixes,
