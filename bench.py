@@ -22,6 +22,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -101,7 +102,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the raw samples: a temporary file unless BENCH_CLOCKS_DIR names a folder
+        self.path = os.path.join(os.environ.get("BENCH_CLOCKS_DIR") or tempfile.gettempdir(),
+                                 f"mxfp4_bench_clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
