@@ -81,6 +81,7 @@ def lib():
             L.oracle_e2m1_code_sr.restype = I
             L.oracle_quantize_row_rand.argtypes = [P, I64, I64, I64, I, I, P, P, P, P]
             L.oracle_quantize_colT_rand.argtypes = [P, I64, I64, I64, I, I, P, P, P, P]
+            L.oracle_rotation_divergence.argtypes = [P, I64, I64, I64, I, I, P]
             L.oracle_num_threads.restype = I
             L.oracle_set_num_threads.argtypes = [I]
             _lib = L
@@ -281,6 +282,18 @@ def error_decomposition(x_bf16, had, mode):
     lib().oracle_error_decomposition(_p(x), R, C, C, had, mode, _p(out))
     keys = ("e2", "scale2", "dz2", "grid2", "scale_grid", "n_deadzone", "n")
     return dict(zip(keys, out.tolist()))
+
+
+def rotation_divergence(x_bf16: np.ndarray, had: int, mode: int) -> dict:
+    """Diagnostic of the canonical fp32 rotation ("Pretraining Large Language Models with
+    MXFP4 on Native FP4 Hardware", A.2, which defines the rotation exactly): among the
+    32-blocks of the row layout of x [R, C], how many would get other codes or another
+    E8M0 byte if the exact fp64 rotation were quantised instead.  Not a failure."""
+    x = _u16(x_bf16)
+    R, C = x.shape
+    out = np.zeros(3, np.int64)
+    lib().oracle_rotation_divergence(_p(x), R, C, C, had, mode, _p(out))
+    return {"blocks_differ": int(out[0]), "bytes_differ": int(out[1]), "blocks": int(out[2])}
 
 
 # --------------------------------------------------------------------------- quantiser fixes

@@ -87,8 +87,12 @@ double oracle_e2m1_value(int code) {
  * mode 1 (ceiling):   smallest e with 6 * 2^e >= amax, so that the E8M0 scale is
  *                     never below the ideal scale amax / 6 ([DECOMP] "core insight").
  * Both clamped to [-127, 127]; amax == 0 gives -127. */
-int oracle_shared_exponent(float amax_f, int mode) {
-    double amax = (double)amax_f;
+static int shared_exponent_f64(double amax, int mode);
+
+int oracle_shared_exponent(float amax_f, int mode) { return shared_exponent_f64((double)amax_f, mode); }
+
+/* The same rule for any non-negative fp64 amax (the fp32 entry point widens exactly). */
+static int shared_exponent_f64(double amax, int mode) {
     if (!(amax > 0.0)) return -127;
     int ex;
     frexp(amax, &ex);              /* amax = f * 2^ex, f in [0.5, 1) */
@@ -616,4 +620,55 @@ void oracle_quantize_colT_rand(const uint16_t* x, int64_t R, int64_t C, int64_t 
     for (int64_t c = 0; c < C; ++c)
         oracle_quantize_vec_rand(x + c, ld, R, had, mode, row_signs, sr ? sr + c * R : 0, codes + c * (R / 2),
                                  scales + c * (R / 32));
+}
+
+/* ------------------------------------------------------------------------- */
+/* Diagnostic: canonical fp32 rotation against the exact rotation             */
+/* ------------------------------------------------------------------------- */
+
+/* The pages fix the rotation only in exact arithmetic ([MXFP4-HW] A.2); the quantiser
+ * takes the canonical fp32 order.  For x [R, C] (row layout, blocks of 32 along C) this
+ * counts the blocks whose E8M0 byte or codes would change if the exact rotation -- fp64
+ * products with the +-1 matrix divided by sqrt(n) -- were quantised instead: amax of
+ * the exact values, the same exponent rule, codes of v / 2^e by the same nearest-grid
+ * search.  out[0] = blocks that differ, out[1] = blocks whose byte differs,
+ * out[2] = blocks.  A diagnostic of the canonical order, not a failure. */
+void oracle_rotation_divergence(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,
+                                int64_t* out) {
+    int64_t differ = 0, byte_differ = 0;
+#pragma omp parallel for schedule(static) reduction(+ : differ, byte_differ)
+    for (int64_t r = 0; r < R; ++r) {
+        float* xf = (float*)malloc(sizeof(float) * (size_t)C);
+        float* v = (float*)malloc(sizeof(float) * (size_t)C);
+        double* xd = (double*)malloc(sizeof(double) * (size_t)C);
+        double* vd = (double*)malloc(sizeof(double) * (size_t)C);
+        for (int64_t c = 0; c < C; ++c) {
+            xf[c] = bf16_to_float(x[r * ld + c]);
+            xd[c] = (double)xf[c];
+        }
+        oracle_rotate_f32(xf, C, had, v);
+        oracle_rotate_f64(xd, C, had, vd);
+        for (int64_t b = 0; b < C / 32; ++b) {
+            const float* blk = v + b * 32;
+            const double* bd = vd + b * 32;
+            const int e = oracle_shared_exponent(block_amax(blk, 32), mode);
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i)
+                if (fabs(bd[i]) > amax) amax = fabs(bd[i]);
+            const int ex = shared_exponent_f64(amax, mode);
+            uint8_t q[32];
+            quantize_block(blk, e, q);
+            int same = ex == e;
+            for (int i = 0; i < 32 && same; ++i) same = oracle_e2m1_code(ldexp(bd[i], -ex)) == q[i];
+            differ += !same;
+            byte_differ += ex != e;
+        }
+        free(xf);
+        free(v);
+        free(xd);
+        free(vd);
+    }
+    out[0] = differ;
+    out[1] = byte_differ;
+    out[2] = R * (C / 32);
 }
