@@ -137,3 +137,31 @@ def test_empty_input(torch):
     x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
     outs = mx.rotate_quantize(x, layouts=1 | 2)
     assert outs["row"].rows == 0
+
+
+@pytest.mark.parametrize("layouts", [1, 2, 3, 4])
+@pytest.mark.parametrize("pad,offset", [(8, 0), (0, 8), (16, 0), (24, 16)])
+def test_strided_and_offset_inputs(torch, layouts, pad, offset):
+    """x as a view into a larger bf16 buffer: leading dimension C + pad and a start
+    offset of `offset` elements (16-byte granules).  Rows that start on a 32-byte
+    boundary take the kernel's 32-byte loads, the others its 16-byte loads; both must
+    give the oracle's bytes for the same values."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    R, C = 320, 1056
+    xbits = synth.heavy_tailed(R, C, 77 + pad + offset)
+    big = torch.zeros((R + 1) * (C + pad) + offset, dtype=torch.bfloat16, device="cuda")
+    view = big[offset:offset + R * (C + pad)].view(R, C + pad)[:, :C]
+    view.copy_(mx.bf16_tensor(xbits))
+    assert view.stride(0) == C + pad and view.data_ptr() % 16 == 0
+    outs = mx.rotate_quantize(view, had=16, mode=0, layouts=layouts, sf_layout=0)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    names = {mx.LAYOUT_ROW: "row", mx.LAYOUT_COLT: "colT", mx.LAYOUT_2D: "2d"}
+    for bit, key in names.items():
+        if not layouts & bit:
+            continue
+        want_c, want_s = oracle.quantize(xbits, ORACLE_HAD[16], 0, key)
+        gc, gs = outs[key].codes.cpu().numpy(), outs[key].plain_scales()
+        assert np.array_equal(gs, want_s), f"{key} scales, pad {pad} offset {offset}"
+        assert np.array_equal(gc, want_c), f"{key} codes, pad {pad} offset {offset}"
