@@ -123,3 +123,40 @@ def test_fix_argument_checks(torch):
     e = mx.bf16_tensor(np.zeros((0, 128), np.uint16))
     q, mbs = mx.rotate_quantize_mbs(e)
     assert q.rows == 0 and mbs.numel() == 0
+
+
+def _strided(torch, xb, pad, offset):
+    """x's values in a view with leading dimension C + pad, starting `offset` elements
+    into a larger buffer."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    R, C = xb.shape
+    big = torch.zeros((R + 1) * (C + pad) + offset, dtype=torch.bfloat16, device="cuda")
+    view = big[offset:offset + R * (C + pad)].view(R, C + pad)[:, :C]
+    view.copy_(mx.bf16_tensor(xb))
+    return view
+
+
+@pytest.mark.parametrize("pad,offset", [(8, 0), (0, 8), (136, 24)])
+def test_of_and_mbs_strided_inputs(torch, pad, offset):
+    """OF and MBS read x through its leading dimension and start address: a view into a
+    larger buffer gives the oracle's bytes for the same values."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    R, C = 130, 384
+    xb = synth.heavy_tailed(R, C, 900 + pad + offset)
+    x = _strided(torch, xb, pad, offset)
+    q1, q2 = mx.rotate_quantize_of(x, had=16, mode=0, alpha_log2=-1, sf_layout=mx.SF_PLAIN)
+    q, mbs = mx.rotate_quantize_mbs(x, had=16, mode=1, sf_layout=mx.SF_PLAIN)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    c1, s1, c2, s2, bad = oracle.quantize_of(xb, ORACLE_HAD[16], 0, -1)
+    assert bad == 0
+    same(q1.plain_scales(), s1, "OF q1 scales")
+    same(q1.codes.cpu().numpy(), c1, "OF q1 codes")
+    same(q2.plain_scales(), s2, "OF q2 scales")
+    same(q2.codes.cpu().numpy(), c2, "OF q2 codes")
+    c, s, m = oracle.quantize_mbs(xb, ORACLE_HAD[16], 1)
+    same(q.plain_scales(), s, "MBS scales")
+    same(q.codes.cpu().numpy(), c, "MBS codes")
+    same(mbs.cpu().numpy(), m, "MBS bytes")

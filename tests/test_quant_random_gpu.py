@@ -107,3 +107,30 @@ def test_sr_argument_checks(torch):
         mx.rotate_quantize_rand(x, layouts=mx.LAYOUT_ROW | mx.LAYOUT_COLT, sr_row=r)
     with pytest.raises(RuntimeError):  # 2D layout with an option
         mx.rotate_quantize_rand(x, layouts=mx.LAYOUT_2D, sr_row=r)
+
+
+@pytest.mark.parametrize("pad,offset", [(8, 0), (0, 8)])
+def test_randomised_strided_inputs(torch, pad, offset):
+    """Random signs and stochastic rounding on both copies, x read through a view with
+    leading dimension C + pad starting `offset` elements into a larger buffer."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    R, C = 128, 384
+    g = np.random.default_rng(31 + pad + offset)
+    xb = synth.heavy_tailed(R, C, 950 + pad + offset)
+    big = torch.zeros((R + 1) * (C + pad) + offset, dtype=torch.bfloat16, device="cuda")
+    x = big[offset:offset + R * (C + pad)].view(R, C + pad)[:, :C]
+    x.copy_(mx.bf16_tensor(xb))
+    cs = oracle.pack_signs(g.random(C) < 0.5)
+    rs = oracle.pack_signs(g.random(R) < 0.5)
+    srr = g.integers(0, 65536, (R, C)).astype(np.uint16)
+    src = g.integers(0, 65536, (C, R)).astype(np.uint16)
+    out = mx.rotate_quantize_rand(x, had=16, mode=0, layouts=mx.LAYOUT_ROW | mx.LAYOUT_COLT,
+                                  col_signs=dev(torch, cs), row_signs=dev(torch, rs), sr_row=dev(torch, srr),
+                                  sr_colT=dev(torch, src), sf_layout=mx.SF_MMA)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    for key, signs, sr in (("row", cs, srr), ("colT", rs, src)):
+        wc, ws = oracle.quantize_rand(xb, ORACLE_HAD[16], 0, key, signs=signs, sr=sr)
+        same(out[key].plain_scales(), ws, f"{key} strided scales")
+        same(out[key].codes.cpu().numpy(), wc, f"{key} strided codes")
