@@ -392,6 +392,7 @@ class L2Flush:
         import torch
 
         self.sum = torch.sum
+        self.sleep = torch.cuda._sleep
         self.w = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
         self.r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
         self.out = torch.empty((), dtype=torch.float32, device=dev)
@@ -399,6 +400,10 @@ class L2Flush:
     def __call__(self):
         self.w.fill_(1.0)
         self.sum(self.r, dim=0, out=self.out)
+        # then keep the GPU busy for about 50 us more, so that the host has enqueued the
+        # timed launches before the GPU reaches the start event: the host's own launch
+        # cost then stays out of the timed interval, even for kernels of a few us
+        self.sleep(100_000)
 
 
 def gpu_arm(args, rank, world, dist):
@@ -687,31 +692,35 @@ def quant_fixes_leg(flush, hbm, iters=20):
             tot += a.elapsed_time(b)
         gbs = by / (tot / iters * 1e-3) / 1e9
         out[name] = {"gbs": round(gbs, 1), "frac": round(gbs / hbm, 4), "us": round(tot / iters * 1e3, 1)}
-    # the quantiser sweep of the heavy-tailed tensors (0.1 t(3) + 0.1% entries x100):
-    # {none, H16, H32} x {row, colT, 2D} x {floor, ceil}, GB/s
-    xs = mx.bf16_tensor(synth.heavy_tailed(R, C, 13))
-    sweep = {}
-    for had in (mx.HAD_NONE, mx.HAD_16, mx.HAD_32):
-        for lay, lname, by in ((mx.LAYOUT_ROW, "row", 2 + 0.5 + 1 / 32), (mx.LAYOUT_COLT, "colT", 2 + 0.5 + 1 / 32),
-                               (mx.LAYOUT_2D, "2d", 2 + 0.5 + 1 / 1024)):
-            for mode, mname in ((mx.SCALE_FLOOR, "floor"), (mx.SCALE_CEIL, "ceil")):
-                # row and transposed copies with their scales in the order the GEMM reads
-                # (the library default); the 2D layout has the plain order only
-                fn = lambda: mx.rotate_quantize(xs, had, mode, lay, sf_layout=mx.SF_MMA)
-                for _ in range(3):
-                    fn()
-                tot = 0.0
-                for _ in range(10):
-                    flush()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record()
-                    fn()
-                    b.record()
-                    b.synchronize()
-                    tot += a.elapsed_time(b)
-                sweep[f"h{had}_{lname}_{mname}"] = round(n * by / (tot / 10 * 1e-3) / 1e9, 1)
-    out["sweep_gbs"] = sweep
-    out["sweep_tensor"] = f"{R}x{C} bf16, 0.1 t(3) + 0.1% entries x100; row / colT scales in MMA order, 2D plain"
+    # the quantiser sweep of the heavy-tailed tensors (0.1 t(3) + 0.1% entries x100), both
+    # sizes of the sweep workload: {none, H16, H32} x {row, colT, 2D} x {floor, ceil}, GB/s
+    for (SR, SC), key in (((R, C), "sweep_gbs"), ((4096, 4096), "sweep_gbs_4096x4096")):
+        xs = mx.bf16_tensor(synth.heavy_tailed(SR, SC, 13))
+        ns = SR * SC
+        sweep = {}
+        for had in (mx.HAD_NONE, mx.HAD_16, mx.HAD_32):
+            for lay, lname, by in ((mx.LAYOUT_ROW, "row", 2 + 0.5 + 1 / 32),
+                                   (mx.LAYOUT_COLT, "colT", 2 + 0.5 + 1 / 32),
+                                   (mx.LAYOUT_2D, "2d", 2 + 0.5 + 1 / 1024)):
+                for mode, mname in ((mx.SCALE_FLOOR, "floor"), (mx.SCALE_CEIL, "ceil")):
+                    # row and transposed copies with their scales in the order the GEMM reads
+                    # (the library default); the 2D layout has the plain order only
+                    fn = lambda: mx.rotate_quantize(xs, had, mode, lay, sf_layout=mx.SF_MMA)
+                    for _ in range(3):
+                        fn()
+                    tot = 0.0
+                    for _ in range(10):
+                        flush()
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record()
+                        fn()
+                        b.record()
+                        b.synchronize()
+                        tot += a.elapsed_time(b)
+                    sweep[f"h{had}_{lname}_{mname}"] = round(ns * by / (tot / 10 * 1e-3) / 1e9, 1)
+        out[key] = sweep
+    out["sweep_tensor"] = (f"{R}x{C} and 4096x4096 bf16, 0.1 t(3) + 0.1% entries x100; row / colT scales in MMA "
+                           "order, 2D plain")
     assert mx.device_status() == 0
     return out
 
