@@ -651,7 +651,7 @@ def quant_fixes_leg(flush, hbm, iters=20):
     launch timed alone with CUDA events after an L2 flush, against the HBM roofline.
     Algorithmic bytes per element: OF 2 + 2 x (0.5 + 1/32); MBS 2 + 0.5 + 1/32 + 1/128;
     random signs + stochastic rounding, both copies, 2 + 2 x 2 (random integers) + 2 x
-    (0.5 + 1/32).
+    (0.5 + 1/32); random signs alone, both copies, 2 + 2 x (0.5 + 1/32).
     Not part of the timed step: a measurement of the variants."""
     import torch
 
@@ -677,6 +677,9 @@ def quant_fixes_leg(flush, hbm, iters=20):
                                                              col_signs=col_signs, row_signs=row_signs, sr_row=sr_row,
                                                              sr_colT=sr_colT),
                              n * (2 + 2 * 2 + 2 * (0.5 + 1 / 32)))
+    legs["signs_dual"] = (lambda: mx.rotate_quantize_rand(x, had=16, mode=0, layouts=mx.LAYOUT_ROW | mx.LAYOUT_COLT,
+                                                          col_signs=col_signs, row_signs=row_signs),
+                          n * (2 + 2 * (0.5 + 1 / 32)))
     out = {"tensor": f"{R}x{C} bf16 activations, H16, OCP floor", "unit": "GB/s", "peak": hbm}
     for name, (fn, by) in legs.items():
         for _ in range(3):

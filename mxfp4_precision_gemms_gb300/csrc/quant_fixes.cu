@@ -94,11 +94,14 @@ __device__ __forceinline__ float pow2_of_byte(uint32_t byte) {
     return __uint_as_float(byte >= 1u ? byte << 23 : 0x00400000u);
 }
 
-__device__ __forceinline__ void store_row(const QuantOut& o, const QuantParams& p, int64_t gr, int64_t gc, bool valid,
-                                          uint4 q, uint32_t byte) {
-    if (!valid) return;
-    *reinterpret_cast<uint4*>(o.codes + gr * (p.C / 2) + gc / 2) = q;
-    store_scale(o, gr, gc / 32, p.C / 32, byte);
+// The thread's two 16-byte code pieces (rows gx and gy, columns gc .. gc + 31) and the
+// tile rows' scale bytes (gathered into one 32-bit store per row).  Every lane calls it.
+__device__ __forceinline__ void store_rows(const QuantOut& o, const QuantParams& p, int64_t col0, int s, int64_t gx,
+                                           int64_t gy, int64_t gc, bool vx, bool vy, uint4 qx, uint4 qy,
+                                           uint32_t bx, uint32_t by) {
+    if (vx) *reinterpret_cast<uint4*>(o.codes + gx * (p.C / 2) + gc / 2) = qx;
+    if (vy) *reinterpret_cast<uint4*>(o.codes + gy * (p.C / 2) + gc / 2) = qy;
+    store_row_scales(o, p, col0, s, gx, gy, vx, vy, bx, by);
 }
 
 template <int HAD>
@@ -118,8 +121,7 @@ __global__ void __launch_bounds__(FX_THREADS, 5) rq_of_kernel(const QuantParams 
     const uint32_t b1x = scale_byte(ax, p.mode), b1y = scale_byte(ay, p.mode);
     uint4 qx, qy;
     quant32x2<1>(v, b1x, b1y, qx, qy);
-    store_row(p.row, p, grx, gc, vx, qx, b1x);
-    store_row(p.row, p, gry, gc, vy, qy, b1y);
+    store_rows(p.row, p, col0, s, grx, gry, gc, vx, vy, qx, qy, b1x, b1y);
 
     // residual v - dq(q1), exact in fp32: the product d * 2^e is exact (a power-of-two
     // scaling of an E2M1 value, at worst a subnormal well above 2^-149), so the fused
@@ -138,8 +140,8 @@ __global__ void __launch_bounds__(FX_THREADS, 5) rq_of_kernel(const QuantParams 
     amax32x2<1>(v, ax, ay);
     const uint32_t b2x = scale_byte(ax, p.mode), b2y = scale_byte(ay, p.mode);
     quant32x2<1>(v, b2x, b2y, qx, qy);
-    store_row(q2, p, grx, gc, vx, qx, (uint32_t)max((int)b2x + alpha_log2, 0));
-    store_row(q2, p, gry, gc, vy, qy, (uint32_t)max((int)b2y + alpha_log2, 0));
+    store_rows(q2, p, col0, s, grx, gry, gc, vx, vy, qx, qy, (uint32_t)max((int)b2x + alpha_log2, 0),
+               (uint32_t)max((int)b2y + alpha_log2, 0));
 }
 
 // MBS byte from the macro-block amax A (fp32 bits): k = floor(256 (T - f) / f) with
@@ -180,8 +182,7 @@ __global__ void __launch_bounds__(FX_THREADS, 5) rq_mbs_kernel(const QuantParams
     const uint32_t bx = scale_byte(ax, p.mode), by = scale_byte(ay, p.mode);
     uint4 qx, qy;
     quant32x2<1>(v, bx, by, qx, qy);
-    store_row(p.row, p, grx, gc, vx, qx, bx);
-    store_row(p.row, p, gry, gc, vy, qy, by);
+    store_rows(p.row, p, col0, s, grx, gry, gc, vx, vy, qx, qy, bx, by);
     if (s == 0) {
         if (vx) mbs[grx * (p.C / 128) + col0 / 128] = (uint8_t)kx;
         if (vy) mbs[gry * (p.C / 128) + col0 / 128] = (uint8_t)ky;

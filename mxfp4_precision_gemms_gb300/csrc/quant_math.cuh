@@ -142,4 +142,134 @@ __device__ __forceinline__ void store_scale(const QuantOut& o, int64_t r, int64_
     o.scales[off] = (uint8_t)byte;
 }
 
+// ---- shared by the tiled quantiser kernels (64 x 128 bf16 tiles, 128 threads) ----
+
+// Staged tile of 64 rows x 128 bf16: 32-bit word index of 16-byte chunk q (0..15) of row
+// r.  The XOR on the chunk index (by q bits 2-3, row bit 0 and row bit 5) keeps the
+// row-wise 16-byte writes (8 rows x 4 segments per warp) and the column-wise 32-bit reads
+// (rows i and 32 + i, 16 column pairs each, per warp) bank-conflict free.
+__device__ __forceinline__ int tile_chunk(int r, int q) {
+    return r * 64 + ((q ^ ((q >> 2) & 3) ^ (((r ^ (r >> 5)) & 1) << 2)) << 2);
+}
+
+// One 32-byte global store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_32B(void* dst, uint4 a, uint4 b) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a.x), "r"(a.y),
+                 "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
+// One 32-byte streaming global load (the address must be 32-byte aligned).
+__device__ __forceinline__ void ld_global_cs_32B(const void* src, uint4& a, uint4& b) {
+    asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(src));
+}
+
+// The thread's two 64-byte row segments of bf16 (rows gx and gy of x, columns gc ..
+// gc + 31; zeros where not valid).  32-byte loads when `wide` (every row segment starts
+// on a 32-byte boundary), so that each load instruction uses whole 32-byte sectors.
+__device__ __forceinline__ void load_row_pair(const QuantParams& p, int64_t gx, int64_t gy, int64_t gc, bool vx,
+                                              bool vy, bool wide, uint4 (&rx)[4], uint4 (&ry)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) rx[j] = ry[j] = make_uint4(0, 0, 0, 0);
+    if (vx) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + gx * p.ld + gc);
+        if (wide) {
+            ld_global_cs_32B(src, rx[0], rx[1]);
+            ld_global_cs_32B(src + 2, rx[2], rx[3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) rx[j] = __ldcs(src + j);
+        }
+    }
+    if (vy) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + gy * p.ld + gc);
+        if (wide) {
+            ld_global_cs_32B(src, ry[0], ry[1]);
+            ld_global_cs_32B(src + 2, ry[2], ry[3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ry[j] = __ldcs(src + j);
+        }
+    }
+}
+
+// Whether every row segment of x starts on a 32-byte boundary.
+__device__ __forceinline__ bool rows_32B_aligned(const QuantParams& p) {
+    return ((reinterpret_cast<uintptr_t>(p.x) | (uintptr_t)(p.ld * 2)) & 31u) == 0;
+}
+
+// Row-copy scale bytes of one tile row: the four segments of the row are lanes
+// 4 pr .. 4 pr + 3 (s = lane & 3) and their bytes are consecutive (k = col0/32 + s,
+// col0/32 a multiple of 4) in both scale orders.  MMA order: one 32-bit store, rows past
+// R and columns past C carrying byte 0 into the zeroed padding.  Plain order: one 32-bit
+// store when the row exists, all four blocks exist and the offset is 4-byte aligned,
+// else byte stores.  Every lane of the warp must call this.
+__device__ __forceinline__ void store_row_scales(const QuantOut& o, const QuantParams& p, int64_t col0, int s,
+                                                 int64_t gx, int64_t gy, bool vx, bool vy, uint32_t bx,
+                                                 uint32_t by) {
+    uint32_t wx = bx << (8 * s), wy = by << (8 * s);
+#pragma unroll
+    for (int d = 1; d <= 2; d <<= 1) {
+        wx |= __shfl_xor_sync(0xffffffffu, wx, d);
+        wy |= __shfl_xor_sync(0xffffffffu, wy, d);
+    }
+    const int64_t k0 = col0 / 32, kb = p.C / 32;
+    if (o.sf_mma) {
+        if (s == 0) {
+            *reinterpret_cast<uint32_t*>(o.scales + sf_mma_offset(gx, k0, o.kb_pad)) = wx;
+            *reinterpret_cast<uint32_t*>(o.scales + sf_mma_offset(gy, k0, o.kb_pad)) = wy;
+        }
+    } else if (k0 + 4 <= kb && (kb & 3) == 0) {
+        if (s == 0 && gx < p.R) *reinterpret_cast<uint32_t*>(o.scales + gx * kb + k0) = wx;
+        if (s == 0 && gy < p.R) *reinterpret_cast<uint32_t*>(o.scales + gy * kb + k0) = wy;
+    } else {
+        const int64_t gc = col0 + 32 * s;
+        if (vx) store_scale(o, gx, gc / 32, kb, bx);
+        if (vy) store_scale(o, gy, gc / 32, kb, by);
+    }
+}
+
+// Transposed copy of one warp's 16 column pairs: lanes l and l ^ 16 hold row blocks 0
+// and 1 of columns (2 cp, 2 cp + 1) as codes qx (column 2 cp), qy (column 2 cp + 1) and
+// bytes bx, by.  One shuffle exchange gives every lane one whole output row (2 cp + rb):
+// its two 16-byte halves leave as one 32-byte store and its two scale bytes as one 16-bit
+// store.  Every lane of the warp must call this.
+__device__ __forceinline__ void store_colT_pair(const QuantOut& o, const QuantParams& p, int64_t row0, int64_t col0,
+                                                int cp, int rb, uint4 qx, uint4 qy, uint32_t bx, uint32_t by) {
+    const uint4 send = rb == 0 ? qy : qx;
+    uint4 recv;
+    recv.x = __shfl_xor_sync(0xffffffffu, send.x, 16);
+    recv.y = __shfl_xor_sync(0xffffffffu, send.y, 16);
+    recv.z = __shfl_xor_sync(0xffffffffu, send.z, 16);
+    recv.w = __shfl_xor_sync(0xffffffffu, send.w, 16);
+    const uint32_t recv_b = __shfl_xor_sync(0xffffffffu, rb == 0 ? by : bx, 16);
+    const uint4 lo = rb == 0 ? qx : recv, hi = rb == 0 ? recv : qy;
+    const uint32_t b0 = rb == 0 ? bx : recv_b, b1 = rb == 0 ? recv_b : by;
+    const int64_t orow = col0 + 2 * cp + rb;
+    const int64_t left = (p.R - row0) / 32;
+    const int nrb = left >= 2 ? 2 : (int)left;  // valid 32-row blocks of the tile
+    if (orow >= p.C || nrb <= 0) return;
+    uint8_t* dst = o.codes + orow * (p.R / 2) + row0 / 2;
+    if (nrb == 2) {
+        if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+            st_global_32B(dst, lo, hi);
+        } else {
+            reinterpret_cast<uint4*>(dst)[0] = lo;
+            reinterpret_cast<uint4*>(dst)[1] = hi;
+        }
+    } else {
+        *reinterpret_cast<uint4*>(dst) = lo;
+    }
+    // k = row0/32 (even) and k + 1 are adjacent bytes in both scale orders
+    const int64_t off = o.sf_mma ? sf_mma_offset(orow, row0 / 32, o.kb_pad) : orow * (p.R / 32) + row0 / 32;
+    if (nrb == 2 && (off & 1) == 0) {
+        *reinterpret_cast<uint16_t*>(o.scales + off) = (uint16_t)(b0 | (b1 << 8));
+    } else {
+        store_scale(o, orow, row0 / 32, p.R / 32, b0);
+        if (nrb == 2) store_scale(o, orow, row0 / 32 + 1, p.R / 32, b1);
+    }
+}
+
 }  // namespace mx

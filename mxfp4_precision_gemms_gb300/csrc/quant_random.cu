@@ -8,19 +8,13 @@
 //     magnitude a in [lo, lo + step) rounds up iff r < ((a - lo) / step) * 65536, every
 //     term exact in fp32; a >= 6 saturates; the sign is kept.
 // Same tiling as rq_kernel (64 x 128 tiles, 128 threads, bf16 tile staged in shared
-// memory for the column work).
+// memory for the column work, transposed rows exchanged within a warp).
 #include "quant_math.cuh"
 
 namespace mx {
 namespace {
 
 constexpr int RQ_TR = 64, RQ_TC = 128, RQ_THREADS = 128;
-
-// 32-bit word index of 16-byte chunk q (0..15) of tile row r (bank-conflict-free for
-// row-wise uint4 writes and column-wise 32-bit reads).
-__device__ __forceinline__ int rq_chunk(int r, int q) {
-    return r * (RQ_TC / 2) + ((q ^ ((q >> 2) & 3) ^ ((r & 1) << 2)) << 2);
-}
 
 // Stochastically rounded grid value of u with the 16-bit integer r.
 __device__ __forceinline__ float sr_grid(float u, uint32_t r) {
@@ -89,23 +83,12 @@ __global__ void __launch_bounds__(RQ_THREADS, 4) rq_rand_kernel(const QuantParam
     const int64_t gc = col0 + 32 * s, grx = row0 + rx, gry = row0 + ry;
     const bool vx = grx < p.R && gc < p.C, vy = gry < p.R && gc < p.C;
     uint4 raw_x[4], raw_y[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) raw_x[j] = raw_y[j] = make_uint4(0, 0, 0, 0);
-    if (vx) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + grx * p.ld + gc);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) raw_x[j] = __ldcs(src + j);
-    }
-    if (vy) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + gry * p.ld + gc);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) raw_y[j] = __ldcs(src + j);
-    }
+    load_row_pair(p, grx, gry, gc, vx, vy, COLT && rows_32B_aligned(p), raw_x, raw_y);
     if constexpr (COLT) {  // the unflipped tile, for the column work
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            *reinterpret_cast<uint4*>(&tile[rq_chunk(rx, 4 * s + j)]) = raw_x[j];
-            *reinterpret_cast<uint4*>(&tile[rq_chunk(ry, 4 * s + j)]) = raw_y[j];
+            *reinterpret_cast<uint4*>(&tile[tile_chunk(rx, 4 * s + j)]) = raw_x[j];
+            *reinterpret_cast<uint4*>(&tile[tile_chunk(ry, 4 * s + j)]) = raw_y[j];
         }
     }
 
@@ -138,48 +121,43 @@ __global__ void __launch_bounds__(RQ_THREADS, 4) rq_rand_kernel(const QuantParam
         } else {
             quant32x2<HAD>(v, bytex, bytey, qx, qy);
         }
-        if (vx) {
-            *reinterpret_cast<uint4*>(p.row.codes + grx * (p.C / 2) + gc / 2) = qx;
-            store_scale(p.row, grx, gc / 32, p.C / 32, bytex);
-        }
-        if (vy) {
-            *reinterpret_cast<uint4*>(p.row.codes + gry * (p.C / 2) + gc / 2) = qy;
-            store_scale(p.row, gry, gc / 32, p.C / 32, bytey);
-        }
+        if (vx) *reinterpret_cast<uint4*>(p.row.codes + grx * (p.C / 2) + gc / 2) = qx;
+        if (vy) *reinterpret_cast<uint4*>(p.row.codes + gry * (p.C / 2) + gc / 2) = qy;
+        store_row_scales(p.row, p, col0, s, grx, gry, vx, vy, bytex, bytey);
     }
 
     if constexpr (COLT) {
         __syncthreads();
-        const int cp = t & 63, rb = t >> 6;
+        // Two adjacent columns x one 32-row block per thread; a warp holds both row blocks
+        // of its 16 column pairs (lanes l and l ^ 16), as in rq_kernel.  Lanes past the
+        // matrix compute on the tile's zeros and store nothing.
+        const int lane = t & 31;
+        const int rb = lane >> 4, cp = 16 * (t >> 5) + (lane & 15);
         const int64_t gcol = col0 + 2 * cp, grow = row0 + 32 * rb;
-        if (gcol < p.C && grow < p.R) {
-            const uint32_t bits = o.row_signs ? *reinterpret_cast<const uint32_t*>(o.row_signs + grow / 8) : 0u;
-            float2 v[32];
-            const int q = cp >> 2, wi = cp & 3;
+        const bool valid = gcol < p.C && grow < p.R;
+        const uint32_t bits = (o.row_signs && valid) ? *reinterpret_cast<const uint32_t*>(o.row_signs + grow / 8) : 0u;
+        float2 v[32];
+        const int q = cp >> 2, wi = cp & 3;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const uint32_t m = ((bits >> i) & 1u) * 0x80008000u;  // the row's sign, both columns
-                const uint32_t w = tile[rq_chunk(32 * rb + i, q) + wi] ^ m;
-                v[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-            }
-            rotate32x2<HAD>(v);
-            float ax, ay;
-            amax32x2<HAD>(v, ax, ay);
-            const uint32_t bytex = scale_byte(ax, p.mode), bytey = scale_byte(ay, p.mode);
-            uint4 qx, qy;
-            if constexpr (SR) {
-                uint32_t r_x[16], r_y[16];
-                load_r(o.sr_colT + gcol * p.R + grow, true, r_x);
-                load_r(o.sr_colT + (gcol + 1) * p.R + grow, true, r_y);
-                quant32x2_sr<HAD>(v, bytex, bytey, r_x, r_y, qx, qy);
-            } else {
-                quant32x2<HAD>(v, bytex, bytey, qx, qy);
-            }
-            *reinterpret_cast<uint4*>(p.colT.codes + gcol * (p.R / 2) + grow / 2) = qx;
-            *reinterpret_cast<uint4*>(p.colT.codes + (gcol + 1) * (p.R / 2) + grow / 2) = qy;
-            store_scale(p.colT, gcol, grow / 32, p.R / 32, bytex);
-            store_scale(p.colT, gcol + 1, grow / 32, p.R / 32, bytey);
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t m = ((bits >> i) & 1u) * 0x80008000u;  // the row's sign, both columns
+            const uint32_t w = tile[tile_chunk(32 * rb + i, q) + wi] ^ m;
+            v[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
         }
+        rotate32x2<HAD>(v);
+        float ax, ay;
+        amax32x2<HAD>(v, ax, ay);
+        const uint32_t bytex = scale_byte(ax, p.mode), bytey = scale_byte(ay, p.mode);
+        uint4 qx, qy;
+        if constexpr (SR) {
+            uint32_t r_x[16], r_y[16];
+            load_r(o.sr_colT + gcol * p.R + grow, valid, r_x);
+            load_r(o.sr_colT + (gcol + 1) * p.R + grow, valid, r_y);
+            quant32x2_sr<HAD>(v, bytex, bytey, r_x, r_y, qx, qy);
+        } else {
+            quant32x2<HAD>(v, bytex, bytey, qx, qy);
+        }
+        store_colT_pair(p.colT, p, row0, col0, cp, rb, qx, qy, bytex, bytey);
     }
 }
 

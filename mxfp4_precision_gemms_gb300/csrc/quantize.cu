@@ -35,28 +35,6 @@ constexpr int QTHREADS = 2 * TR;
 constexpr int QBLOCKS_PER_SM = 6;
 constexpr int TILE_BYTES = TR * TC * 2;  // the raw bf16 tile
 
-// Staged tile: 32-bit word index of 16-byte chunk q (0..15) of row r.  The XOR on the
-// chunk index (by q bits 2-3, row bit 0 and row bit 5) keeps the row-wise 16-byte writes
-// (8 rows x 4 segments per warp) and the column-wise 32-bit reads (rows i and 32 + i,
-// 16 column pairs each, per warp) bank-conflict free.
-__device__ __forceinline__ int bf16_chunk(int r, int q) {
-    return r * (TC / 2) + ((q ^ ((q >> 2) & 3) ^ (((r ^ (r >> 5)) & 1) << 2)) << 2);
-}
-
-// One 32-byte global store (the address must be 32-byte aligned).
-__device__ __forceinline__ void st_global_32B(void* dst, uint4 a, uint4 b) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a.x), "r"(a.y),
-                 "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
-                 : "memory");
-}
-
-// One 32-byte streaming global load (the address must be 32-byte aligned).
-__device__ __forceinline__ void ld_global_cs_32B(const void* src, uint4& a, uint4& b) {
-    asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-                 : "l"(src));
-}
-
 template <int HAD, bool ROW, bool COLT, bool TWOD>
 __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel(const QuantParams p) {
     extern __shared__ __align__(16) uint8_t q_smem[];
@@ -82,38 +60,16 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
     float2 v[32];
     {
         uint4 raw_x[4], raw_y[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) raw_x[j] = raw_y[j] = make_uint4(0, 0, 0, 0);
-        // 32-byte loads when every row segment starts on a 32-byte boundary, so that each
-        // load instruction uses whole 32-byte sectors.  Measured on 8192 x {4096, 14336}:
-        // row + transposed 5-20% faster, transposed only 2-14%, 2D unchanged; the
-        // row-only pass was 13% slower with them and keeps 16-byte loads.
-        const bool a32 = (COLT || TWOD) && ((reinterpret_cast<uintptr_t>(p.x) | (uintptr_t)(p.ld * 2)) & 31u) == 0;
-        if (vx) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.x + grx * p.ld + gc);
-            if (a32) {
-                ld_global_cs_32B(src, raw_x[0], raw_x[1]);
-                ld_global_cs_32B(src + 2, raw_x[2], raw_x[3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) raw_x[j] = __ldcs(src + j);
-            }
-        }
-        if (vy) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.x + gry * p.ld + gc);
-            if (a32) {
-                ld_global_cs_32B(src, raw_y[0], raw_y[1]);
-                ld_global_cs_32B(src + 2, raw_y[2], raw_y[3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) raw_y[j] = __ldcs(src + j);
-            }
-        }
+        // 32-byte loads (whole sectors per instruction) when the rows allow them.
+        // Measured on 8192 x {4096, 14336}: row + transposed 5-20% faster, transposed only
+        // 2-14%, 2D unchanged; the row-only pass was 13% slower with them and keeps
+        // 16-byte loads.
+        load_row_pair(p, grx, gry, gc, vx, vy, (COLT || TWOD) && rows_32B_aligned(p), raw_x, raw_y);
         if constexpr (COLT) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                *reinterpret_cast<uint4*>(&tile_w[bf16_chunk(rx, 4 * s + j)]) = raw_x[j];
-                *reinterpret_cast<uint4*>(&tile_w[bf16_chunk(ry, 4 * s + j)]) = raw_y[j];
+                *reinterpret_cast<uint4*>(&tile_w[tile_chunk(rx, 4 * s + j)]) = raw_x[j];
+                *reinterpret_cast<uint4*>(&tile_w[tile_chunk(ry, 4 * s + j)]) = raw_y[j];
             }
         }
 #pragma unroll
@@ -160,30 +116,7 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
             quant32x2<HAD>(v, bytex, bytey, qx, qy);
             if (vx) *reinterpret_cast<uint4*>(p.row.codes + grx * (p.C / 2) + gc / 2) = qx;
             if (vy) *reinterpret_cast<uint4*>(p.row.codes + gry * (p.C / 2) + gc / 2) = qy;
-            // The four segments of a row are lanes 4 pr .. 4 pr + 3 and their four bytes are
-            // consecutive (k = col0/32 + s, col0/32 a multiple of 4) in both scale orders.
-            // MMA order: one 32-bit store, rows past R and columns past C carrying byte 0
-            // into the zeroed padding.  Plain order: one 32-bit store when the row exists,
-            // all four blocks exist and the offset is 4-byte aligned, else byte stores.
-            uint32_t wx = bytex << (8 * s), wy = bytey << (8 * s);
-#pragma unroll
-            for (int o = 1; o <= 2; o <<= 1) {
-                wx |= __shfl_xor_sync(0xffffffffu, wx, o);
-                wy |= __shfl_xor_sync(0xffffffffu, wy, o);
-            }
-            const int64_t k0 = col0 / 32, kb = p.C / 32;
-            if (p.row.sf_mma) {
-                if (s == 0) {
-                    *reinterpret_cast<uint32_t*>(p.row.scales + sf_mma_offset(grx, k0, p.row.kb_pad)) = wx;
-                    *reinterpret_cast<uint32_t*>(p.row.scales + sf_mma_offset(gry, k0, p.row.kb_pad)) = wy;
-                }
-            } else if (k0 + 4 <= kb && (kb & 3) == 0) {
-                if (s == 0 && grx < p.R) *reinterpret_cast<uint32_t*>(p.row.scales + grx * kb + k0) = wx;
-                if (s == 0 && gry < p.R) *reinterpret_cast<uint32_t*>(p.row.scales + gry * kb + k0) = wy;
-            } else {
-                if (vx) store_scale(p.row, grx, gc / 32, p.C / 32, bytex);
-                if (vy) store_scale(p.row, gry, gc / 32, p.C / 32, bytey);
-            }
+            store_row_scales(p.row, p, col0, s, grx, gry, vx, vy, bytex, bytey);
         }
     }
 
@@ -198,7 +131,7 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
         const int q = cp >> 2, wi = cp & 3;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const uint32_t w = tile_w[bf16_chunk(32 * rb + i, q) + wi];
+            const uint32_t w = tile_w[tile_chunk(32 * rb + i, q) + wi];
             v[i] = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
         }
         rotate32x2<HAD>(v);
@@ -207,42 +140,7 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
         const uint32_t bytex = scale_byte(ax, p.mode), bytey = scale_byte(ay, p.mode);
         uint4 qx, qy;
         quant32x2<HAD>(v, bytex, bytey, qx, qy);
-        // row block 0 keeps output row 2 cp (its qx) and takes block 1's qx; row block 1
-        // keeps output row 2 cp + 1 (its qy) and takes block 0's qy
-        const uint4 send = rb == 0 ? qy : qx;
-        uint4 recv;
-        recv.x = __shfl_xor_sync(0xffffffffu, send.x, 16);
-        recv.y = __shfl_xor_sync(0xffffffffu, send.y, 16);
-        recv.z = __shfl_xor_sync(0xffffffffu, send.z, 16);
-        recv.w = __shfl_xor_sync(0xffffffffu, send.w, 16);
-        const uint32_t recv_b = __shfl_xor_sync(0xffffffffu, rb == 0 ? bytey : bytex, 16);
-        const uint4 lo = rb == 0 ? qx : recv, hi = rb == 0 ? recv : qy;
-        const uint32_t b0 = rb == 0 ? bytex : recv_b, b1 = rb == 0 ? recv_b : bytey;
-        const int64_t orow = col0 + 2 * cp + rb;
-        const int64_t left = (p.R - row0) / 32;
-        const int nrb = left >= 2 ? 2 : (int)left;  // valid 32-row blocks of the tile
-        if (orow < p.C && nrb > 0) {
-            uint8_t* dst = p.colT.codes + orow * (p.R / 2) + row0 / 2;
-            if (nrb == 2) {
-                if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
-                    st_global_32B(dst, lo, hi);
-                } else {
-                    reinterpret_cast<uint4*>(dst)[0] = lo;
-                    reinterpret_cast<uint4*>(dst)[1] = hi;
-                }
-            } else {
-                *reinterpret_cast<uint4*>(dst) = lo;
-            }
-            // k = row0/32 (even) and k + 1 are adjacent bytes in both scale orders
-            const int64_t off = p.colT.sf_mma ? sf_mma_offset(orow, row0 / 32, p.colT.kb_pad)
-                                              : orow * (p.R / 32) + row0 / 32;
-            if (nrb == 2 && (off & 1) == 0) {
-                *reinterpret_cast<uint16_t*>(p.colT.scales + off) = (uint16_t)(b0 | (b1 << 8));
-            } else {
-                store_scale(p.colT, orow, row0 / 32, p.R / 32, b0);
-                if (nrb == 2) store_scale(p.colT, orow, row0 / 32 + 1, p.R / 32, b1);
-            }
-        }
+        store_colT_pair(p.colT, p, row0, col0, cp, rb, qx, qy, bytex, bytey);
     }
 }
 
