@@ -73,7 +73,7 @@ __device__ __forceinline__ void load_r(const uint16_t* src, bool valid, uint32_t
 }
 
 template <int HAD, bool ROW, bool COLT, bool SR>
-__global__ void __launch_bounds__(RQ_THREADS, 4) rq_rand_kernel(const QuantParams p, const RandOpts o) {
+__global__ void __launch_bounds__(RQ_THREADS, SR ? 4 : 6) rq_rand_kernel(const QuantParams p, const RandOpts o) {
     __shared__ __align__(16) uint32_t tile[COLT ? RQ_TR * RQ_TC / 2 : 4];
     const int t = threadIdx.x;
     const int64_t row0 = (int64_t)blockIdx.y * RQ_TR, col0 = (int64_t)blockIdx.x * RQ_TC;
