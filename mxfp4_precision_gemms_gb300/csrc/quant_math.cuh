@@ -67,6 +67,39 @@ __device__ __forceinline__ void rotate32x2(float2 (&v)[32]) {
     }
 }
 
+// Stride-1 butterfly straight from a bf16 pair: w holds elements 2i (low half) and 2i + 1
+// (high half); c is element 2i + 1 widened to fp32.  The mixed-precision add / sub widen
+// the low half exactly and round once, so (s, d) equal fl32(x_2i + x_2i+1) and
+// fl32(x_2i - x_2i+1) of the unpacked values.
+__device__ __forceinline__ void bfly_lo(uint32_t w, float c, float& s, float& d) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, l, %3;\n\t}"
+        : "=f"(s), "=f"(d)
+        : "r"(w), "f"(c));
+}
+
+// rotate32x2 without its stride-1 stage (done by bfly_lo while unpacking).
+template <int HAD>
+__device__ __forceinline__ void rotate32x2_from2(float2 (&v)[32]) {
+    if constexpr (HAD > 1) {
+#pragma unroll
+        for (int s = 2; s < HAD; s <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                if ((i & s) == 0) {
+                    const float2 a = v[i], b = v[i + s];
+                    v[i] = f2_add(a, b);
+                    v[i + s] = f2_sub(a, b);
+                }
+            }
+        }
+        if constexpr (HAD == 32) {
+            const float2 c = make_float2(0.17677669529663687f, 0.17677669529663687f);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = f2_mul(v[i], c);
+        }
+    }
+}
+
 // Three-input fp32 maximum (one instruction on sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
