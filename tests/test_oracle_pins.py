@@ -297,6 +297,63 @@ def test_layouts_consistent(oracle_mod):
             assert np.array_equal(s2, sr.reshape(2, 32, 3).max(axis=1))
 
 
+def codes_2d_independent(oracle_mod, xb, had, mode):
+    """The 32x32 2D layout rebuilt from pinned pieces, not from the oracle's 2D code:
+    rotation along the columns by the canonical fp32 rotation (pinned above), one
+    exponent per 32x32 tile by the brute-force scan over the tile's amax, and every
+    element rounded by counting E2M1 midpoints in exact rationals.
+    Returns per-element codes [R, C] and the scale bytes [R/32, C/32]."""
+    R, C = xb.shape
+    v = oracle_mod.rotate_f32(synth.bf16_to_f32(xb), had)
+    codes = np.zeros((R, C), np.uint8)
+    scales = np.zeros((R // 32, C // 32), np.uint8)
+    for tr in range(R // 32):
+        for tc in range(C // 32):
+            tile = v[32 * tr:32 * tr + 32, 32 * tc:32 * tc + 32]
+            e = exponent_by_scan(Fraction(float(np.abs(tile).max())), mode)
+            scales[tr, tc] = e + 127
+            step = Fraction(2) ** e
+            for i in range(32):
+                for j in range(32):
+                    val = float(tile[i, j])
+                    codes[32 * tr + i, 32 * tc + j] = e2m1_code_by_thresholds(Fraction(val) / step,
+                                                                              math.copysign(1.0, val) < 0)
+    return codes, scales
+
+
+@pytest.mark.parametrize("had", [1, 16, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_2d_codes_by_tile_exponent(oracle_mod, had, mode):
+    """2D codes and bytes equal the independent rebuild on heavy-tailed data, and the
+    data is such that quantising each row segment with its own exponent (a plausible
+    slip) would change codes: the per-row copy differs from the 2D copy."""
+    xb = synth.heavy_tailed(64, 96, 17)
+    c2, s2 = oracle_mod.quantize(xb, had, mode, "2d")
+    want_c, want_s = codes_2d_independent(oracle_mod, xb, had, mode)
+    assert np.array_equal(s2, want_s)
+    assert np.array_equal(oracle_mod.unpack_codes(c2), want_c)
+    cr, _ = oracle_mod.quantize(xb, had, mode, "row")
+    assert (oracle_mod.unpack_codes(cr) != want_c).sum() > 100
+
+
+def load_golden_2d():
+    with open(os.path.join(GOLDEN, "quant_2d_examples.jsonl")) as f:
+        return [json.loads(l) for l in f if l.strip()]
+
+
+@pytest.mark.parametrize("case", load_golden_2d(), ids=lambda c: c["name"])
+def test_hand_worked_2d_examples(oracle_mod, case):
+    """Hand-worked 32x32 tiles (tests/golden/quant_2d_examples.jsonl, each with its why)."""
+    x = np.array([case["x_row0"]] + [case["x_other_rows"]] * 31, np.float32)
+    want = np.array([case["codes_row0"]] + [case["codes_other_rows"]] * 31, np.uint8)
+    codes, scales = oracle_mod.quantize(synth.bf16_bits(x), case["had"], case["mode"], "2d")
+    assert scales.shape == (1, 1) and int(scales[0, 0]) == case["scale"]
+    assert np.array_equal(oracle_mod.unpack_codes(codes), want)
+    # the independent rebuild agrees with the hand-worked values too
+    ic, isc = codes_2d_independent(oracle_mod, synth.bf16_bits(x), case["had"], case["mode"])
+    assert int(isc[0, 0]) == case["scale"] and np.array_equal(ic, want)
+
+
 # ---------------------------------------------------------------- error decomposition
 
 
