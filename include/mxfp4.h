@@ -141,6 +141,11 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
  * cores (QDQ numerics: "Decomposing MXFP4 quantization error", experiments).
  * A: [M, K] quantised along K, B: [N, K] quantised along K, both MXFP4_SF_MMA,
  *    same K (cols).
+ * Provenance (MXFP4_ERR_INVALID_ARG otherwise): A and B carry the same `had` and
+ *    `mode` -- the rotations cancel only when both sides of the contraction were
+ *    rotated by the same H (C.1-C.3) -- and each is a ROW or COLT copy, with a COLT
+ *    A only beside a COLT B.  The linear layer's pairs are (ROW, ROW) in Fprop,
+ *    (ROW, COLT) in Dgrad and (COLT, COLT) in Wgrad.
  * C: device, [M, N] row-major with leading dimension ldc >= N (ldc % 8 == 0,
  *    16-byte aligned), fp32 or bf16 per out_dtype.  accumulate = 1 adds to C
  *    (fp32 only).
@@ -237,7 +242,9 @@ size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp
  *    operand (needs M % 32 == 0); produced in the same pass that reads X.
  * save_wT (optional): receives W^T quantised along N, [K, N], the Dgrad operand
  *    (needs N % 32 == 0); produced in the same pass that reads W.
- * Saved tensors must be MXFP4_SF_MMA.  K % 32 == 0. */
+ * Saved tensors must be MXFP4_SF_MMA.  K % 32 == 0, N % 8 == 0 (y's leading dimension).
+ * Every argument of both quantiser passes and of the GEMM is checked before the first
+ * launch: a rejected call leaves the workspace, the saved copies and y untouched. */
 mxfp4_status mxfp4_linear_fprop(const void* x, const void* w, int64_t M, int64_t N, int64_t K,
                                 const mxfp4_config* cfg, void* y, mxfp4_tensor* save_xT, mxfp4_tensor* save_wT,
                                 void* ws, size_t ws_bytes, mxfp4_stream_t stream);
@@ -247,14 +254,19 @@ mxfp4_status mxfp4_linear_fprop(const void* x, const void* w, int64_t M, int64_t
  * mxfp4_linear_fprop's save_wT); dx: device [M, K] (ld K).  dY is rotated and
  * quantised along N (row layout) into the workspace.
  * save_dyT (optional): receives dY^T quantised along M, [N, M], the Wgrad operand
- *    (needs M % 32 == 0).  N % 32 == 0. */
+ *    (needs M % 32 == 0).  N % 32 == 0, K % 8 == 0 (dx's leading dimension).
+ * wT must be a COLT copy made under cfg's had and mode (MXFP4_ERR_INVALID_ARG
+ * otherwise): W's row copy has the same shape when W is square, and a copy under
+ * another rotation would not cancel.  Everything is checked before the first launch. */
 mxfp4_status mxfp4_linear_dgrad(const void* dy, const mxfp4_tensor* wT, int64_t M, int64_t N, int64_t K,
                                 const mxfp4_config* cfg, void* dx, mxfp4_tensor* save_dyT, void* ws,
                                 size_t ws_bytes, mxfp4_stream_t stream);
 
 /* Wgrad dW = dY^T X ("Pretraining ... Native FP4 Hardware", C.3), contraction over
  * the M tokens.  dyT: [N, M], xT: [K, M] (both quantised along M, MMA scales);
- * dw: device [N, K] (ld K) in cfg->out_dtype; cfg->accumulate adds to dw. */
+ * dw: device [N, K] (ld K) in cfg->out_dtype; cfg->accumulate adds to dw.
+ * dyT and xT must both be COLT copies made under cfg's had and mode
+ * (MXFP4_ERR_INVALID_ARG otherwise). */
 mxfp4_status mxfp4_linear_wgrad(const mxfp4_tensor* dyT, const mxfp4_tensor* xT, const mxfp4_config* cfg,
                                 void* dw, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
 
@@ -268,8 +280,13 @@ mxfp4_status mxfp4_linear_wgrad(const mxfp4_tensor* dyT, const mxfp4_tensor* xT,
  * (mxfp4_noalloc_scratch_bytes()), which every GPU running this library holds until
  * the process exits.  Shapes whose mxfp4_workspace_bytes(MXFP4_OP_FPROP, ...) exceed
  * it are rejected with MXFP4_ERR_WORKSPACE before anything is launched.
- * The first call on a device looks up the scratch area's device address (a CUDA
- * runtime query, no allocation); make that first call before any stream capture.
+ * The 64 MiB is reserved by the CUDA driver when the library's device code is loaded
+ * on a device: at library load under eager module loading, or -- under the default
+ * lazy loading -- on this entry point's first call on that device, which also looks
+ * up the area's device address.  That first call can therefore fail with
+ * MXFP4_ERR_CUDA (out of memory) or synchronise the device: make it at
+ * initialisation, before the caller's allocator reserves the device's memory and
+ * before any stream capture.
  * All calls share the one area and it keeps the previous call's contents (every
  * byte this path reads is rewritten first); calls that may overlap on the GPU (for
  * example on two streams without ordering) race on it and must be serialised.

@@ -191,12 +191,14 @@ def sf_plain_to_mma(plain: np.ndarray, rows: int, cols: int) -> np.ndarray:
 
 
 def qtensor_from_host(codes: np.ndarray, plain_scales: np.ndarray, layout: int = LAYOUT_ROW,
-                      device="cuda") -> QTensor:
-    """Uploads host codes [rows, cols/2] and plain scales [rows, cols/32] as an MMA-order QTensor."""
+                      device="cuda", had: int = HAD_NONE, mode: int = SCALE_FLOOR) -> QTensor:
+    """Uploads host codes [rows, cols/2] and plain scales [rows, cols/32] as an MMA-order
+    QTensor; had / mode record how they were produced (the GEMM requires both operands
+    to agree)."""
     rows, cols = codes.shape[0], codes.shape[1] * 2
     c = torch.from_numpy(np.ascontiguousarray(codes)).to(device)
     s = torch.from_numpy(sf_plain_to_mma(plain_scales, rows, cols)).to(device)
-    return QTensor(c, s, rows, cols, layout, SF_MMA)
+    return QTensor(c, s, rows, cols, layout, SF_MMA, had, mode)
 
 
 # ----------------------------------------------------------------- entry points

@@ -206,6 +206,10 @@ mxfp4_status check_gemm_operand(const mxfp4_tensor* t, const char* name) {
     if (t->sf_layout != MXFP4_SF_MMA) return fail(MXFP4_ERR_INVALID_ARG, "%s: GEMM operands need MMA scales", name);
     if (t->layout == MXFP4_LAYOUT_2D)
         return fail(MXFP4_ERR_INVALID_ARG, "%s: 2D-layout tensors cannot feed the GEMM", name);
+    if (t->layout != MXFP4_LAYOUT_ROW && t->layout != MXFP4_LAYOUT_COLT)
+        return fail(MXFP4_ERR_INVALID_ARG, "%s: bad layout %d", name, t->layout);
+    if (!valid_had(t->had) || !valid_mode(t->mode))
+        return fail(MXFP4_ERR_INVALID_ARG, "%s: bad had %d / mode %d", name, t->had, t->mode);
     if (t->rows <= 0 || t->cols <= 0) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "%s: empty", name);
     if (t->cols % 32 != 0) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "%s: cols %% 32 != 0", name);
     if (t->rows > (int64_t)INT32_MAX || t->cols / 2 > (int64_t)INT32_MAX)
@@ -280,9 +284,24 @@ mxfp4_status mxfp4_device_status(mxfp4_stream_t stream) {
     return ok();
 }
 
-mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
-                                   unsigned layouts, mxfp4_tensor* row_out, mxfp4_tensor* colT_out,
-                                   mxfp4_tensor* twoD_out, mxfp4_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+void fill_desc(mxfp4_tensor* t, int64_t r, int64_t c, int layout, int had, int mode) {
+    t->rows = r;
+    t->cols = c;
+    t->layout = layout;
+    t->had = had;
+    t->mode = mode;
+}
+
+// Every check of a rotate+quantise call, with no CUDA call: nothing is touched or
+// launched.  *empty: the problem has no elements (no pointer is used).
+mxfp4_status rq_validate(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode, unsigned layouts,
+                         const mxfp4_tensor* row_out, const mxfp4_tensor* colT_out, const mxfp4_tensor* twoD_out,
+                         bool* empty) {
+    *empty = false;
     if (rows < 0 || cols < 0) return fail(MXFP4_ERR_INVALID_ARG, "negative size");
     if (!valid_had(had)) return fail(MXFP4_ERR_INVALID_ARG, "hadamard must be 0, 16 or 32 (got %d)", had);
     if (!valid_mode(mode)) return fail(MXFP4_ERR_INVALID_ARG, "scale mode must be 0 or 1 (got %d)", mode);
@@ -297,18 +316,9 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
                     (long long)rows);
     if ((want_row && !row_out) || (want_colT && !colT_out) || (want_2d && !twoD_out))
         return fail(MXFP4_ERR_INVALID_ARG, "a requested output descriptor is NULL");
-    auto fill = [&](mxfp4_tensor* t, int64_t r, int64_t c, int layout) {
-        t->rows = r;
-        t->cols = c;
-        t->layout = layout;
-        t->had = had;
-        t->mode = mode;
-    };
-    if (rows == 0 || cols == 0) {  // nothing to read or write: no pointer is used
-        if (want_row) fill(row_out, rows, cols, MXFP4_LAYOUT_ROW);
-        if (want_colT) fill(colT_out, cols, rows, MXFP4_LAYOUT_COLT);
-        if (want_2d) fill(twoD_out, rows, cols, MXFP4_LAYOUT_2D);
-        return ok();
+    if (rows == 0 || cols == 0) {
+        *empty = true;
+        return MXFP4_OK;
     }
     if (!x) return fail(MXFP4_ERR_INVALID_ARG, "x is NULL");
     if (ld < cols || ld % 8)
@@ -319,14 +329,18 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
     if (want_row && (st = check_out(row_out, "row_out", true))) return st;
     if (want_colT && (st = check_out(colT_out, "colT_out", true))) return st;
     if (want_2d && (st = check_out(twoD_out, "twoD_out", false))) return st;
-    int dev;
-    if ((st = check_device(&dev))) return st;
+    return MXFP4_OK;
+}
 
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (want_row) fill(row_out, rows, cols, MXFP4_LAYOUT_ROW);
-    if (want_colT) fill(colT_out, cols, rows, MXFP4_LAYOUT_COLT);
-    if (want_2d) fill(twoD_out, rows, cols, MXFP4_LAYOUT_2D);
-
+// Fills the descriptors of a validated, non-empty rotate+quantise call on a checked
+// device, clears MMA scale padding and launches the kernel.
+mxfp4_status rq_launch(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode, unsigned layouts,
+                       mxfp4_tensor* row_out, mxfp4_tensor* colT_out, mxfp4_tensor* twoD_out, cudaStream_t s) {
+    const bool want_row = layouts & MXFP4_LAYOUT_ROW, want_colT = layouts & MXFP4_LAYOUT_COLT,
+               want_2d = layouts & MXFP4_LAYOUT_2D;
+    if (want_row) fill_desc(row_out, rows, cols, MXFP4_LAYOUT_ROW, had, mode);
+    if (want_colT) fill_desc(colT_out, cols, rows, MXFP4_LAYOUT_COLT, had, mode);
+    if (want_2d) fill_desc(twoD_out, rows, cols, MXFP4_LAYOUT_2D, had, mode);
     for (mxfp4_tensor* t : {want_row ? row_out : nullptr, want_colT ? colT_out : nullptr}) {
         if (needs_sf_padding(t)) {
             cudaError_t e =
@@ -346,6 +360,28 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
     cudaError_t e = launch_rotate_quantize(p, had, layouts, s);
     if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize launch");
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                   unsigned layouts, mxfp4_tensor* row_out, mxfp4_tensor* colT_out,
+                                   mxfp4_tensor* twoD_out, mxfp4_stream_t stream) {
+    bool empty;
+    mxfp4_status st = rq_validate(x, rows, cols, ld, had, mode, layouts, row_out, colT_out, twoD_out, &empty);
+    if (st) return st;
+    if (empty) {  // nothing to read or write: no pointer is used
+        if (layouts & MXFP4_LAYOUT_ROW) fill_desc(row_out, rows, cols, MXFP4_LAYOUT_ROW, had, mode);
+        if (layouts & MXFP4_LAYOUT_COLT) fill_desc(colT_out, cols, rows, MXFP4_LAYOUT_COLT, had, mode);
+        if (layouts & MXFP4_LAYOUT_2D) fill_desc(twoD_out, rows, cols, MXFP4_LAYOUT_2D, had, mode);
+        return ok();
+    }
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    return rq_launch(x, rows, cols, ld, had, mode, layouts, row_out, colT_out, twoD_out,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 namespace {
@@ -500,15 +536,30 @@ mxfp4_status mxfp4_rotate_quantize_ex(const void* x, int64_t rows, int64_t cols,
     return ok();
 }
 
-mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, int64_t ldc, int out_dtype,
-                        int accumulate, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
-    (void)ws;
-    (void)ws_bytes;
+}  // extern "C"
+
+namespace {
+
+// Every check of a GEMM call C = A . B^T, with no CUDA call.  Beyond shapes and
+// pointers: both operands must come from the same rotation and scale rule (the
+// rotations cancel only when both sides of the contraction carry the same H,
+// "Pretraining ... Native FP4 Hardware" C.1-C.3), and a transposed copy on the A side
+// needs one on the B side too: the linear layer's GEMMs pair (row, row) in Fprop,
+// (row, transposed) in Dgrad and (transposed, transposed) in Wgrad.
+mxfp4_status gemm_validate(const mxfp4_tensor* A, const mxfp4_tensor* B, const void* C, int64_t ldc, int out_dtype,
+                           int accumulate) {
     mxfp4_status st;
     if ((st = check_gemm_operand(A, "A")) || (st = check_gemm_operand(B, "B"))) return st;
     if (A->cols != B->cols)
         return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "contraction mismatch: A cols %lld, B cols %lld", (long long)A->cols,
                     (long long)B->cols);
+    if (A->had != B->had || A->mode != B->mode)
+        return fail(MXFP4_ERR_INVALID_ARG,
+                    "A (had %d, mode %d) and B (had %d, mode %d) were quantised differently: the rotations cancel "
+                    "only under the same Hadamard and scale rule",
+                    A->had, A->mode, B->had, B->mode);
+    if (A->layout == MXFP4_LAYOUT_COLT && B->layout != MXFP4_LAYOUT_COLT)
+        return fail(MXFP4_ERR_INVALID_ARG, "A is a transposed copy but B is not (Wgrad takes two transposed copies)");
     if (!C) return fail(MXFP4_ERR_INVALID_ARG, "C is NULL");
     if (out_dtype != MXFP4_OUT_F32 && out_dtype != MXFP4_OUT_BF16)
         return fail(MXFP4_ERR_INVALID_ARG, "bad out_dtype %d", out_dtype);
@@ -516,34 +567,60 @@ mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, i
     if (ldc < B->rows || ldc % 8)
         return fail(MXFP4_ERR_MISALIGNED, "ldc (%lld) must be >= N and a multiple of 8", (long long)ldc);
     if (!aligned16(C)) return fail(MXFP4_ERR_MISALIGNED, "C not 16-byte aligned");
-    int dev;
-    if ((st = check_device(&dev))) return st;
+    return MXFP4_OK;
+}
 
-    GemmParams p{};
-    if (!encode_codes_map(&p.map_a, A->codes, A->rows, A->cols, 128) ||
-        !encode_codes_map(&p.map_b, B->codes, B->rows, B->cols, 128) ||
-        !encode_out_map(&p.map_c, C, A->rows, B->rows, ldc, out_dtype == MXFP4_OUT_BF16) ||
-        !encode_sf_map(&p.map_sfa, A->scales, A->rows, A->cols) || !encode_sf_map(&p.map_sfb, B->scales, B->rows, B->cols))
+// Encodes the tensor maps and fills the kernel parameters of a validated GEMM (a
+// driver call, no launch).
+mxfp4_status gemm_prepare(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, int64_t ldc, int out_dtype,
+                          int accumulate, GemmParams* p) {
+    *p = GemmParams{};
+    if (!encode_codes_map(&p->map_a, A->codes, A->rows, A->cols, 128) ||
+        !encode_codes_map(&p->map_b, B->codes, B->rows, B->cols, 128) ||
+        !encode_out_map(&p->map_c, C, A->rows, B->rows, ldc, out_dtype == MXFP4_OUT_BF16) ||
+        !encode_sf_map(&p->map_sfa, A->scales, A->rows, A->cols) ||
+        !encode_sf_map(&p->map_sfb, B->scales, B->rows, B->cols))
         return fail(MXFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    p.sfa = A->scales;
-    p.sfb = B->scales;
-    p.M = A->rows;
-    p.N = B->rows;
-    p.K = A->cols;
-    p.kb_pad = sf_kb_pad(A->cols);
-    p.C = C;
-    p.ldc = ldc;
-    p.out_bf16 = out_dtype == MXFP4_OUT_BF16;
-    p.accumulate = accumulate ? 1 : 0;
+    p->sfa = A->scales;
+    p->sfb = B->scales;
+    p->M = A->rows;
+    p->N = B->rows;
+    p->K = A->cols;
+    p->kb_pad = sf_kb_pad(A->cols);
+    p->C = C;
+    p->ldc = ldc;
+    p->out_bf16 = out_dtype == MXFP4_OUT_BF16;
+    p->accumulate = accumulate ? 1 : 0;
+    return MXFP4_OK;
+}
+
+mxfp4_status gemm_launch(GemmParams& p, cudaStream_t s) {
     p.status = device_status_ptr();
     p.wait_ns = wait_limit();
     if (t_inject_gemm_faults > 0) {
         --t_inject_gemm_faults;
         p.test_drop_first_stage = 1;
     }
-    cudaError_t e = launch_gemm(p, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_gemm(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, int64_t ldc, int out_dtype,
+                        int accumulate, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    mxfp4_status st;
+    if ((st = gemm_validate(A, B, C, ldc, out_dtype, accumulate))) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    GemmParams p;
+    if ((st = gemm_prepare(A, B, C, ldc, out_dtype, accumulate, &p))) return st;
+    return gemm_launch(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
@@ -635,6 +712,8 @@ extern "C" {
 mxfp4_status mxfp4_linear_fprop(const void* x, const void* w, int64_t M, int64_t N, int64_t K,
                                 const mxfp4_config* cfg, void* y, mxfp4_tensor* save_xT, mxfp4_tensor* save_wT,
                                 void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
+    // Every argument is checked (and the GEMM's tensor maps encoded) before the first
+    // launch, so a rejected call leaves the workspace, the saved copies and y untouched.
     mxfp4_status st;
     if ((st = check_cfg(cfg))) return st;
     if (!x || !w || !y) return fail(MXFP4_ERR_INVALID_ARG, "x, w and y must be non-NULL");
@@ -645,15 +724,23 @@ mxfp4_status mxfp4_linear_fprop(const void* x, const void* w, int64_t M, int64_t
     if ((st = check_ws(ws, ws_bytes, mxfp4_workspace_bytes(MXFP4_OP_FPROP, M, N, K, cfg)))) return st;
     uint8_t* cur = static_cast<uint8_t*>(ws);
     mxfp4_tensor xq = carve(cur, M, K), wq = carve(cur, N, K);
-    if ((st = mxfp4_rotate_quantize(x, M, K, K, cfg->had, cfg->mode,
-                                    MXFP4_LAYOUT_ROW | (save_xT ? MXFP4_LAYOUT_COLT : 0), &xq, save_xT, nullptr,
-                                    stream)))
-        return st;
-    if ((st = mxfp4_rotate_quantize(w, N, K, K, cfg->had, cfg->mode,
-                                    MXFP4_LAYOUT_ROW | (save_wT ? MXFP4_LAYOUT_COLT : 0), &wq, save_wT, nullptr,
-                                    stream)))
-        return st;
-    return mxfp4_gemm(&xq, &wq, y, N, cfg->out_dtype, cfg->accumulate, nullptr, 0, stream);
+    const unsigned lx = MXFP4_LAYOUT_ROW | (save_xT ? MXFP4_LAYOUT_COLT : 0);
+    const unsigned lw = MXFP4_LAYOUT_ROW | (save_wT ? MXFP4_LAYOUT_COLT : 0);
+    bool empty;
+    if ((st = rq_validate(x, M, K, K, cfg->had, cfg->mode, lx, &xq, save_xT, nullptr, &empty))) return st;
+    if ((st = rq_validate(w, N, K, K, cfg->had, cfg->mode, lw, &wq, save_wT, nullptr, &empty))) return st;
+    // the GEMM operands as the two passes will describe them
+    fill_desc(&xq, M, K, MXFP4_LAYOUT_ROW, cfg->had, cfg->mode);
+    fill_desc(&wq, N, K, MXFP4_LAYOUT_ROW, cfg->had, cfg->mode);
+    if ((st = gemm_validate(&xq, &wq, y, N, cfg->out_dtype, cfg->accumulate))) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    GemmParams gp;
+    if ((st = gemm_prepare(&xq, &wq, y, N, cfg->out_dtype, cfg->accumulate, &gp))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = rq_launch(x, M, K, K, cfg->had, cfg->mode, lx, &xq, save_xT, nullptr, s))) return st;
+    if ((st = rq_launch(w, N, K, K, cfg->had, cfg->mode, lw, &wq, save_wT, nullptr, s))) return st;
+    return gemm_launch(gp, s);
 }
 
 mxfp4_status mxfp4_linear_dgrad(const void* dy, const mxfp4_tensor* wT, int64_t M, int64_t N, int64_t K,
@@ -666,16 +753,28 @@ mxfp4_status mxfp4_linear_dgrad(const void* dy, const mxfp4_tensor* wT, int64_t 
     if (N % 32) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "N %% 32 != 0");
     if (wT->rows != K || wT->cols != N)
         return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "wT must be [K, N] = [%lld, %lld]", (long long)K, (long long)N);
+    if (wT->layout != MXFP4_LAYOUT_COLT)
+        return fail(MXFP4_ERR_INVALID_ARG, "wT must be the transposed copy of W (quantised along N)");
+    if (wT->had != cfg->had || wT->mode != cfg->mode)
+        return fail(MXFP4_ERR_INVALID_ARG, "wT was quantised with had %d / mode %d, the layer uses had %d / mode %d",
+                    wT->had, wT->mode, cfg->had, cfg->mode);
     if (save_dyT && save_dyT->sf_layout != MXFP4_SF_MMA)
         return fail(MXFP4_ERR_INVALID_ARG, "save_dyT needs MMA scales");
     if ((st = check_ws(ws, ws_bytes, mxfp4_workspace_bytes(MXFP4_OP_DGRAD, M, N, K, cfg)))) return st;
     uint8_t* cur = static_cast<uint8_t*>(ws);
     mxfp4_tensor dyq = carve(cur, M, N);
-    if ((st = mxfp4_rotate_quantize(dy, M, N, N, cfg->had, cfg->mode,
-                                    MXFP4_LAYOUT_ROW | (save_dyT ? MXFP4_LAYOUT_COLT : 0), &dyq, save_dyT, nullptr,
-                                    stream)))
-        return st;
-    return mxfp4_gemm(&dyq, wT, dx, K, cfg->out_dtype, cfg->accumulate, nullptr, 0, stream);
+    const unsigned ld_ = MXFP4_LAYOUT_ROW | (save_dyT ? MXFP4_LAYOUT_COLT : 0);
+    bool empty;
+    if ((st = rq_validate(dy, M, N, N, cfg->had, cfg->mode, ld_, &dyq, save_dyT, nullptr, &empty))) return st;
+    fill_desc(&dyq, M, N, MXFP4_LAYOUT_ROW, cfg->had, cfg->mode);
+    if ((st = gemm_validate(&dyq, wT, dx, K, cfg->out_dtype, cfg->accumulate))) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    GemmParams gp;
+    if ((st = gemm_prepare(&dyq, wT, dx, K, cfg->out_dtype, cfg->accumulate, &gp))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = rq_launch(dy, M, N, N, cfg->had, cfg->mode, ld_, &dyq, save_dyT, nullptr, s))) return st;
+    return gemm_launch(gp, s);
 }
 
 mxfp4_status mxfp4_linear_wgrad(const mxfp4_tensor* dyT, const mxfp4_tensor* xT, const mxfp4_config* cfg,
@@ -684,6 +783,12 @@ mxfp4_status mxfp4_linear_wgrad(const mxfp4_tensor* dyT, const mxfp4_tensor* xT,
     if ((st = check_cfg(cfg))) return st;
     if (!dyT || !xT || !dw) return fail(MXFP4_ERR_INVALID_ARG, "dyT, xT and dw must be non-NULL");
     if (dyT->cols != xT->cols) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "dyT and xT must share the token dim");
+    if (dyT->layout != MXFP4_LAYOUT_COLT || xT->layout != MXFP4_LAYOUT_COLT)
+        return fail(MXFP4_ERR_INVALID_ARG, "dyT and xT must be transposed copies (quantised along the tokens)");
+    if (dyT->had != cfg->had || dyT->mode != cfg->mode || xT->had != cfg->had || xT->mode != cfg->mode)
+        return fail(MXFP4_ERR_INVALID_ARG,
+                    "dyT (had %d, mode %d) and xT (had %d, mode %d) must both match the layer's had %d / mode %d",
+                    dyT->had, dyT->mode, xT->had, xT->mode, cfg->had, cfg->mode);
     return mxfp4_gemm(dyT, xT, dw, xT->rows, cfg->out_dtype, cfg->accumulate, ws, ws_bytes, stream);
 }
 

@@ -40,8 +40,14 @@ def test_buffer_sizes(L):
     assert mx.workspace_bytes(mx.OP_WGRAD, 8192, 6144, 4096, cfg) == 0
 
 
-def _tensor(codes=0x1000, scales=0x2000, rows=128, cols=256, layout=1, sf=1):
-    return mx.MxTensorC(codes, scales, rows, cols, layout, sf, 16, 0)
+def _tensor(codes=0x1000, scales=0x2000, rows=128, cols=256, layout=1, sf=1, had=16, mode=0):
+    return mx.MxTensorC(codes, scales, rows, cols, layout, sf, had, mode)
+
+
+# With no GPU in this process, any call that gets past validation reaches its first CUDA
+# call (the device check) and returns MXFP4_ERR_CUDA.  A validation status therefore
+# shows that the call returned before touching CUDA, i.e. before any launch.
+PASSED_VALIDATION = 5
 
 
 def _rq(L, x=0x1000, rows=64, cols=64, ld=64, had=16, mode=0, layouts=1, row=None, colT=None, twoD=None):
@@ -124,6 +130,25 @@ def test_gemm_rejects_bad_arguments(L):
     assert g(a, b, ldc=64) == 3                          # ldc < N
     assert g(a, _tensor(layout=4)) == 1                  # 2D operand
     assert g(_tensor(cols=48), _tensor(cols=48)) == 2    # cols % 32
+    assert g(a, b) == PASSED_VALIDATION
+
+
+def test_gemm_rejects_operands_of_different_provenance(L):
+    """The rotations cancel only when both operands carry the same Hadamard (and scale
+    rule); a transposed copy on the A side needs a transposed B (Wgrad)."""
+    c = ctypes.c_void_p(0x4000)
+    g = lambda A, B: L.mxfp4_gemm(ctypes.byref(A), ctypes.byref(B), c, 128, 0, 0, None, 0, None)
+    row, colT = dict(layout=mx.LAYOUT_ROW), dict(layout=mx.LAYOUT_COLT)
+    assert g(_tensor(had=16), _tensor(had=32)) == 1      # H16 against H32: no cancellation
+    assert g(_tensor(had=16), _tensor(had=0)) == 1
+    assert g(_tensor(mode=0), _tensor(mode=1)) == 1      # floor against ceiling scales
+    assert b"quantised differently" in L.mxfp4_last_error()
+    assert g(_tensor(had=8), _tensor(had=8)) == 1        # not a rotation this library makes
+    assert g(_tensor(mode=5), _tensor(mode=5)) == 1
+    assert g(_tensor(layout=3), _tensor(layout=3)) == 1  # not one layout
+    assert g(_tensor(**colT), _tensor(**row)) == 1       # transposed A with a row-copy B
+    for A, B in ((row, row), (row, colT), (colT, colT)):  # Fprop, Dgrad, Wgrad pairs
+        assert g(_tensor(**A), _tensor(**B)) == PASSED_VALIDATION
 
 
 def test_linear_rejects_bad_arguments(L):
@@ -141,6 +166,57 @@ def test_linear_rejects_bad_arguments(L):
     wT = _tensor(rows=64, cols=96)
     assert L.mxfp4_linear_dgrad(P(0x1000), ctypes.byref(wT), 64, 64, 64, ctypes.byref(cfg), P(0x3000), None,
                                 P(0x10000), 1 << 40, None) == 2  # wT shape mismatch
+
+
+def test_fprop_validates_both_operands_before_any_launch(L):
+    """Fprop quantises X, then W, then multiplies: a bad W, saved copy or output must be
+    rejected before X's pass is queued (the old order launched it first)."""
+    P = ctypes.c_void_p
+    cfg, bf16_acc = mx.MxConfigC(16, 0, 0, 0), mx.MxConfigC(16, 0, 1, 1)
+
+    def f(M=128, N=256, K=256, x=0x1000, w=0x2000, y=0x3000, c=cfg, xT=None, wT=None):
+        return L.mxfp4_linear_fprop(P(x), P(w), M, N, K, ctypes.byref(c), P(y), ctypes.byref(xT) if xT else None,
+                                    ctypes.byref(wT) if wT else None, P(0x100000), 1 << 40, None)
+    xT, wT = _tensor(rows=256, cols=128, layout=2), _tensor(rows=256, cols=256, layout=2)
+    assert f(xT=xT, wT=wT) == PASSED_VALIDATION
+    assert f(w=0x2008) == 3                              # misaligned W
+    assert f(y=0x3004) == 3                              # misaligned Y
+    assert f(N=100) == 3                                 # ldc = N not a multiple of 8
+    assert f(N=200, wT=wT) == 2                          # W^T copy needs N % 32 == 0
+    assert f(M=100, xT=xT) == 2                          # X^T copy needs M % 32 == 0
+    assert f(wT=_tensor(codes=0x5004, layout=2)) == 3    # misaligned saved copy
+    assert f(xT=_tensor(scales=0, layout=2)) == 1        # saved copy without scales
+    assert f(c=bf16_acc) == 1                            # accumulate needs fp32 output
+
+
+def test_dgrad_and_wgrad_check_operand_roles(L):
+    """W^T must be the transposed copy under the layer's rotation and scale rule, and
+    Wgrad takes two transposed copies under it: a row copy of a square W, or an H32 copy
+    in an H16 layer, would give a silently wrong product."""
+    P = ctypes.c_void_p
+    cfg = mx.MxConfigC(16, 0, 1, 0)
+
+    def d(wT, M=256, dy=0x1000, dx=0x3000, dyT=None):
+        return L.mxfp4_linear_dgrad(P(dy), ctypes.byref(wT), M, 256, 256, ctypes.byref(cfg), P(dx),
+                                    ctypes.byref(dyT) if dyT else None, P(0x100000), 1 << 40, None)
+    good = dict(rows=256, cols=256, layout=mx.LAYOUT_COLT)
+    assert d(_tensor(**good)) == PASSED_VALIDATION
+    assert d(_tensor(**{**good, "layout": mx.LAYOUT_ROW})) == 1   # W's row copy (square W)
+    assert d(_tensor(**good, had=32)) == 1                       # H32 copy in an H16 layer
+    assert d(_tensor(**good, mode=1)) == 1
+    assert d(_tensor(**good), dy=0x1008) == 3                    # misaligned dY
+    assert d(_tensor(**good), dx=0x3004) == 3                    # misaligned dX
+    assert d(_tensor(**good), M=100, dyT=_tensor(rows=256, cols=100, layout=2)) == 2  # dY^T needs M % 32
+
+    wcfg = mx.MxConfigC(16, 0, 0, 0)
+    w = lambda a, b, c=wcfg: L.mxfp4_linear_wgrad(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), P(0x3000),
+                                                  None, 0, None)
+    colT = dict(rows=256, cols=512, layout=mx.LAYOUT_COLT)
+    assert w(_tensor(**colT), _tensor(**colT)) == PASSED_VALIDATION
+    assert w(_tensor(**{**colT, "layout": mx.LAYOUT_ROW}), _tensor(**colT)) == 1
+    assert w(_tensor(**colT), _tensor(**{**colT, "layout": mx.LAYOUT_ROW})) == 1
+    assert w(_tensor(**colT, had=0), _tensor(**colT, had=0)) == 1  # both H-less in an H16 layer
+    assert w(_tensor(**colT), _tensor(**colT), c=mx.MxConfigC(32, 0, 0, 0)) == 1
 
 
 def test_status_strings(L):

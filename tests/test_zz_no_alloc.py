@@ -5,8 +5,10 @@ host framework owns all device memory, or loops that must not call cudaMalloc --
 by running Fprop on a fixed scratch area inside the library.  Here it is called
 through the C ABI twice in a row (different inputs, so stale scratch from the
 first call would show) and compared with mxfp4_linear_fprop using a caller
-workspace, within the 1e-5 * sum|a||b| tolerance of the other GPU tests.  This
-file is collected last on purpose."""
+workspace: both run the same kernels, so Y and all four saved arrays (codes and
+scales of X^T and W^T) must match byte for byte; Y is also within the 1e-5 *
+sum|a||b| tolerance of the oracle, as in the other GPU tests.  This file is
+collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -42,10 +44,12 @@ def test_noalloc_fprop_matches_workspace_fprop():
         assert st == 0, L.mxfp4_last_error()
         torch.cuda.synchronize()
         assert mx.device_status() == 0
-        _, S = oracle.fprop(X, W, 16, 0)
-        assert_within(y.double().cpu().numpy(), y_ref.double().cpu().numpy(), S, what=f"noalloc call {call}")
-        assert np.array_equal(xT.codes.cpu().numpy(), xT_ref.codes.cpu().numpy())
-        assert np.array_equal(wT.scales.cpu().numpy(), wT_ref.scales.cpu().numpy())
+        want, S = oracle.fprop(X, W, 16, 0)
+        assert torch.equal(y, y_ref), f"noalloc call {call}: Y differs from the workspace path"
+        assert_within(y.double().cpu().numpy(), want, S, what=f"noalloc call {call}")
+        for name, got, ref in (("xT codes", xT.codes, xT_ref.codes), ("xT scales", xT.scales, xT_ref.scales),
+                               ("wT codes", wT.codes, wT_ref.codes), ("wT scales", wT.scales, wT_ref.scales)):
+            assert np.array_equal(got.cpu().numpy(), ref.cpu().numpy()), f"noalloc call {call}: {name}"
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
