@@ -211,34 +211,51 @@ class Layer:
         self.gemm_flops = 3 * 2 * M * N * K
 
 
-def run_step(layers, ev=None, aux=None):
-    """One pass of the hot path.  If `ev` is a list, CUDA events are recorded around
-    every kernel launch: ev gets (kind, start, end, work) tuples.  If `aux` is a second
-    CUDA stream, each linear layer's independent launches run on two branches: the X
-    and W quantisations (both feed Fprop), then Dgrad and Wgrad (both need only the dY
-    quantisation and the saved transposed copies).  The layers stay in order: a layer
-    starts once both branches of the previous one have finished."""
+def run_step(layers, ev=None, aux=None, had=16, pair=True, group=True):
+    """One pass of the hot path under rotation `had` (16: H16, 32: H32, 0: none): per
+    linear, X and W rotated and quantised (row and transposed copies) -- in one launch
+    when `pair`, else two -- then Fprop; dY quantised, then Dgrad and Wgrad -- in one
+    grouped launch when `group`, else two.  If `ev` is a list, CUDA events are recorded
+    around every kernel launch: ev gets (kind, start, end, work) tuples.  If `aux` is a
+    second CUDA stream, the launches that are independent run on two branches (without
+    `pair`, the X quantisation beside W's; without `group`, Dgrad beside Wgrad).  The
+    layers stay in order: a layer starts once both branches of the previous one have
+    finished."""
     import torch
 
     from mxfp4_precision_gemms_gb300 import binding as mx
 
+    H = had
+    RC = mx.LAYOUT_ROW | mx.LAYOUT_COLT
+
+    def quant_xw(L):
+        mx.rotate_quantize_pair(L.x, L.w, H, mx.SCALE_FLOOR, RC, outs_a={"row": L.xq, "colT": L.xT},
+                                outs_b={"row": L.wq, "colT": L.wT})
+
+    def backward_group(L):
+        mx.gemm_group([(L.dyq, L.wT, mx.OUT_BF16, False, L.dx), (L.dyT, L.xT, mx.OUT_F32, False, L.dw)])
+
     if aux is not None:
         main = torch.cuda.current_stream()
-        RC = mx.LAYOUT_ROW | mx.LAYOUT_COLT
         for L in layers:
-            M, N, K = T_TOKENS, L.N, L.K
             aux.wait_stream(main)
-            mx.rotate_quantize(L.x, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.xq, "colT": L.xT})
-            with torch.cuda.stream(aux):
-                mx.rotate_quantize(L.w, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.wq, "colT": L.wT})
-            main.wait_stream(aux)
+            if pair:
+                quant_xw(L)
+            else:
+                mx.rotate_quantize(L.x, H, mx.SCALE_FLOOR, RC, outs={"row": L.xq, "colT": L.xT})
+                with torch.cuda.stream(aux):
+                    mx.rotate_quantize(L.w, H, mx.SCALE_FLOOR, RC, outs={"row": L.wq, "colT": L.wT})
+                main.wait_stream(aux)
             mx.gemm(L.xq, L.wq, mx.OUT_BF16, out=L.y)
-            mx.rotate_quantize(L.dy, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.dyq, "colT": L.dyT})
-            aux.wait_stream(main)
-            with torch.cuda.stream(aux):
-                mx.gemm(L.dyT, L.xT, mx.OUT_F32, out=L.dw)
-            mx.gemm(L.dyq, L.wT, mx.OUT_BF16, out=L.dx)
-            main.wait_stream(aux)
+            mx.rotate_quantize(L.dy, H, mx.SCALE_FLOOR, RC, outs={"row": L.dyq, "colT": L.dyT})
+            if group:
+                backward_group(L)
+            else:
+                aux.wait_stream(main)
+                with torch.cuda.stream(aux):
+                    mx.gemm(L.dyT, L.xT, mx.OUT_F32, out=L.dw)
+                mx.gemm(L.dyq, L.wT, mx.OUT_BF16, out=L.dx)
+                main.wait_stream(aux)
         return
 
     def timed(kind, work, fn):
@@ -251,26 +268,34 @@ def run_step(layers, ev=None, aux=None):
         b.record()
         ev.append((kind, a, b, work))
 
-    RC = mx.LAYOUT_ROW | mx.LAYOUT_COLT
     for L in layers:
         M, N, K = T_TOKENS, L.N, L.K
-        timed("quant", quant_bytes(M, K, True), lambda: mx.rotate_quantize(
-            L.x, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.xq, "colT": L.xT}))
-        timed("quant", quant_bytes(N, K, True), lambda: mx.rotate_quantize(
-            L.w, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.wq, "colT": L.wT}))
+        if pair:
+            timed("quant", quant_bytes(M, K, True) + quant_bytes(N, K, True), lambda: quant_xw(L))
+        else:
+            timed("quant", quant_bytes(M, K, True), lambda: mx.rotate_quantize(
+                L.x, H, mx.SCALE_FLOOR, RC, outs={"row": L.xq, "colT": L.xT}))
+            timed("quant", quant_bytes(N, K, True), lambda: mx.rotate_quantize(
+                L.w, H, mx.SCALE_FLOOR, RC, outs={"row": L.wq, "colT": L.wT}))
         timed("gemm", 2 * M * N * K, lambda: mx.gemm(L.xq, L.wq, mx.OUT_BF16, out=L.y))
         timed("quant", quant_bytes(M, N, True), lambda: mx.rotate_quantize(
-            L.dy, mx.HAD_16, mx.SCALE_FLOOR, RC, outs={"row": L.dyq, "colT": L.dyT}))
-        timed("gemm", 2 * M * N * K, lambda: mx.gemm(L.dyq, L.wT, mx.OUT_BF16, out=L.dx))
-        timed("gemm", 2 * M * N * K, lambda: mx.gemm(L.dyT, L.xT, mx.OUT_F32, out=L.dw))
+            L.dy, H, mx.SCALE_FLOOR, RC, outs={"row": L.dyq, "colT": L.dyT}))
+        if group:
+            timed("gemm", 2 * 2 * M * N * K, lambda: backward_group(L))
+        else:
+            timed("gemm", 2 * M * N * K, lambda: mx.gemm(L.dyq, L.wT, mx.OUT_BF16, out=L.dx))
+            timed("gemm", 2 * M * N * K, lambda: mx.gemm(L.dyT, L.xT, mx.OUT_F32, out=L.dw))
 
 
-LAUNCHES_PER_LAYER = 6  # 3 rotate+quantise + 3 GEMM kernels
+def launches_per_layer(pair=True, group=True):
+    # rotate+quantise launches (2 or 3) + GEMM launches (2 or 3)
+    return (2 if pair else 3) + (2 if group else 3)
 
 
 def run_e2e_step(layers, ws, streams):
     """The same step through the public linear-layer API with host buffers: H2D of
-    X, W, dY from pinned memory, fprop/dgrad/wgrad, D2H of Y, dX, dW.  Three streams
+    X, W, dY from pinned memory, mxfp4_linear_fprop and mxfp4_linear_backward (Dgrad and
+    Wgrad in one grouped launch), D2H of Y, dX, dW.  Three streams
     (copy-in, compute, copy-out) ordered by events at the finest grain the data allows:
     Fprop starts once X and W have landed (dY still uploading), and each output starts
     downloading as soon as the GEMM that writes it has finished."""
@@ -280,7 +305,6 @@ def run_e2e_step(layers, ws, streams):
 
     s_in, s_comp, s_out = streams
     cfg = mx.Config(had=mx.HAD_16, mode=mx.SCALE_FLOOR, out_dtype=mx.OUT_BF16)
-    wcfg = mx.Config(had=mx.HAD_16, mode=mx.SCALE_FLOOR, out_dtype=mx.OUT_F32)
     start = torch.cuda.current_stream()
     for st in streams:
         st.wait_stream(start)
@@ -302,10 +326,8 @@ def run_e2e_step(layers, ws, streams):
             mx.linear_fprop(L.x, L.w, cfg, y=L.y, xT=L.xT, wT=L.wT, ws=ws, stream=s_comp)
             ev_y = mark(s_comp)
             s_comp.wait_event(ev_dy)
-            mx.linear_dgrad(L.dy, L.wT, cfg, dx=L.dx, dyT=L.dyT, ws=ws, stream=s_comp)
-            ev_dx = mark(s_comp)
-            mx.linear_wgrad(L.dyT, L.xT, wcfg, dw=L.dw, stream=s_comp)
-            ev_dw = mark(s_comp)
+            mx.linear_backward(L.dy, L.wT, L.xT, cfg, dx=L.dx, dw=L.dw, ws=ws, stream=s_comp)
+            ev_dx = ev_dw = mark(s_comp)
         with torch.cuda.stream(s_out):
             for ev, src, dst in ((ev_y, L.y, "y"), (ev_dx, L.dx, "dx"), (ev_dw, L.dw, "dw")):
                 s_out.wait_event(ev)
@@ -423,8 +445,9 @@ def gpu_arm(args, rank, world, dist):
 
     # directly measured dense kind::mxf4 MMA rate (back-to-back MMAs, resident operands)
     probe = max(mx.mma_peak_tflops(0, 1 << 16) for _ in range(3))
+    pair, group = not args.separate_xw, not args.no_group
     for _ in range(args.warmup):
-        run_step(layers)
+        run_step(layers, pair=pair, group=group)
     torch.cuda.synchronize()
     assert mx.device_status() == 0, "device status after warm-up"
     # The step's 24 launches captured once as a CUDA graph (the library makes no host
@@ -437,13 +460,13 @@ def gpu_arm(args, rank, world, dist):
         side.wait_stream(torch.cuda.current_stream())
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side):
-            run_step(layers, aux=aux)
+            run_step(layers, aux=aux, pair=pair, group=group)
         torch.cuda.synchronize()
         for _ in range(args.warmup):
             graph.replay()
         torch.cuda.synchronize()
         assert mx.device_status() == 0, "device status after graph warm-up"
-    step = graph.replay if graph is not None else (lambda: run_step(layers, aux=aux))
+    step = graph.replay if graph is not None else (lambda: run_step(layers, aux=aux, pair=pair, group=group))
 
     # ---- timed region: K steps, L2 flushed before each, device-timed with events around
     # each step; the kernels of a step run back to back (a GEMM starts its set-up while
@@ -466,7 +489,7 @@ def gpu_arm(args, rank, world, dist):
         barrier(dist)
         for _ in range(args.steps):
             flush()
-            run_step(layers, kern_ev)
+            run_step(layers, kern_ev, pair=pair, group=group)
         torch.cuda.synchronize()
     barrier(dist)
     status = mx.device_status()
@@ -486,8 +509,11 @@ def gpu_arm(args, rank, world, dist):
     except Exception:
         pass
     hbm = peaks.get("hbm_gbs") or 6800.0
-    bf16_sus = peaks.get("bf16_tflops_sustained") or 1700.0
-    fp4_peak = bf16_sus * (13.5 / 2.25)  # nominal dense FP4 / BF16 ratio on GB300
+    # Each GEMM of the roofline pass is timed on its own (an event pair around every
+    # launch, ~50-500 us each), so the burst figure applies; x6 is the nominal dense
+    # FP4 / BF16 ratio on GB300.
+    bf16_burst = peaks.get("bf16_tflops") or 1900.0
+    fp4_peak = bf16_burst * (13.5 / 2.25)
     g_ms, g_fl, g_n = agg.get("gemm", (0, 0, 0))
     q_ms, q_by, q_n = agg.get("quant", (0, 0, 0))
     gemm_tflops = g_fl / (g_ms * 1e-3) / 1e12 if g_ms else 0.0
@@ -496,11 +522,11 @@ def gpu_arm(args, rank, world, dist):
     traffic = measured_traffic()
     roof_gemm = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1),
                  "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4), "traffic": traffic["gemm"],
-                 "kernel": "mxf4_gemm_pair_kernel", "peak_source": "measured bf16 sustained x 6 (nominal fp4/bf16)",
+                 "kernel": "mxf4_gemm_pair_kernel", "peak_source": "measured bf16 burst x 6 (nominal fp4/bf16), of measured",
                  "peak_probe_tflops": round(probe, 1), "frac_of_probe": round(gemm_tflops / probe, 4)}
     roof_quant = {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": hbm, "unit": "GB/s",
                   "frac": round(quant_gbs / hbm, 4), "traffic": traffic["quant"], "kernel": "rq_kernel",
-                  "peak_source": "measured (hbm_gbs)"}
+                  "peak_source": "measured (hbm_gbs), of measured"}
     dominant = roof_gemm if gemm_share >= 0.5 else roof_quant
 
     # ---- end to end through the public API with host buffers
@@ -550,8 +576,24 @@ def gpu_arm(args, rank, world, dist):
     fp8 = None
     if not args.skip_fp8:
         fp8 = fp8_comparator(layers, flush, args.steps, args.warmup)
-        if fp8 is not None:
-            fp8["mxfp4_step_speedup"] = round(fp8["ms_per_step"] / ms_per_step, 3)
+        if fp8 is not None and "gemm_only_ms_per_step" in fp8:
+            # The FP8 GEMMs alone against this path's whole step (its quantisation
+            # included), and GEMM kernels against GEMM kernels.  The unfused FP8 step
+            # (torch amax, casts, transposes) is reported for context only.
+            fp8["mxfp4_step_over_fp8_gemms"] = round(fp8["gemm_only_ms_per_step"] / ms_per_step, 3)
+            fp8["gemm_over_gemm"] = round(gemm_tflops / fp8["gemm_only_tflops"], 3)
+
+    h32 = None
+    if not args.skip_h32:
+        h32 = h32_leg(layers, flush, args.steps, args.warmup,
+                      {"ms_per_step": ms_per_step, "quant_gbs": quant_gbs, "gemm_tflops": gemm_tflops}, pair, group,
+                      h16_graph=graph)
+
+    stress = None
+    n_layers = len(layers)
+    if not args.skip_stress:
+        del layers
+        stress = wgrad_stress_leg(flush, min(args.steps, 10), fp4_peak, hbm)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -561,10 +603,12 @@ def gpu_arm(args, rank, world, dist):
         "config": {"workload": WORKLOAD, "tokens": T_TOKENS, "flops_per_step": fl,
                    "l2": "flushed before every timed step (256 MB write, then a 256 MB read of another buffer, then a ~50 us GPU spin so host launch cost stays outside the events); per-step events exclude all of it",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": (("CUDA graph of the step's 24 launches, replayed" if graph is not None
-                               else "stream launches")
-                              + ("" if aux is None else "; per linear, X and W quantisations on two branches "
-                                 "before Fprop, Dgrad and Wgrad on two branches after the dY quantisation"))},
+                   "launch": ((f"CUDA graph of the step's {launches_per_layer(pair, group) * n_layers} launches, "
+                               "replayed" if graph is not None else "stream launches")
+                              + ("; per linear, X and W quantised in one launch" if pair else
+                                 "; per linear, X and W quantisations on two branches")
+                              + ("; Dgrad and Wgrad in one grouped GEMM launch" if group else
+                                 "; Dgrad and Wgrad on two branches"))},
         "roofline": dominant,
         "kernels": {"gemm": {**roof_gemm, "launches": g_n, "ms_total": round(g_ms, 3), "share": round(gemm_share, 3)},
                     "quant": {**roof_quant, "launches": q_n, "ms_total": round(q_ms, 3),
@@ -572,7 +616,7 @@ def gpu_arm(args, rank, world, dist):
         "gemm_only_tflops": round(gemm_tflops, 1),
         "quantize_gbs": round(quant_gbs, 1),
         "e2e": e2e,
-        "gpu_launches": args.steps * LAUNCHES_PER_LAYER * len(layers),
+        "gpu_launches": args.steps * launches_per_layer(pair, group) * n_layers,
         "clocks": clk.summary(),
         "gpu": torch.cuda.get_device_name(dev),
         "step_ms_stats": step_stats(step_ms),
@@ -580,33 +624,293 @@ def gpu_arm(args, rank, world, dist):
         "fp8_comparator": fp8,
         "quant_fixes": fixes,
         "decoder_block": block,
+        "h32": h32,
+        "config3": stress,
     }
     return out
 
 
+def _ev_pair():
+    import torch
+
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def h32_leg(layers, flush, steps, warmup, h16, pair=True, group=True, h16_graph=None):
+    """The step of the headline under H32 instead of H16 (the pages compare the two
+    rotations: H16 kernels about 8% faster than H32, 1.08x, on AMD MI355X).  Same
+    layers, launches, graph and L2 flush as the H16 step; then the per-kernel pass for
+    the quantiser and GEMM rates.  `h16` holds the H16 step's figures; with `h16_graph`
+    the H16 step is timed again, interleaved step by step with the H32 one, so that the
+    ratio does not depend on when in the run each was taken."""
+    import torch
+
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    aux = torch.cuda.Stream()
+    for _ in range(warmup):
+        run_step(layers, had=32, pair=pair, group=group)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        run_step(layers, aux=aux, had=32, pair=pair, group=group)
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        graph.replay()
+    tot, tot16 = [], []
+    for _ in range(steps):
+        for g, acc in ((graph, tot), (h16_graph, tot16)):
+            if g is None:
+                continue
+            flush()
+            a, b = _ev_pair()
+            a.record()
+            g.replay()
+            b.record()
+            acc.append((a, b))
+    ev = []
+    for _ in range(steps):
+        flush()
+        run_step(layers, ev, had=32, pair=pair, group=group)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0, "device status after the H32 step"
+    ms = sum(a.elapsed_time(b) for a, b in tot) / steps
+    ms16 = sum(a.elapsed_time(b) for a, b in tot16) / steps if tot16 else h16["ms_per_step"]
+    agg = {}
+    for kind, a, b, work in ev:
+        d = agg.setdefault(kind, [0.0, 0.0])
+        d[0] += a.elapsed_time(b)
+        d[1] += work
+    q_gbs = agg["quant"][1] / (agg["quant"][0] * 1e-3) / 1e9
+    g_tf = agg["gemm"][1] / (agg["gemm"][0] * 1e-3) / 1e12
+    fl = flops_per_step()
+    return {"workload": "the headline step under H32 (same layers, launches and flush)",
+            "ms_per_step": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+            "quant_gbs": round(q_gbs, 1), "gemm_tflops": round(g_tf, 1),
+            "h16_ms_per_step_interleaved": round(ms16, 4),
+            "h16_over_h32": {"step": round(ms / ms16, 3), "quant": round(h16["quant_gbs"] / q_gbs, 3),
+                             "gemm": round(h16["gemm_tflops"] / g_tf, 3)},
+            "pages": "H16 kernels 8% faster than H32 (1.08x), AMD MI355X"}
+
+
+def wgrad_stress_leg(flush, steps, fp4_peak, hbm):
+    """Wgrad stress: dW [4096, 14336] = dY^T X contracted over T = 32768 tokens, dY
+    [32768, 4096] ~ N(0, 1e-4) with 2% outlier tokens x20, X [32768, 14336] ~ N(0, 1)
+    with 1% outlier channels x50; both operands quantised column-wise (transposed, 32x1
+    blocks along the tokens), fp32 out, 3.85 TFLOP per GEMM; for H16, H32 and no
+    rotation.  Per rotation: the two transposed quantisations and the GEMM, each timed
+    with an event pair after an L2 flush, the three rotations interleaved round by round.
+    The seeds are those of the parity test."""
+    import torch
+
+    from mxfp4_precision_gemms_gb300 import binding as mx
+    from mxfp4_precision_gemms_gb300 import synth
+
+    T, N, K = 32768, 4096, 14336
+    x = mx.bf16_tensor(synth.activations(T, K, 3000))
+    dy = mx.bf16_tensor(synth.output_grads(T, N, 3002))
+    fl = 2 * N * K * T
+    out = {"workload": f"dW [{N}, {K}] = dY^T X over T={T} tokens, transposed (32x1) copies, fp32 out",
+           "tflop": round(fl / 1e12, 3)}
+    xT = mx.empty_qtensor(K, T, mx.LAYOUT_COLT, mx.SF_MMA)
+    dyT = mx.empty_qtensor(N, T, mx.LAYOUT_COLT, mx.SF_MMA)
+    dw = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    qbytes = quant_bytes(T, K, False) + quant_bytes(T, N, False)
+    rots = ((16, "h16"), (32, "h32"), (0, "none"))
+    t = {name: {"qx": 0.0, "qd": 0.0, "g": 0.0} for _, name in rots}
+    for it in range(3 + steps):  # 3 warm-up rounds; the rotations interleaved round by round
+        for had, name in rots:
+            qx = lambda: mx.rotate_quantize(x, had, mx.SCALE_FLOOR, mx.LAYOUT_COLT, outs={"colT": xT})
+            qd = lambda: mx.rotate_quantize(dy, had, mx.SCALE_FLOOR, mx.LAYOUT_COLT, outs={"colT": dyT})
+            g = lambda: mx.gemm(dyT, xT, mx.OUT_F32, out=dw)
+            flush()
+            evs = []
+            for k, fn in (("qx", qx), ("qd", qd), ("g", g)):
+                a, b = _ev_pair()
+                a.record()
+                fn()
+                b.record()
+                evs.append((k, a, b))
+            torch.cuda.synchronize()
+            if it >= 3:
+                for k, a, b in evs:
+                    t[name][k] += a.elapsed_time(b) / steps
+    for had, name in rots:
+        t_ = t[name]
+        g_tf = fl / (t_["g"] * 1e-3) / 1e12
+        q_ms = t_["qx"] + t_["qd"]
+        out[name] = {"gemm_us": round(t_["g"] * 1e3, 1), "gemm_tflops": round(g_tf, 1),
+                     "gemm_frac": round(g_tf / fp4_peak, 4), "quant_us": round(q_ms * 1e3, 1),
+                     "quant_gbs": round(qbytes / (q_ms * 1e-3) / 1e9, 1),
+                     "quant_incl_tflops": round(fl / ((q_ms + t_["g"]) * 1e-3) / 1e12, 1)}
+    assert mx.device_status() == 0, "device status after the Wgrad stress"
+    out["h16_over_h32_quant_incl"] = round(out["h16"]["quant_incl_tflops"] / out["h32"]["quant_incl_tflops"], 3)
+    out["peak"] = {"tflops": round(fp4_peak, 1), "hbm_gbs": hbm}
+    return out
+
+
+BLOCK_INPUTS = (("attn_in", 4096, ("q", "k", "v")), ("o_in", 4096, ("o",)), ("mlp_in", 4096, ("gate", "up")),
+                ("down_in", 14336, ("down",)))
+
+
+class BlockInput:
+    """One activation of the decoder block and its two quantised copies (row, for the
+    Fprops that read it; transposed, for their Wgrads): q, k and v read the same
+    normalised input, gate and up another."""
+
+    def __init__(self, name, K, seed, dev):
+        import torch
+
+        from mxfp4_precision_gemms_gb300 import binding as mx
+        from mxfp4_precision_gemms_gb300 import synth
+
+        self.name, self.K = name, K
+        self.x = mx.bf16_tensor(synth.activations(T_TOKENS, K, seed), dev)
+        self.xq = mx.empty_qtensor(T_TOKENS, K, mx.LAYOUT_ROW, mx.SF_MMA, dev)
+        self.xT = mx.empty_qtensor(K, T_TOKENS, mx.LAYOUT_COLT, mx.SF_MMA, dev)
+        self.quant_bytes = quant_bytes(T_TOKENS, K, True)
+
+
+class BlockLinear:
+    """One linear layer of the block: its weight W [N, K] and output gradient dY [T, N]
+    (each with row and transposed copies), and its outputs Y (bf16), its dX
+    contribution (bf16) and dW (fp32)."""
+
+    def __init__(self, name, N, inp, seed, dev):
+        import torch
+
+        from mxfp4_precision_gemms_gb300 import binding as mx
+        from mxfp4_precision_gemms_gb300 import synth
+
+        M, K = T_TOKENS, inp.K
+        self.name, self.N, self.K, self.inp = name, N, K, inp
+        self.w = mx.bf16_tensor(synth.weights(N, K, seed + 1), dev)
+        self.dy = mx.bf16_tensor(synth.output_grads(M, N, seed + 2), dev)
+        E = mx.empty_qtensor
+        self.wq, self.wT = E(N, K, mx.LAYOUT_ROW, mx.SF_MMA, dev), E(K, N, mx.LAYOUT_COLT, mx.SF_MMA, dev)
+        self.dyq, self.dyT = E(M, N, mx.LAYOUT_ROW, mx.SF_MMA, dev), E(N, M, mx.LAYOUT_COLT, mx.SF_MMA, dev)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        self.dw = torch.empty((N, K), dtype=torch.float32, device=dev)
+        self.quant_bytes = quant_bytes(N, K, True) + quant_bytes(M, N, True)
+        self.gemm_flops = 3 * 2 * M * N * K
+
+
+def run_block(groups, ev=None):
+    """Forward and backward GEMMs of one decoder block with every launch separate: for
+    each activation, its dual quantisation once, then every linear that reads it -- W's
+    dual quantisation, Fprop; dY's dual quantisation, Dgrad, Wgrad (39 launches).  With
+    `ev`, CUDA events around each activation's quantisation and around each linear's
+    five launches: ev gets (name, start, end)."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    H, F, RC = mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW | mx.LAYOUT_COLT
+
+    def mark(name, fn):
+        if ev is None:
+            fn()
+            return
+        a, b = _ev_pair()
+        a.record()
+        fn()
+        b.record()
+        ev.append((name, a, b))
+
+    def linear(L):
+        mx.rotate_quantize(L.w, H, F, RC, outs={"row": L.wq, "colT": L.wT})
+        mx.gemm(L.inp.xq, L.wq, mx.OUT_BF16, out=L.y)
+        mx.rotate_quantize(L.dy, H, F, RC, outs={"row": L.dyq, "colT": L.dyT})
+        mx.gemm(L.dyq, L.wT, mx.OUT_BF16, out=L.dx)
+        mx.gemm(L.dyT, L.inp.xT, mx.OUT_F32, out=L.dw)
+
+    for inp, lins in groups:
+        mark(inp.name, lambda: mx.rotate_quantize(inp.x, H, F, RC, outs={"row": inp.xq, "colT": inp.xT}))
+        for L in lins:
+            mark(L.name, lambda: linear(L))
+
+
+def run_block_grouped(groups, ev=None):
+    """The block with every launch that can be shared, shared: per activation, the
+    activation and its linears' weights quantised two matrices per launch (they share
+    the contraction K), all of its linears' Fprops in one grouped GEMM launch, the output
+    gradients quantised (two per launch where they have the same shape), and all of its
+    linears' Dgrads and Wgrads in one grouped launch -- 20 launches for the block.  With
+    `ev`, CUDA events around each activation's launches: ev gets (name, start, end)."""
+    import torch
+
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    H, F, RC = mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW | mx.LAYOUT_COLT
+    for inp, lins in groups:
+        if ev is not None:
+            a, b = _ev_pair()
+            a.record()
+        mats = [(inp.x, {"row": inp.xq, "colT": inp.xT})] + [(L.w, {"row": L.wq, "colT": L.wT}) for L in lins]
+        for i in range(0, len(mats), 2):
+            if i + 1 < len(mats):
+                mx.rotate_quantize_pair(mats[i][0], mats[i + 1][0], H, F, RC, outs_a=mats[i][1], outs_b=mats[i + 1][1])
+            else:
+                mx.rotate_quantize(mats[i][0], H, F, RC, outs=mats[i][1])
+        mx.gemm_group([(inp.xq, L.wq, mx.OUT_BF16, False, L.y) for L in lins])
+        i = 0
+        while i < len(lins):
+            L = lins[i]
+            if i + 1 < len(lins) and lins[i + 1].N == L.N:
+                L2 = lins[i + 1]
+                mx.rotate_quantize_pair(L.dy, L2.dy, H, F, RC, outs_a={"row": L.dyq, "colT": L.dyT},
+                                        outs_b={"row": L2.dyq, "colT": L2.dyT})
+                i += 2
+            else:
+                mx.rotate_quantize(L.dy, H, F, RC, outs={"row": L.dyq, "colT": L.dyT})
+                i += 1
+        mx.gemm_group([(L.dyq, L.wT, mx.OUT_BF16, False, L.dx) for L in lins]
+                      + [(L.dyT, inp.xT, mx.OUT_F32, False, L.dw) for L in lins])
+        if ev is not None:
+            b.record()
+            ev.append(("+".join(L.name for L in lins), a, b))
+
+
 def decoder_block_leg(flush, steps, warmup, dev):
-    """One Llama-3.1-8B-shaped decoder block at T = 8192: the seven linear layers (q, k, v,
-    o, gate, up, down; k and v have N = 1024), each with Fprop, Dgrad and Wgrad under H16 +
-    MXFP4, quantisation included -- 42 launches, 10.72 TFLOP.  Each linear's X, W and dY
-    are drawn from the block's distributions (seed base 4000 + 10 i); the block's non-GEMM
-    ops (RMSNorm, SiLU, attention core) lie outside the timed GEMM path and are not run.
-    Total: the block's launches as one two-branch CUDA graph, events around each replay.
-    Per layer: the same launches on one stream with events around each layer's six.  L2 is
+    """One Llama-3.1-8B-shaped decoder block at T = 8192: the seven linear layers (q, k,
+    v, o, gate, up, down; k and v have N = 1024), each with Fprop, Dgrad and Wgrad under
+    H16 + MXFP4, quantisation included -- 10.72 TFLOP.  q, k and v read one activation
+    and gate and up another, as in the block; each activation is rotated and quantised
+    once (row and transposed copies) and shared, so the block has 4 activation, 7 weight
+    and 7 output-gradient quantisations and 21 GEMMs (39 launches).  The dX
+    contributions of q, k and v (and of gate and up) are summed outside the GEMM path,
+    with the block's other non-GEMM ops (RMSNorm, SiLU, attention core), which are not
+    run.  Inputs: activations N(0,1) + 1% channels x50, weights N(0,0.02), output
+    gradients N(0,1e-4) + 2% tokens x20 (seed base 4000).
+    Total: the block's 20 launches with grouped GEMMs and paired quantisations
+    (run_block_grouped), captured as one CUDA graph, events around each replay; the
+    same launches with events around each activation's group give `per_group`.  Per
+    layer (`per_layer`): every launch separate (run_block, 39 launches), one stream,
+    events around each layer's own launches (its W and dY quantisations and three GEMMs)
+    and around each activation's quantisation, which is charged to the layers that read
+    it in proportion to their FLOPs; `separate_ms` is that serial block's total.  L2 is
     emptied before every timed block."""
     import torch
 
     from mxfp4_precision_gemms_gb300 import binding as mx
     from mxfp4_precision_gemms_gb300 import synth
 
-    layers = [Layer(n, N, K, 4000 + 10 * i, dev) for i, (n, N, K) in enumerate(synth.LLAMA8B_BLOCK_LINEARS)]
-    fl = flops_per_step(synth.LLAMA8B_BLOCK_LINEARS)
+    shapes = dict((n, N) for n, N, _ in synth.LLAMA8B_BLOCK_LINEARS)
+    groups = []
+    for gi, (iname, K, names) in enumerate(BLOCK_INPUTS):
+        inp = BlockInput(iname, K, 4000 + 100 * gi, dev)
+        groups.append((inp, [BlockLinear(n, shapes[n], inp, 4000 + 100 * gi + 10 * (j + 1), dev)
+                             for j, n in enumerate(names)]))
+    linears = [L for _, lins in groups for L in lins]
+    fl = sum(L.gemm_flops for L in linears)
     for _ in range(warmup):
-        run_step(layers)
-    side, aux = torch.cuda.Stream(), torch.cuda.Stream()
+        run_block(groups)
+        run_block_grouped(groups)
+    side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=side):
-        run_step(layers, aux=aux)
+        run_block_grouped(groups)
     torch.cuda.synchronize()
     for _ in range(warmup):
         graph.replay()
@@ -614,35 +918,51 @@ def decoder_block_leg(flush, steps, warmup, dev):
     tot = []
     for _ in range(steps):
         flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b = _ev_pair()
         a.record()
         graph.replay()
         b.record()
         tot.append((a, b))
-    per = {L.name: 0.0 for L in layers}
+    per, per_group, sep = {}, {}, 0.0
     for _ in range(steps):
         flush()
-        for L in layers:
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            run_step([L])
-            b.record()
-            L.ev = (a, b)
+        ev = []
+        run_block(groups, ev=ev)
         torch.cuda.synchronize()
-        for L in layers:
-            per[L.name] += L.ev[0].elapsed_time(L.ev[1])
+        for name, a, b in ev:
+            per[name] = per.get(name, 0.0) + a.elapsed_time(b) / steps
+            sep += a.elapsed_time(b) / steps
+        flush()
+        ev = []
+        run_block_grouped(groups, ev=ev)
+        torch.cuda.synchronize()
+        for name, a, b in ev:
+            per_group[name] = per_group.get(name, 0.0) + a.elapsed_time(b) / steps
     torch.cuda.synchronize()
     assert mx.device_status() == 0, "device status after the decoder-block leg"
     ms = sum(a.elapsed_time(b) for a, b in tot) / steps
     out = {"workload": "one Llama-3.1-8B decoder block, T=8192: q, k, v, o, gate, up, down; fprop+dgrad+wgrad, "
-                       "H16, OCP floor, quantisation included",
+                       "H16, OCP floor, quantisation included; q/k/v and gate/up share their input's quantised copies",
            "tflop_per_block": round(fl / 1e12, 3), "ms": round(ms, 4), "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
-           "launch": "CUDA graph of the block's 42 launches, two branches per linear", "per_layer": {}}
-    for L in layers:
-        lms = per[L.name] / steps
-        out["per_layer"][L.name] = {"N": L.N, "K": L.K, "ms": round(lms, 4),
-                                    "tflops": round(L.gemm_flops / (lms * 1e-3) / 1e12, 1)}
-    out["per_layer_note"] = "each layer's six launches on one stream, events around them"
+           "launch": "CUDA graph of the block's 20 launches: per activation, quantisations two matrices per launch, "
+                     "one grouped launch for the Fprops and one for the Dgrads and Wgrads",
+           "per_group": {}, "separate_ms": round(sep, 4),
+           "separate_tflops": round(fl / (sep * 1e-3) / 1e12, 1), "per_layer": {},
+           "input_quant_us": {inp.name: round(per[inp.name] * 1e3, 1) for inp, _ in groups}}
+    for inp, lins in groups:
+        name = "+".join(L.name for L in lins)
+        gfl = sum(L.gemm_flops for L in lins)
+        out["per_group"][name] = {"ms": round(per_group[name], 4),
+                                  "tflops": round(gfl / (per_group[name] * 1e-3) / 1e12, 1)}
+    for inp, lins in groups:
+        gfl = sum(L.gemm_flops for L in lins)
+        for L in lins:
+            lms = per[L.name] + per[inp.name] * L.gemm_flops / gfl
+            out["per_layer"][L.name] = {"N": L.N, "K": L.K, "ms": round(lms, 4),
+                                        "tflops": round(L.gemm_flops / (lms * 1e-3) / 1e12, 1)}
+    out["per_layer_note"] = ("every launch separate: each layer's own five launches on one stream, events around "
+                             "them, plus its FLOP share of its input's quantisation; per_group times the grouped "
+                             "launches of each activation's linears together")
     return out
 
 
@@ -652,7 +972,8 @@ def quant_fixes_leg(flush, hbm, iters=20):
     launch timed alone with CUDA events after an L2 flush, against the HBM roofline.
     Algorithmic bytes per element: OF 2 + 2 x (0.5 + 1/32); MBS 2 + 0.5 + 1/32 + 1/128;
     random signs + stochastic rounding, both copies, 2 + 2 x 2 (random integers) + 2 x
-    (0.5 + 1/32); random signs alone, both copies, 2 + 2 x (0.5 + 1/32).
+    (0.5 + 1/32); random signs alone, both copies, 2 + 2 x (0.5 + 1/32); the same two
+    with Philox numbers drawn in the kernel, 2 + 2 x (0.5 + 1/32) (nothing random read).
     Not part of the timed step: a measurement of the variants."""
     import torch
 
@@ -681,6 +1002,15 @@ def quant_fixes_leg(flush, hbm, iters=20):
     legs["signs_dual"] = (lambda: mx.rotate_quantize_rand(x, had=16, mode=0, layouts=mx.LAYOUT_ROW | mx.LAYOUT_COLT,
                                                           col_signs=col_signs, row_signs=row_signs),
                           n * (2 + 2 * (0.5 + 1 / 32)))
+    # the same with the numbers drawn in the kernel (Philox4x32-10): nothing random is read
+    legs["philox_signs_sr_dual"] = (
+        lambda: mx.rotate_quantize_philox(x, had=16, mode=0, layouts=mx.LAYOUT_ROW | mx.LAYOUT_COLT,
+                                          col_sign_seed=11, row_sign_seed=12, sr_seed=13),
+        n * (2 + 2 * (0.5 + 1 / 32)))
+    legs["philox_signs_dual"] = (
+        lambda: mx.rotate_quantize_philox(x, had=16, mode=0, layouts=mx.LAYOUT_ROW | mx.LAYOUT_COLT,
+                                          col_sign_seed=11, row_sign_seed=12),
+        n * (2 + 2 * (0.5 + 1 / 32)))
     out = {"tensor": f"{R}x{C} bf16 activations, H16, OCP floor", "unit": "GB/s", "peak": hbm}
     for name, (fn, by) in legs.items():
         for _ in range(3):
@@ -798,12 +1128,14 @@ def fp8_comparator(layers, flush, steps, warmup):
         b.synchronize()
         gt += a.elapsed_time(b)
     gms = gt / steps
-    return {"impl": "torch._scaled_mm e4m3 per-tensor", "ms_per_step": round(ms, 4),
-            "tflops": round(flops_per_step() / (ms * 1e-3) / 1e12, 1),
+    return {"impl": "torch._scaled_mm e4m3 per-tensor",
             "gemm_only_ms_per_step": round(gms, 4),
             "gemm_only_tflops": round(flops_per_step() / (gms * 1e-3) / 1e12, 1),
-            "note": "ms_per_step includes unfused torch quantisation and transposes; gemm_only times the "
-                    "12 FP8 GEMMs of the step on pre-quantised operands"}
+            "unfused_step_ms": round(ms, 4),
+            "note": "gemm_only times the 12 FP8 GEMMs of the step on operands quantised beforehand; "
+                    "mxfp4_step_over_fp8_gemms = those GEMMs' time / this path's whole step (quantisation "
+                    "included); gemm_over_gemm = MXFP4 GEMM TFLOP/s / FP8 GEMM TFLOP/s.  unfused_step_ms (torch "
+                    "amax, casts and transposes around the FP8 GEMMs) is context, not a comparison"}
 
 
 # --------------------------------------------------------------------------- oracle (CPU)
@@ -835,6 +1167,27 @@ def oracle_on_host_cores():
     return oracle
 
 
+def oracle_quantizer_timing(oracle):
+    """The quantiser oracle, as it stands, on the full rotate+quantise sweep tensors
+    (4096 x 4096 and 8192 x 14336, 0.1 t(3) + 0.1% entries x100), H16, OCP floor, row
+    layout, with one thread and with one thread per available core: GB/s of the same
+    algorithmic bytes as the GPU pass (2 + 0.5 + 1/32 per element)."""
+    from mxfp4_precision_gemms_gb300 import synth
+
+    cores = oracle.num_threads()
+    out = {"layout": "row (1x32), H16, OCP floor", "unit": "GB/s", "cores_all": cores}
+    for R, C in ((4096, 4096), (8192, 14336)):
+        x = synth.heavy_tailed(R, C, 13)
+        for nt, key in ((1, "1_thread"), (cores, "all_threads")):
+            oracle.set_num_threads(nt)
+            t = time.perf_counter()
+            oracle.quantize(x, 16, 0, "row")
+            dt = time.perf_counter() - t
+            out[f"{R}x{C}_{key}"] = {"gbs": round(R * C * (2 + 0.5 + 1 / 32) / dt / 1e9, 4), "s": round(dt, 2)}
+    oracle.set_num_threads(cores)
+    return out
+
+
 def cpu_baseline_leg():
     from mxfp4_precision_gemms_gb300 import synth
 
@@ -843,7 +1196,8 @@ def cpu_baseline_leg():
     fl, sec = oracle_sample(tokens, synth.LLAMA8B_LINEARS)
     return {"value": round(fl / sec / 1e12, 6), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"fprop+dgrad+wgrad of the four Llama linears on a {tokens}-token slab "
-                      f"({fl / 1e9:.1f} GFLOP, {sec:.1f} s)"}
+                      f"({fl / 1e9:.1f} GFLOP, {sec:.1f} s)",
+            "quantize": oracle_quantizer_timing(oracle)}
 
 
 def reference_arm(args, rank, world):
@@ -874,75 +1228,94 @@ def reference_arm(args, rank, world):
             "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def profile_case():
-    """Small case for ncu captures, each kernel launched twice (capture the second):
-    the down-proj X quantiser (8192x14336 bf16, 235 MB, row + transposed copies; rq_kernel
-    -s 1), and three GEMM shape classes (mxf4_gemm): gate/up Fprop 8192x14336x4096 bf16 out
-    (-s 1), gate/up Wgrad 14336x4096x8192 fp32 out (-s 3), k/v Dgrad 8192x4096x1024 bf16
-    out (-s 5)."""
+def profile_case(which="classes"):
+    """Small cases for ncu captures, so that no capture runs the whole benchmark.
+
+    classes: each kernel launched twice (capture the second): the down-proj X quantiser
+      (8192x14336 bf16, 235 MB, row + transposed copies; rq_kernel -s 1), and GEMM shape
+      classes (mxf4_gemm): gate/up Fprop 8192x14336x4096 bf16 out (-s 1), gate/up Wgrad
+      14336x4096x8192 fp32 out (-s 3), k/v Dgrad 8192x4096x1024 bf16 out (-s 5), k/v Fprop
+      8192x1024x4096 bf16 out (-s 7), k/v Wgrad 1024x4096x8192 fp32 out (-s 9).
+    step: the headline step's 20 launches (4 X+W pair and 4 dY quantisations, 12 GEMMs)
+      twice, on stream launches; capture one kernel's second round for its DRAM bytes per
+      launch: -k regex:mxf4_gemm -s 12 -c 12, or -k regex:rq_kernel -s 8 -c 8 (DRAM
+      counters only: one pass, nothing saved or restored between passes)."""
     import torch
 
     from mxfp4_precision_gemms_gb300 import binding as mx
     from mxfp4_precision_gemms_gb300 import synth
 
     torch.cuda.set_device(0)
+    if which == "step":
+        dev = torch.device("cuda", 0)
+        layers = [Layer(n, N, K, 2000 + 10 * i, dev) for i, (n, N, K) in enumerate(synth.LLAMA8B_LINEARS)]
+        for _ in range(2):
+            run_step(layers)
+        torch.cuda.synchronize()
+        assert mx.device_status() == 0
+        print("profile case (step) ok")
+        return
     RC = mx.LAYOUT_ROW | mx.LAYOUT_COLT
     xd = mx.bf16_tensor(synth.activations(8192, 14336, 1))
     for _ in range(2):
         mx.rotate_quantize(xd, mx.HAD_16, mx.SCALE_FLOOR, RC)
-    x = mx.bf16_tensor(synth.activations(8192, 4096, 2))
-    w = mx.bf16_tensor(synth.weights(14336, 4096, 3))
-    xq = mx.rotate_quantize(x, mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW)["row"]
-    wq = mx.rotate_quantize(w, mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW)["row"]
-    for _ in range(2):
-        mx.gemm(xq, wq, mx.OUT_BF16)
-    # Wgrad: dW [14336, 4096] = dY^T X, contraction over the 8192 tokens, fp32 out
-    dyt = mx.rotate_quantize(mx.bf16_tensor(synth.output_grads(14336, 8192, 4)), mx.HAD_16, mx.SCALE_FLOOR,
-                             mx.LAYOUT_ROW)["row"]
-    xt = mx.rotate_quantize(mx.bf16_tensor(synth.activations(4096, 8192, 5)), mx.HAD_16, mx.SCALE_FLOOR,
-                            mx.LAYOUT_ROW)["row"]
-    for _ in range(2):
-        mx.gemm(dyt, xt, mx.OUT_F32)
-    # k/v Dgrad: dX [8192, 4096] = dY W, contraction over N = 1024
-    dy = mx.rotate_quantize(mx.bf16_tensor(synth.output_grads(8192, 1024, 6)), mx.HAD_16, mx.SCALE_FLOOR,
-                            mx.LAYOUT_ROW)["row"]
-    wt = mx.rotate_quantize(mx.bf16_tensor(synth.weights(4096, 1024, 7)), mx.HAD_16, mx.SCALE_FLOOR,
-                            mx.LAYOUT_ROW)["row"]
-    for _ in range(2):
-        mx.gemm(dy, wt, mx.OUT_BF16)
+    del xd
+
+    def q(bits):
+        return mx.rotate_quantize(mx.bf16_tensor(bits), mx.HAD_16, mx.SCALE_FLOOR, mx.LAYOUT_ROW)["row"]
+
+    cases = [
+        (q(synth.activations(8192, 4096, 2)), q(synth.weights(14336, 4096, 3)), mx.OUT_BF16),   # gate/up Fprop
+        (q(synth.output_grads(14336, 8192, 4)), q(synth.activations(4096, 8192, 5)), mx.OUT_F32),  # gate/up Wgrad
+        (q(synth.output_grads(8192, 1024, 6)), q(synth.weights(4096, 1024, 7)), mx.OUT_BF16),   # k/v Dgrad
+        (q(synth.activations(8192, 4096, 8)), q(synth.weights(1024, 4096, 9)), mx.OUT_BF16),    # k/v Fprop
+        (q(synth.output_grads(1024, 8192, 10)), q(synth.activations(4096, 8192, 11)), mx.OUT_F32),  # k/v Wgrad
+    ]
+    for A, B, od in cases:
+        for _ in range(2):
+            mx.gemm(A, B, od)
     torch.cuda.synchronize()
     assert mx.device_status() == 0
     print("profile case ok")
 
 
-def write_traffic(csv_path):
+TRAFFIC_COMMAND = (
+    "python bench.py --profile-case step > gpurun_out/pc.log 2>&1 && "
+    "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none -k regex:mxf4_gemm -s 12 -c 12 "
+    "--csv --log-file gpurun_out/traffic_gemm.csv python bench.py --profile-case step && "
+    "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none -k regex:rq_kernel -s 8 -c 8 "
+    "--csv --log-file gpurun_out/traffic_quant.csv python bench.py --profile-case step; then "
+    "python bench.py --traffic-from gpurun_out/traffic_gemm.csv gpurun_out/traffic_quant.csv")
+
+
+def write_traffic(csv_paths):
     """Averages dram__bytes_read.sum + dram__bytes_write.sum per launch of each kernel
-    from an ncu --csv capture of this benchmark and records it with the source hashes."""
+    over per-kernel ncu --csv captures of `--profile-case step` (the headline step's 12
+    GEMMs, or its 12 dual quantisations) and records it with the source hashes."""
     import csv
 
     per = {"gemm": [], "quant": []}
-    rows = [r for r in csv.reader(open(csv_path)) if r]
-    hdr = next(r for r in rows if r[0] == "ID")
-    launches = {}
-    for r in rows:
-        if len(r) != len(hdr) or r[0] == "ID":
-            continue
-        d = dict(zip(hdr, r))
-        if d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
-            continue
-        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}[d["Metric Unit"]]
-        launches.setdefault((d["ID"], d["Kernel Name"]), 0.0)
-        launches[(d["ID"], d["Kernel Name"])] += float(d["Metric Value"].replace(",", "")) * scale
-    for (_, name), b in launches.items():
-        if "mxf4_gemm" in name:
-            per["gemm"].append(b)
-        elif "rq_kernel" in name:
-            per["quant"].append(b)
+    for csv_path in csv_paths:
+        rows = [r for r in csv.reader(open(csv_path)) if r]
+        hdr = next(r for r in rows if r[0] == "ID")
+        launches = {}
+        for r in rows:
+            if len(r) != len(hdr) or r[0] == "ID":
+                continue
+            d = dict(zip(hdr, r))
+            if d["Metric Name"] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                continue
+            scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}[d["Metric Unit"]]
+            launches.setdefault((d["ID"], d["Kernel Name"]), 0.0)
+            launches[(d["ID"], d["Kernel Name"])] += float(d["Metric Value"].replace(",", "")) * scale
+        for (_, name), b in launches.items():
+            if "mxf4_gemm" in name:
+                per["gemm"].append(b)
+            elif "rq_kernel" in name:
+                per["quant"].append(b)
     rec = {k: {"bytes_per_launch": round(sum(v) / len(v)), "launches": len(v),
                "sources_sha": kernel_sources_sha(KERNEL_SOURCES[k])} for k, v in per.items() if v}
-    rec["command"] = ("ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
-                      "--clock-control none --csv --log-file <csv> python bench.py --steps 1 --warmup 3 "
-                      "--skip-e2e --skip-cpu-baseline --skip-fp8 --skip-fixes --skip-block")
+    rec["command"] = TRAFFIC_COMMAND
     path = os.path.join(ROOT, "profiles", "traffic_llama8b_linears_T8192.json")
     json.dump(rec, open(path, "w"), indent=1)
     print(json.dumps(rec))
@@ -960,14 +1333,22 @@ def main():
     ap.add_argument("--skip-block", action="store_true", help="skip the decoder-block (seven linears) measurement")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-fp8", action="store_true", help="skip the FP8 (torch._scaled_mm) comparator")
+    ap.add_argument("--skip-h32", action="store_true", help="skip the H32 run of the step")
+    ap.add_argument("--skip-stress", action="store_true", help="skip the T=32768 Wgrad stress (H16/H32/none)")
+    ap.add_argument("--no-group", action="store_true",
+                    help="launch each linear's Dgrad and Wgrad separately (default: one grouped launch)")
+    ap.add_argument("--separate-xw", action="store_true",
+                    help="quantise each linear's X and W in two launches (default: one pair launch)")
     ap.add_argument("--serial-step", action="store_true",
                     help="launch the timed step's 24 kernels on one stream (default: two branches per linear)")
-    ap.add_argument("--profile-case", action="store_true", help="run the small ncu case and exit")
-    ap.add_argument("--traffic-from", metavar="CSV", help="turn an ncu CSV of dram bytes for this benchmark "
-                    "into profiles/traffic_llama8b_linears_T8192.json and exit")
+    ap.add_argument("--profile-case", nargs="?", const="classes", choices=["classes", "step"],
+                    help="run a small ncu case and exit (classes: one launch pair per shape class; step: the "
+                         "headline step's launches twice)")
+    ap.add_argument("--traffic-from", metavar="CSV", nargs="+", help="turn per-kernel ncu CSVs of dram bytes "
+                    "over --profile-case step into profiles/traffic_llama8b_linears_T8192.json and exit")
     args = ap.parse_args()
     if args.profile_case:
-        profile_case()
+        profile_case(args.profile_case)
         return
     if args.traffic_from:
         write_traffic(args.traffic_from)

@@ -106,7 +106,7 @@ typedef struct {
     int32_t accumulate; /* 1: C += result (fp32 output only); 0: C = result */
 } mxfp4_config;
 
-enum { MXFP4_OP_FPROP = 0, MXFP4_OP_DGRAD = 1, MXFP4_OP_WGRAD = 2 };
+enum { MXFP4_OP_FPROP = 0, MXFP4_OP_DGRAD = 1, MXFP4_OP_WGRAD = 2, MXFP4_OP_BACKWARD = 3 };
 
 /* Bytes of packed codes for a rows x cols quantised matrix. */
 size_t mxfp4_codes_bytes(int64_t rows, int64_t cols);
@@ -137,6 +137,20 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
                                    unsigned layouts, mxfp4_tensor* row_out, mxfp4_tensor* colT_out,
                                    mxfp4_tensor* twoD_out, mxfp4_stream_t stream);
 
+/* Two matrices with the same number of columns -- a GEMM's two operands, which share
+ * the contraction dimension (Fprop's X [M, K] and W [N, K]) -- rotated and quantised
+ * in ONE launch, each exactly as mxfp4_rotate_quantize would (same had, mode and
+ * layouts for both; ROW, COLT or both, no 2D).  One launch spares the smaller matrix
+ * its own ramp-up and partly filled last wave.
+ * a: device bf16 [a_rows, cols] (leading dimension a_ld); b: [b_rows, cols] (b_ld);
+ * both under the rules of mxfp4_rotate_quantize.  Outputs as there: a_row / b_row for
+ * ROW, a_colT ([cols, a_rows]) / b_colT for COLT; outputs not requested may be NULL.
+ * Validation of both matrices and all outputs precedes the launch. */
+mxfp4_status mxfp4_rotate_quantize_pair(const void* a, int64_t a_rows, int64_t a_ld, const void* b, int64_t b_rows,
+                                        int64_t b_ld, int64_t cols, int had, int mode, unsigned layouts,
+                                        mxfp4_tensor* a_row, mxfp4_tensor* a_colT, mxfp4_tensor* b_row,
+                                        mxfp4_tensor* b_colT, mxfp4_stream_t stream);
+
 /* Block-scaled MXFP4 GEMM C = A . B^T with FP32 accumulation on the tcgen05 tensor
  * cores (QDQ numerics: "Decomposing MXFP4 quantization error", experiments).
  * A: [M, K] quantised along K, B: [N, K] quantised along K, both MXFP4_SF_MMA,
@@ -152,6 +166,29 @@ mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, in
  * ws/ws_bytes: unused by this kernel (pass NULL/0); reserved for split-K. */
 mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, int64_t ldc, int out_dtype,
                         int accumulate, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
+
+/* One problem of mxfp4_gemm_group: C = A . B^T with the rules of mxfp4_gemm. */
+typedef struct {
+    const mxfp4_tensor* A;
+    const mxfp4_tensor* B;
+    void* C;
+    int64_t ldc;
+    int32_t out_dtype;  /* mxfp4_out_dtype */
+    int32_t accumulate; /* 1: C += A . B^T (fp32 output only) */
+} mxfp4_gemm_desc;
+
+/* 1 to 8 independent GEMMs in ONE persistent launch of the CTA-pair kernel: their
+ * 256 x 256 output tiles form one schedule, so the problems share the launch's fixed
+ * costs (set-up, pipeline fill, last-tile drain) and fill one another's partly used
+ * last waves.  The linear layer's backward is such a pair (Dgrad and Wgrad, "Pretraining
+ * ... Native FP4 Hardware" C.2-C.3; both read only quantised copies made beforehand), and
+ * so are projections that read the same input (q, k, v of attention).
+ * Every problem follows mxfp4_gemm's rules and is checked before anything is launched;
+ * no two outputs may share a byte (MXFP4_ERR_INVALID_ARG).  Each output equals what
+ * mxfp4_gemm computes for that problem with the CTA-pair kernel (M > 128 and N > 128),
+ * bit for bit; narrower problems also run on the pair kernel here.  A group of one is
+ * exactly mxfp4_gemm. */
+mxfp4_status mxfp4_gemm_group(const mxfp4_gemm_desc* descs, int count, mxfp4_stream_t stream);
 
 /* Error-decomposition measurement ("Decomposing MXFP4 quantization error for LLM
  * reinforcement learning", core insight and property 1).  x: device bf16 [rows, cols]
@@ -231,6 +268,40 @@ mxfp4_status mxfp4_rotate_quantize_ex(const void* x, int64_t rows, int64_t cols,
                                       unsigned layouts, const mxfp4_quant_opts* opts, mxfp4_tensor* row_out,
                                       mxfp4_tensor* colT_out, mxfp4_tensor* twoD_out, mxfp4_stream_t stream);
 
+/* The randomised baselines with their random numbers drawn in the kernel from
+ * Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
+ * 1, 2, 3", SC'11), a counter-based generator: nothing random is read from memory, and
+ * every number is a fixed function of (seed, counter), so a run can be replayed.
+ *   col_signs: 1 negates column j (row copy) when bit j of the sign vector of seed
+ *     col_sign_seed is set -- bit j % 32 of output word (j % 128) / 32 of
+ *     Philox(counter (j / 128, 0, 0, 0), key (seed low 32 bits, seed high 32 bits)).
+ *     The sign vector belongs to a dimension: a GEMM's two operands must use the same
+ *     seed for their shared contraction (X's and W's columns: K; W's rows and dY's
+ *     columns: N; X's and dY's rows: M) so that the rotation still cancels.
+ *   row_signs: the same over the rows (transposed copy), seed row_sign_seed.
+ *   stochastic_rounding: the rule of mxfp4_quant_opts with the 16-bit integer of
+ *     (line l, position i) of the stored copy (row copy: l = row, i = column; transposed
+ *     copy: l = column, i = row) taken as half i % 8 (word (i % 8) / 2, low half
+ *     first) of Philox(counter (i / 8, l, copy, 0), key (sr_seed low, sr_seed high)),
+ *     copy = 0 for the row copy and 1 for the transposed copy.
+ * With the same numbers, the result equals mxfp4_rotate_quantize_ex given those numbers
+ * as arrays.  reserved must be 0. */
+typedef struct {
+    uint64_t col_sign_seed;
+    uint64_t row_sign_seed;
+    uint64_t sr_seed;
+    int32_t col_signs;
+    int32_t row_signs;
+    int32_t stochastic_rounding;
+    int32_t reserved;
+} mxfp4_philox_opts;
+
+/* mxfp4_rotate_quantize (ROW, COLT or both) with in-kernel Philox random signs and/or
+ * stochastic rounding as set in opts (every option 0: exactly mxfp4_rotate_quantize). */
+mxfp4_status mxfp4_rotate_quantize_philox(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                          unsigned layouts, const mxfp4_philox_opts* opts, mxfp4_tensor* row_out,
+                                          mxfp4_tensor* colT_out, mxfp4_stream_t stream);
+
 /* Workspace bytes needed by mxfp4_linear_{fprop,dgrad,wgrad} (op = MXFP4_OP_*). */
 size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp4_config* cfg);
 
@@ -243,6 +314,8 @@ size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp
  * save_wT (optional): receives W^T quantised along N, [K, N], the Dgrad operand
  *    (needs N % 32 == 0); produced in the same pass that reads W.
  * Saved tensors must be MXFP4_SF_MMA.  K % 32 == 0, N % 8 == 0 (y's leading dimension).
+ * X and W are quantised in one launch (as by mxfp4_rotate_quantize_pair) when both
+ * transposed copies, or neither, are requested.
  * Every argument of both quantiser passes and of the GEMM is checked before the first
  * launch: a rejected call leaves the workspace, the saved copies and y untouched. */
 mxfp4_status mxfp4_linear_fprop(const void* x, const void* w, int64_t M, int64_t N, int64_t K,
@@ -269,6 +342,21 @@ mxfp4_status mxfp4_linear_dgrad(const void* dy, const mxfp4_tensor* wT, int64_t 
  * (MXFP4_ERR_INVALID_ARG otherwise). */
 mxfp4_status mxfp4_linear_wgrad(const mxfp4_tensor* dyT, const mxfp4_tensor* xT, const mxfp4_config* cfg,
                                 void* dw, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
+
+/* The whole backward of a linear layer ("Pretraining ... Native FP4 Hardware", C.2 and
+ * C.3): dY [M, N] bf16 (ld N) is rotated and quantised once, along N (row copy, the
+ * Dgrad operand) and along M (transposed copy, the Wgrad operand), into the workspace
+ * (mxfp4_workspace_bytes(MXFP4_OP_BACKWARD, ...)); then Dgrad dX = dY W and Wgrad
+ * dW = dY^T X run as ONE grouped launch (mxfp4_gemm_group).
+ * wT: [K, N] and xT: [K, M], the COLT copies saved by mxfp4_linear_fprop, made under
+ * cfg's had and mode.  dx: device [M, K] (ld K) in cfg->out_dtype, overwritten.
+ * dw: device fp32 [N, K] (ld K), overwritten, or added to when cfg->accumulate
+ * (gradient accumulation).  M % 32 == 0, N % 32 == 0.  Everything is checked before
+ * the first launch.  Outputs equal mxfp4_linear_dgrad + mxfp4_linear_wgrad bit for bit
+ * where those run on the CTA-pair kernel (M, N, K > 128). */
+mxfp4_status mxfp4_linear_backward(const void* dy, const mxfp4_tensor* wT, const mxfp4_tensor* xT, int64_t M,
+                                   int64_t N, int64_t K, const mxfp4_config* cfg, void* dx, void* dw, void* ws,
+                                   size_t ws_bytes, mxfp4_stream_t stream);
 
 /* Fprop without caller-provided scratch.  The pages have no counterpart: this entry
  * exists for callers that cannot allocate device memory -- a plugin inside a host

@@ -24,7 +24,7 @@ SCALE_FLOOR, SCALE_CEIL = 0, 1
 LAYOUT_ROW, LAYOUT_COLT, LAYOUT_2D = 1, 2, 4
 OUT_F32, OUT_BF16 = 0, 1
 SF_PLAIN, SF_MMA = 0, 1
-OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
+OP_FPROP, OP_DGRAD, OP_WGRAD, OP_BACKWARD = 0, 1, 2, 3
 
 STATUS = {0: "MXFP4_OK", 1: "MXFP4_ERR_INVALID_ARG", 2: "MXFP4_ERR_UNSUPPORTED_SHAPE", 3: "MXFP4_ERR_MISALIGNED",
           4: "MXFP4_ERR_WORKSPACE", 5: "MXFP4_ERR_CUDA", 6: "MXFP4_ERR_TIMEOUT", 7: "MXFP4_ERR_UNSUPPORTED_DEVICE"}
@@ -40,6 +40,19 @@ class QuantOptsC(ctypes.Structure):
     """mxfp4_quant_opts: sign bitmasks and random integers (device pointers or NULL)."""
     _fields_ = [("col_signs", ctypes.c_void_p), ("row_signs", ctypes.c_void_p), ("sr_row", ctypes.c_void_p),
                 ("sr_colT", ctypes.c_void_p)]
+
+
+class GemmDescC(ctypes.Structure):
+    """mxfp4_gemm_desc: one problem of a grouped GEMM launch."""
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("out_dtype", ctypes.c_int32), ("accumulate", ctypes.c_int32)]
+
+
+class PhiloxOptsC(ctypes.Structure):
+    """mxfp4_philox_opts: seeds and switches of the in-kernel Philox4x32-10 numbers."""
+    _fields_ = [("col_sign_seed", ctypes.c_uint64), ("row_sign_seed", ctypes.c_uint64), ("sr_seed", ctypes.c_uint64),
+                ("col_signs", ctypes.c_int32), ("row_signs", ctypes.c_int32),
+                ("stochastic_rounding", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class MxConfigC(ctypes.Structure):
@@ -74,14 +87,19 @@ def lib():
                 "mxfp4_scales_bytes": ([I64, I64, I, I], S),
                 "mxfp4_quantized_bytes": ([I64, I64, I, I], S),
                 "mxfp4_rotate_quantize": ([P, I64, I64, I64, I, I, U, T, T, T, P], I),
+                "mxfp4_rotate_quantize_pair": ([P, I64, I64, P, I64, I64, I64, I, I, U, T, T, T, T, P], I),
                 "mxfp4_rotate_quantize_of": ([P, I64, I64, I64, I, I, I, T, T, P], I),
                 "mxfp4_rotate_quantize_ex": ([P, I64, I64, I64, I, I, U, ctypes.POINTER(QuantOptsC), T, T, T, P], I),
                 "mxfp4_rotate_quantize_mbs": ([P, I64, I64, I64, I, I, T, P, P], I),
+                "mxfp4_rotate_quantize_philox": ([P, I64, I64, I64, I, I, U, ctypes.POINTER(PhiloxOptsC), T, T, P],
+                                                 I),
                 "mxfp4_gemm": ([T, T, P, I64, I, I, P, S, P], I),
+                "mxfp4_gemm_group": ([ctypes.POINTER(GemmDescC), I, P], I),
                 "mxfp4_workspace_bytes": ([I, I64, I64, I64, CF], S),
                 "mxfp4_linear_fprop": ([P, P, I64, I64, I64, CF, P, T, T, P, S, P], I),
                 "mxfp4_linear_dgrad": ([P, T, I64, I64, I64, CF, P, T, P, S, P], I),
                 "mxfp4_linear_wgrad": ([T, T, CF, P, P, S, P], I),
+                "mxfp4_linear_backward": ([P, T, T, I64, I64, I64, CF, P, P, P, S, P], I),
                 "mxfp4_linear_fprop_noalloc": ([P, P, I64, I64, I64, CF, P, T, T, P], I),
                 "mxfp4_noalloc_scratch_bytes": ([], S),
                 "mxfp4_error_decomposition": ([P, I64, I64, I64, I, I, P, P], I),
@@ -225,6 +243,37 @@ def rotate_quantize(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR,
     return outs
 
 
+def rotate_quantize_pair(a: torch.Tensor, b: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR,
+                         layouts: int = LAYOUT_ROW | LAYOUT_COLT, sf_layout: int = SF_MMA,
+                         outs_a: dict | None = None, outs_b: dict | None = None, stream=None) -> tuple[dict, dict]:
+    """mxfp4_rotate_quantize_pair: two bf16 CUDA matrices with the same number of columns
+    (a GEMM's operands) rotated and quantised in one launch.  Returns two dicts like
+    rotate_quantize's ({'row': QTensor, 'colT': QTensor} for the requested layouts)."""
+    for x in (a, b):
+        _check_bf16_matrix(x)
+    if a.shape[1] != b.shape[1]:
+        raise ValueError("a and b must have the same number of columns")
+    C = a.shape[1]
+    res = []
+    for x, outs in ((a, outs_a), (b, outs_b)):
+        outs = dict(outs or {})
+        R = x.shape[0]
+        if layouts & LAYOUT_ROW and "row" not in outs:
+            outs["row"] = empty_qtensor(R, C, LAYOUT_ROW, sf_layout, x.device)
+        if layouts & LAYOUT_COLT and "colT" not in outs:
+            outs["colT"] = empty_qtensor(C, R, LAYOUT_COLT, sf_layout, x.device)
+        res.append(outs)
+    cs = [{k: v.c() for k, v in o.items()} for o in res]
+    ref = lambda i, k: ctypes.byref(cs[i][k]) if k in cs[i] else None
+    _check(lib().mxfp4_rotate_quantize_pair(_ptr(a), a.shape[0], a.stride(0), _ptr(b), b.shape[0], b.stride(0), C,
+                                            had, mode, layouts, ref(0, "row"), ref(0, "colT"), ref(1, "row"),
+                                            ref(1, "colT"), _stream(stream)))
+    for o in res:
+        for v in o.values():
+            v.had, v.mode = had, mode
+    return res[0], res[1]
+
+
 def _check_bf16_matrix(x: torch.Tensor):
     if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or (x.numel() and x.stride(1) != 1):
         raise ValueError("x must be a CUDA bf16 matrix with unit column stride")
@@ -271,6 +320,30 @@ def rotate_quantize_rand(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_F
     return outs
 
 
+def rotate_quantize_philox(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR, layouts: int = LAYOUT_ROW,
+                           col_sign_seed: int | None = None, row_sign_seed: int | None = None,
+                           sr_seed: int | None = None, sf_layout: int = SF_MMA, stream=None) -> dict:
+    """mxfp4_rotate_quantize_philox: random signs (a seed per dimension) and stochastic
+    rounding (sr_seed) drawn in the kernel from Philox4x32-10; None turns an option off.
+    Returns {'row': ..., 'colT': ...} for the requested layouts."""
+    _check_bf16_matrix(x)
+    R, C = x.shape
+    outs = {}
+    if layouts & LAYOUT_ROW:
+        outs["row"] = empty_qtensor(R, C, LAYOUT_ROW, sf_layout, x.device)
+    if layouts & LAYOUT_COLT:
+        outs["colT"] = empty_qtensor(C, R, LAYOUT_COLT, sf_layout, x.device)
+    opts = PhiloxOptsC(col_sign_seed or 0, row_sign_seed or 0, sr_seed or 0, int(col_sign_seed is not None),
+                       int(row_sign_seed is not None), int(sr_seed is not None), 0)
+    cs = {k: v.c() for k, v in outs.items()}
+    ref = lambda k: ctypes.byref(cs[k]) if (k in cs) else None
+    _check(lib().mxfp4_rotate_quantize_philox(_ptr(x), R, C, x.stride(0), had, mode, layouts, ctypes.byref(opts),
+                                              ref("row"), ref("colT"), _stream(stream)))
+    for v in outs.values():
+        v.had, v.mode = had, mode
+    return outs
+
+
 def rotate_quantize_mbs(x: torch.Tensor, had: int = HAD_16, mode: int = SCALE_FLOOR, sf_layout: int = SF_MMA,
                         stream=None) -> tuple[QTensor, torch.Tensor]:
     """mxfp4_rotate_quantize_mbs: macro-block scaling, row layout.  Returns (q, mbs) with
@@ -296,6 +369,25 @@ def gemm(A: QTensor, B: QTensor, out_dtype: int = OUT_F32, accumulate: bool = Fa
     _check(lib().mxfp4_gemm(ctypes.byref(a), ctypes.byref(b), _ptr(out), out.stride(0), out_dtype, int(accumulate),
                             None, 0, _stream(stream)))
     return out
+
+
+def gemm_group(problems, stream=None) -> list:
+    """mxfp4_gemm_group: several C = A . B^T in one launch.  `problems` is a list of
+    (A, B, out_dtype, accumulate, out) tuples (out may be None: allocated here).
+    Returns the outputs in order."""
+    outs, cs, descs = [], [], []
+    for A, B, out_dtype, accumulate, out in problems:
+        if out is None:
+            dt = torch.float32 if out_dtype == OUT_F32 else torch.bfloat16
+            out = (torch.zeros if accumulate else torch.empty)((A.rows, B.rows), dtype=dt, device=A.codes.device)
+        a, b = A.c(), B.c()
+        cs += [a, b]
+        outs.append(out)
+        descs.append(GemmDescC(ctypes.addressof(a), ctypes.addressof(b), out.data_ptr(), out.stride(0), out_dtype,
+                               int(accumulate)))
+    arr = (GemmDescC * len(descs))(*descs)
+    _check(lib().mxfp4_gemm_group(arr, len(descs), _stream(stream)))
+    return outs
 
 
 @dataclass
@@ -395,6 +487,26 @@ def linear_wgrad(dyT: QTensor, xT: QTensor, cfg: Config, dw: torch.Tensor | None
     _check(lib().mxfp4_linear_wgrad(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c), _ptr(dw), None, 0,
                                     _stream(stream)))
     return dw
+
+
+def linear_backward(dy: torch.Tensor, wT: QTensor, xT: QTensor, cfg: Config, dx: torch.Tensor | None = None,
+                    dw: torch.Tensor | None = None, ws: Workspace | None = None, stream=None):
+    """dX = dY W (cfg.out_dtype) and dW = dY^T X (fp32; added to dw when cfg.accumulate)
+    from dY [M,N] bf16 and the saved W^T [K,N], X^T [K,M]: one dY quantisation and one
+    grouped GEMM launch.  Returns (dX, dW)."""
+    M, N = dy.shape
+    K = wT.rows
+    if dx is None:
+        dx = torch.empty((M, K), dtype=torch.float32 if cfg.out_dtype == OUT_F32 else torch.bfloat16,
+                         device=dy.device)
+    if dw is None:
+        dw = (torch.zeros if cfg.accumulate else torch.empty)((N, K), dtype=torch.float32, device=dy.device)
+    c, cw, cx = cfg.c(), wT.c(), xT.c()
+    nb = workspace_bytes(OP_BACKWARD, M, N, K, cfg)
+    buf = (ws or _default_ws).get(nb, dy.device)
+    _check(lib().mxfp4_linear_backward(_ptr(dy), ctypes.byref(cw), ctypes.byref(cx), M, N, K, ctypes.byref(c),
+                                       _ptr(dx), _ptr(dw), _ptr(buf), nb, _stream(stream)))
+    return dx, dw
 
 
 DECOMP_KEYS = ("e2", "scale2", "dz2", "grid2", "scale_grid", "n_deadzone", "n")

@@ -74,25 +74,73 @@ struct GemmCfg {
     static_assert(OFF_BAR % 8 == 0 && OFF_A % 1024 == 0 && OFF_B % 1024 == 0, "barrier / swizzle-atom alignment");
 };
 
-// TMA-store epilogue: lane i writes its row's 64 bytes into the warp's staging tile
-// (64-byte swizzle: 16-byte chunk j of row r at j ^ ((r >> 1) & 3), conflict-free),
-// then one lane stores the 32-row x 64-byte box with TMA (add-reduce for accumulate).
-// The staging tile is reused only after the previous store has read it.
+// Lane i writes its row's 64 bytes into a 32-row x 64-byte staging box (64-byte
+// swizzle: 16-byte chunk j of row r at j ^ ((r >> 1) & 3), conflict-free).
+__device__ __forceinline__ void stage_box(uint8_t* box, int lane, const uint32_t* w) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
+// One staged box to C with TMA (add-reduce for accumulate), skipped outside C.
+__device__ __forceinline__ void issue_box(const GemmParams& p, const uint8_t* box, int64_t row_base, int64_t col0) {
+    if (row_base < p.M && col0 < p.N) {
+        if (p.accumulate)
+            tma_reduce_add_2d(&p.map_c, box, (int32_t)col0, (int32_t)row_base);
+        else
+            tma_store_2d(&p.map_c, box, (int32_t)col0, (int32_t)row_base);
+    }
+}
+
+// TMA-store epilogue through the warp's one staging box, which is reused only after
+// the previous store has read it.
 __device__ __forceinline__ void tma_store_block(const GemmParams& p, uint8_t* stg, int lane, int64_t row_base,
                                                int64_t col0, const uint32_t* w) {
     if (lane == 0) bulk_wait_read_all();
     __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    stage_box(stg, lane, w);
     fence_async_smem();
     __syncwarp();
-    if (lane == 0 && row_base < p.M && col0 < p.N) {
-        if (p.accumulate)
-            tma_reduce_add_2d(&p.map_c, stg, (int32_t)col0, (int32_t)row_base);
-        else
-            tma_store_2d(&p.map_c, stg, (int32_t)col0, (int32_t)row_base);
+    if (lane == 0) {
+        issue_box(p, stg, row_base, col0);
+        bulk_commit();
+    }
+}
+
+// The warp's whole 32-row slice of its last tile (four 32-column chunks) staged at once
+// in `area` (8 KB bf16, 16 KB fp32; boxes 2 KB apart), then stored with back-to-back TMA
+// stores: the tile that ends the kernel does not wait on one box at a time.
+__device__ __forceinline__ void store_slice_at_once(const GemmParams& p, uint8_t* area, int lane, int64_t row_base,
+                                                   int64_t c0, const uint32_t (&v)[4][32]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (p.out_bf16) {
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const __nv_bfloat162 h =
+                    __floats2bfloat162_rn(__uint_as_float(v[c][2 * j]), __uint_as_float(v[c][2 * j + 1]));
+                w[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            stage_box(area + c * STG_WARP_BYTES, lane, w);
+        } else {
+            stage_box(area + (2 * c) * STG_WARP_BYTES, lane, v[c]);
+            stage_box(area + (2 * c + 1) * STG_WARP_BYTES, lane, v[c] + 16);
+        }
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (p.out_bf16) {
+                issue_box(p, area + c * STG_WARP_BYTES, row_base, c0 + c * 32);
+            } else {
+                issue_box(p, area + (2 * c) * STG_WARP_BYTES, row_base, c0 + c * 32);
+                issue_box(p, area + (2 * c + 1) * STG_WARP_BYTES, row_base, c0 + c * 32 + 16);
+            }
+        }
         bulk_commit();
     }
 }
@@ -342,16 +390,28 @@ struct PairCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(2 * SMEM > 228 * 1024, "one CTA per SM");
     static_assert(OFF_BAR % 8 == 0 && OFF_B % 1024 == 0 && OFF_SFA % 1024 == 0 && OFF_STG % 16 == 0, "alignment");
+    static_assert(EPI_WARPS * 8 * STG_WARP_BYTES <= OFF_SFA, "the last tile's slices fit in the A and B stages");
 };
 
+// The problem that global tile `tile` of a group belongs to, and the tile's index within
+// that problem (tiles are numbered problem after problem, row-major within each).
+__device__ __forceinline__ int group_problem(const GemmGroup& g, int64_t tile, int64_t& local) {
+    int pi = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxGemmGroup; ++i)
+        if (i < g.count && tile >= g.tile_start[i]) pi = i;
+    local = tile - g.tile_start[pi];
+    return pi;
+}
+
 template <int STAGES>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const __grid_constant__ GemmGroup g) {
     using Cfg = PairCfg<STAGES>;
     extern __shared__ uint8_t smem_raw[];
     // The layout has no slack for aligning the 128-byte-swizzled operand tiles.  Both
     // CTAs see the same base, so both return here, before any cluster barrier.
     if (smem_u32(smem_raw) & 1023u) {
-        if (threadIdx.x == 0) atomicOr(p.status, kStatusSmemLayout);
+        if (threadIdx.x == 0) atomicOr(g.status, kStatusSmemLayout);
         return;
     }
     uint8_t* smem = smem_raw;
@@ -368,11 +428,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const int num_k = (int)((p.K + 255) / 256);
-    const int64_t num_n = (p.N + 255) / 256;
-    const int64_t num_tiles = ((p.M + 255) / 256) * num_n;
+    const int64_t num_tiles = g.tile_start[g.count];
     const int64_t cluster = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
-    const int64_t atoms_per_row_block = p.kb_pad / 4;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -383,10 +440,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
         mbar_init(acc_empty, 2 * EPI_WARPS);
         mbar_init(mma_done, 1);
         fence_mbar_init();
-        prefetch_tmap(&p.map_a);
-        prefetch_tmap(&p.map_b);
-        prefetch_tmap(&p.map_sfa);
-        prefetch_tmap(&p.map_sfb);
+        for (int i = 0; i < g.count; ++i) {
+            prefetch_tmap(&g.prob[i].map_a);
+            prefetch_tmap(&g.prob[i].map_b);
+            prefetch_tmap(&g.prob[i].map_sfa);
+            prefetch_tmap(&g.prob[i].map_sfb);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_holder, Cfg::TMEM_COLS);
@@ -413,7 +472,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
             uint32_t it = 0;
             bool ok = true;
             for (int64_t tile = cluster; ok && tile < num_tiles; tile += num_clusters) {
-                const int64_t m0 = (tile / num_n) * 256, n0 = (tile % num_n) * 256;
+                int64_t lt;
+                const GemmParams& p = g.prob[group_problem(g, tile, lt)];
+                const int num_k = (int)((p.K + 255) / 256);
+                const int64_t num_n = (p.N + 255) / 256;
+                const int64_t atoms_per_row_block = p.kb_pad / 4;
+                const int64_t m0 = (lt / num_n) * 256, n0 = (lt % num_n) * 256;
                 const int32_t ya = (int32_t)(m0 + rank * 128), yb = (int32_t)(n0 + rank * 128);
                 const int32_t sfa_y = (int32_t)((m0 / 128 + rank) * atoms_per_row_block * 4);
                 const int32_t sfb_y0 = (int32_t)((n0 / 128) * atoms_per_row_block * 4);
@@ -421,11 +485,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
                 for (int kt = 0; kt < num_k; ++kt, ++it) {
                     const int s = (int)(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (it >= STAGES && !wait_bounded(&empty[s], ph ^ 1u, p.wait_ns, p.status)) {
+                    if (it >= STAGES && !wait_bounded(&empty[s], ph ^ 1u, g.wait_ns, g.status)) {
                         ok = false;
                         break;
                     }
-                    if (it == 0 && p.test_drop_first_stage && rank == 0) continue;  // fault injection
+                    if (it == 0 && g.test_drop_first_stage && rank == 0) continue;  // fault injection
                     if (rank == 0) mbar_arrive_expect_tx(&full[s], Cfg::TX_PAIR);
                     const uint32_t bar = full_leader + (uint32_t)s * 8u;
                     tma_load_2d_pair(sA + s * Cfg::A_STAGE, &p.map_a, bar, kt * BK_BYTES, ya);
@@ -443,8 +507,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
 #pragma unroll
             for (int s = 0; s < STAGES; ++s) {
                 if (!armed[s]) continue;
-                if (rank == 0) wait_bounded(&full[s], (armed[s] - 1u) & 1u, p.wait_ns, p.status);
-                wait_bounded(&empty[s], (armed[s] - 1u) & 1u, p.wait_ns, p.status);
+                if (rank == 0) wait_bounded(&full[s], (armed[s] - 1u) & 1u, g.wait_ns, g.status);
+                wait_bounded(&empty[s], (armed[s] - 1u) & 1u, g.wait_ns, g.status);
             }
         }
     } else if (warp == 1) {
@@ -455,10 +519,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
                 uint32_t it = 0, tcount = 0;
                 bool ok = true;
                 for (int64_t tile = cluster; ok && tile < num_tiles; tile += num_clusters, ++tcount) {
+                    int64_t lt;
+                    const int num_k = (int)((g.prob[group_problem(g, tile, lt)].K + 255) / 256);
                     for (int kt = 0; kt < num_k; ++kt, ++it) {
                         const int s = (int)(it % STAGES);
                         const uint32_t ph = (it / STAGES) & 1u;
-                        if (!wait_bounded(&full[s], ph, p.wait_ns, p.status)) {
+                        if (!wait_bounded(&full[s], ph, g.wait_ns, g.status)) {
                             ok = false;
                             break;
                         }
@@ -482,7 +548,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
                         // accumulator is waited for only now: the copies of a tile's first
                         // stage overlap the epilogue's read-out of the previous tile.
                         if (kt == 0 && tcount > 0) {
-                            if (!wait_bounded(acc_empty, (tcount - 1u) & 1u, p.wait_ns, p.status)) {
+                            if (!wait_bounded(acc_empty, (tcount - 1u) & 1u, g.wait_ns, g.status)) {
                                 ok = false;
                                 break;
                             }
@@ -506,7 +572,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
             }
             // Both CTAs: every MMA of the pair has completed (and this CTA's mma_done
             // arrival has landed) before TMEM is released.
-            wait_bounded(mma_done, 0, p.wait_ns, p.status);
+            wait_bounded(mma_done, 0, g.wait_ns, g.status);
         }
     } else {
         // ---------------- epilogue (both CTAs): the CTA's 128 rows of the tile
@@ -516,10 +582,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
         const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
         uint32_t tcount = 0;
         for (int64_t tile = cluster; tile < num_tiles; tile += num_clusters, ++tcount) {
-            if (!wait_bounded(acc_full, tcount & 1u, p.wait_ns, p.status)) break;
+            if (!wait_bounded(acc_full, tcount & 1u, g.wait_ns, g.status)) break;
             tc_fence_after();
-            const int64_t row_base = (tile / num_n) * 256 + rank * 128 + q * 32;
-            const int64_t c0 = (tile % num_n) * 256 + h * 128;
+            int64_t lt;
+            const GemmParams& p = g.prob[group_problem(g, tile, lt)];
+            const int64_t num_n = (p.N + 255) / 256;
+            const int64_t row_base = (lt / num_n) * 256 + rank * 128 + q * 32;
+            const int64_t c0 = (lt % num_n) * 256 + h * 128;
             uint32_t v[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -529,9 +598,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
             __syncwarp();
             // The TMEM reads above have completed (wait::ld); the arrive only reports it.
             if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_leader);
+            if (tile + num_clusters >= num_tiles) {
+                // This pair's last tile.  Its accumulator is full, so every MMA has
+                // completed, and with it every read of the operand ring and every TMA load
+                // into it: the ring is idle and takes the whole slice at once (16 KB per
+                // warp, 128 KB for the eight warps, inside the ring's A and B stages).
+                store_slice_at_once(p, smem + Cfg::OFF_A + (warp - 2) * 8 * STG_WARP_BYTES, lane, row_base, c0, v);
+            } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                store_chunk_tma(p, stg, lane, row_base, c0 + c * 32, v[c]);
+                for (int c = 0; c < 4; ++c) {
+                    store_chunk_tma(p, stg, lane, row_base, c0 + c * 32, v[c]);
+                }
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -567,7 +644,7 @@ cudaError_t launch_cfg(const GemmParams& p, cudaStream_t s) {
 // Returns cudaErrorNotSupported (nothing launched) when no cluster of two CTAs can be
 // resident on this device, so the caller can fall back to the single-CTA kernel.
 template <int STAGES>
-cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
+cudaError_t launch_pair(const GemmGroup& g, cudaStream_t s) {
     using Cfg = PairCfg<STAGES>;
     auto kern = mxf4_gemm_pair_kernel<STAGES>;
     static DeviceSlots cluster_slots;
@@ -595,10 +672,35 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
     });
     if (e != cudaSuccess) return e;
     if (max_clusters < 1) return cudaErrorNotSupported;
-    const int64_t tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
+    const int64_t tiles = g.tile_start[g.count];
     const int64_t clusters = tiles < max_clusters ? tiles : max_clusters;
     return launch_overlapped(kern, dim3((unsigned)(2 * clusters)), dim3(GEMM_THREADS), Cfg::SMEM, s, 2,
-                             MXF_PDL_GEMM != 0, p);
+                             MXF_PDL_GEMM != 0, g);
+}
+
+// A group of one, or several problems ordered by contraction length (longest first:
+// the static round-robin schedule then ends on the shortest tiles).
+GemmGroup make_group(const GemmParams* probs, int n) {
+    GemmGroup g{};
+    int order[kMaxGemmGroup];
+    for (int i = 0; i < n; ++i) order[i] = i;
+    for (int i = 1; i < n; ++i)  // stable insertion sort by K, descending
+        for (int j = i; j > 0 && probs[order[j]].K > probs[order[j - 1]].K; --j) {
+            const int t = order[j];
+            order[j] = order[j - 1];
+            order[j - 1] = t;
+        }
+    g.count = n;
+    g.tile_start[0] = 0;
+    for (int i = 0; i < n; ++i) {
+        const GemmParams& p = probs[order[i]];
+        g.prob[i] = p;
+        g.tile_start[i + 1] = g.tile_start[i] + ((p.M + 255) / 256) * ((p.N + 255) / 256);
+    }
+    g.status = probs[0].status;
+    g.wait_ns = probs[0].wait_ns;
+    g.test_drop_first_stage = probs[0].test_drop_first_stage;
+    return g;
 }
 
 }  // namespace
@@ -609,7 +711,7 @@ cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s) {
 #if MXG_PAIR
     if (p.M > 128 && p.N > 128) {
-        const cudaError_t e = launch_pair<MXG_PAIR_STAGES>(p, s);
+        const cudaError_t e = launch_pair<MXG_PAIR_STAGES>(make_group(&p, 1), s);
         if (e != cudaErrorNotSupported) return e;
     }
 #endif
@@ -619,6 +721,20 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s) {
 #else
     return launch_cfg<256, MXG_STAGES_256, 1>(p, s);
 #endif
+}
+
+// Several GEMMs in one persistent launch of the CTA-pair kernel (1 <= n <=
+// kMaxGemmGroup); a group of one takes launch_gemm's kernel choice.
+cudaError_t launch_gemm_group(const GemmParams* probs, int n, cudaStream_t s) {
+    if (n < 1 || n > kMaxGemmGroup) return cudaErrorInvalidValue;
+    if (n == 1) return launch_gemm(probs[0], s);
+    const cudaError_t e = launch_pair<MXG_PAIR_STAGES>(make_group(probs, n), s);
+    if (e != cudaErrorNotSupported) return e;
+    for (int i = 0; i < n; ++i) {  // no pair cluster fits: one launch per problem
+        const cudaError_t ei = launch_gemm(probs[i], s);
+        if (ei != cudaSuccess) return ei;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace mx

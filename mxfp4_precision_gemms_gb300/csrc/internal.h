@@ -36,6 +36,10 @@ struct QuantParams {
 
 // Launches the fused rotate+quantise kernel for the requested layouts.
 cudaError_t launch_rotate_quantize(const QuantParams& p, int had, unsigned layouts, cudaStream_t s);
+// The same for two matrices with the same number of columns (C) in one launch (row and
+// transposed layouts; both get the same layouts, rotation and scale rule).
+cudaError_t launch_rotate_quantize_pair(const QuantParams& a, const QuantParams& b, int had, unsigned layouts,
+                                        cudaStream_t s);
 // Quantiser fixes (row layout): OF writes Q(v) to p.row and Q(v - dq(Q(v))) to q2;
 // MBS writes Q((1 + k/256) v) to p.row and the bytes k to mbs [R, C/128].
 cudaError_t launch_rotate_quantize_of(const QuantParams& p, const QuantOut& q2, int had, int alpha_log2,
@@ -49,6 +53,11 @@ struct RandOpts {
     const uint8_t* row_signs;  // over R, for the transposed copy
     const uint16_t* sr_row;    // [R, C]
     const uint16_t* sr_colT;   // [C, R]
+    // Generated instead (gen = 1): Philox4x32-10 sign vectors and stochastic-rounding
+    // integers, keyed by these seeds (the arrays above are then unused).
+    int32_t gen;
+    int32_t col_sign_on, row_sign_on, sr_on;
+    uint64_t col_sign_seed, row_sign_seed, sr_seed;
 };
 cudaError_t launch_rotate_quantize_rand(const QuantParams& p, const RandOpts& o, int had, unsigned layouts,
                                         cudaStream_t s);
@@ -72,6 +81,20 @@ struct GemmParams {
 };
 
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s);
+
+// Up to kMaxGemmGroup GEMMs in one persistent launch: one static tile schedule over
+// the problems' 256 x 256 tiles (problem after problem, tile_start[i] = the first global
+// tile of problem i, tile_start[count] = all tiles).
+constexpr int kMaxGemmGroup = 8;
+struct GemmGroup {
+    GemmParams prob[kMaxGemmGroup];
+    int64_t tile_start[kMaxGemmGroup + 1];
+    int32_t count;
+    uint32_t* status;
+    uint64_t wait_ns;
+    int32_t test_drop_first_stage;
+};
+cudaError_t launch_gemm_group(const GemmParams* probs, int n, cudaStream_t s);
 
 cudaError_t run_mma_peak_probe(int kind, int64_t iters, float* ms, int* ctas, uint32_t* status, uint64_t wait_ns);
 

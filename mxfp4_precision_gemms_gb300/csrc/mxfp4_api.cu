@@ -50,12 +50,39 @@ uint64_t wait_limit() { return t_wait_ns ? t_wait_ns : kDefaultWaitNs; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static std::atomic<CtxGetCurrentFn> fn{nullptr};
+    CtxGetCurrentFn f = fn.load();
+    if (!f) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            f = reinterpret_cast<CtxGetCurrentFn>(p);
+            fn.store(f);
+        }
+    }
+    return f;
+}
+
 // Checks that the current device is a GB300 (compute capability 10.3) and looks up
-// the device address of its status word once.
+// the device address of its status word once.  It also makes sure the calling thread
+// has a current context: the runtime binds the device's primary context to a thread
+// only at that thread's first call that needs one, and the tensor-map encoder (a
+// driver call) runs before any launch -- a thread that has made no launch yet (for
+// example an autograd worker thread) would otherwise encode without a context.
 mxfp4_status check_device(int* dev_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+        e = cudaSetDevice(dev);  // binds (and if needed initialises) the primary context
+        if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    }
     if (dev < 0 || dev >= kMaxDevices) return fail(MXFP4_ERR_UNSUPPORTED_DEVICE, "device index %d", dev);
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_device_ok[dev] == 0) {
@@ -101,6 +128,9 @@ EncodeTiledFn encode_fn() {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+thread_local int t_encode_result = 0;  // CUresult of this thread's last tensor-map encode
+int last_encode_result() { return t_encode_result; }
+
 bool valid_had(int h) { return h == 0 || h == 16 || h == 32; }
 bool valid_mode(int m) { return m == 0 || m == 1; }
 
@@ -129,9 +159,9 @@ bool encode_codes_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t
     const cuuint64_t strides[1] = {(cuuint64_t)(cols / 2)};
     const cuuint32_t box[2] = {128, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, estr,
+    return (t_encode_result = f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE)) == CUDA_SUCCESS;
 }
 
 // 2D tensor map over the GEMM output C [rows, cols] (bf16 or fp32, leading dimension
@@ -144,9 +174,9 @@ bool encode_out_map(CUtensorMap* map, void* c, int64_t rows, int64_t cols, int64
     const cuuint64_t strides[1] = {(cuuint64_t)(ldc * esz)};
     const cuuint32_t box[2] = {(cuuint32_t)(64 / esz), 32};
     const cuuint32_t estr[2] = {1, 1};
-    return f(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, c, dims, strides, box,
+    return (t_encode_result = f(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, c, dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE)) == CUDA_SUCCESS;
 }
 
 // 2D tensor map over MMA-order scale factors of a [rows, cols] operand, viewed as
@@ -159,9 +189,9 @@ bool encode_sf_map(CUtensorMap* map, const void* scales, int64_t rows, int64_t c
     const cuuint64_t strides[1] = {128};
     const cuuint32_t box[2] = {128, 8};
     const cuuint32_t estr[2] = {1, 1};
-    return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(scales), dims, strides, box, estr,
+    return (t_encode_result = f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(scales), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE)) == CUDA_SUCCESS;
 }
 
 }  // namespace mx
@@ -362,9 +392,82 @@ mxfp4_status rq_launch(const void* x, int64_t rows, int64_t cols, int64_t ld, in
     return ok();
 }
 
+// Both matrices of a validated pair call (same cols, same layouts), on a checked device:
+// descriptors filled, MMA scale padding cleared, one launch.
+mxfp4_status rq_pair_launch(const void* a, int64_t a_rows, int64_t a_ld, const void* b, int64_t b_rows, int64_t b_ld,
+                            int64_t cols, int had, int mode, unsigned layouts, mxfp4_tensor* a_row,
+                            mxfp4_tensor* a_colT, mxfp4_tensor* b_row, mxfp4_tensor* b_colT, cudaStream_t s) {
+    const bool want_row = layouts & MXFP4_LAYOUT_ROW, want_colT = layouts & MXFP4_LAYOUT_COLT;
+    if (want_row) {
+        fill_desc(a_row, a_rows, cols, MXFP4_LAYOUT_ROW, had, mode);
+        fill_desc(b_row, b_rows, cols, MXFP4_LAYOUT_ROW, had, mode);
+    }
+    if (want_colT) {
+        fill_desc(a_colT, cols, a_rows, MXFP4_LAYOUT_COLT, had, mode);
+        fill_desc(b_colT, cols, b_rows, MXFP4_LAYOUT_COLT, had, mode);
+    }
+    for (mxfp4_tensor* t : {want_row ? a_row : nullptr, want_colT ? a_colT : nullptr, want_row ? b_row : nullptr,
+                            want_colT ? b_colT : nullptr}) {
+        if (needs_sf_padding(t)) {
+            cudaError_t e =
+                cudaMemsetAsync(t->scales, 0, mxfp4_scales_bytes(t->rows, t->cols, t->layout, t->sf_layout), s);
+            if (e != cudaSuccess) return cuda_fail(e, "clear scale padding");
+        }
+    }
+    QuantParams pa{}, pb{};
+    pa.x = static_cast<const uint16_t*>(a);
+    pa.R = a_rows;
+    pa.C = cols;
+    pa.ld = a_ld;
+    pa.mode = mode;
+    pa.row = to_out(want_row ? a_row : nullptr);
+    pa.colT = to_out(want_colT ? a_colT : nullptr);
+    pb = pa;
+    pb.x = static_cast<const uint16_t*>(b);
+    pb.R = b_rows;
+    pb.ld = b_ld;
+    pb.row = to_out(want_row ? b_row : nullptr);
+    pb.colT = to_out(want_colT ? b_colT : nullptr);
+    cudaError_t e = launch_rotate_quantize_pair(pa, pb, had, layouts, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize_pair launch");
+    return ok();
+}
+
 }  // namespace
 
 extern "C" {
+
+mxfp4_status mxfp4_rotate_quantize_pair(const void* a, int64_t a_rows, int64_t a_ld, const void* b, int64_t b_rows,
+                                        int64_t b_ld, int64_t cols, int had, int mode, unsigned layouts,
+                                        mxfp4_tensor* a_row, mxfp4_tensor* a_colT, mxfp4_tensor* b_row,
+                                        mxfp4_tensor* b_colT, mxfp4_stream_t stream) {
+    if (layouts & MXFP4_LAYOUT_2D) return fail(MXFP4_ERR_INVALID_ARG, "the pair call makes row and column copies only");
+    bool ea, eb;
+    mxfp4_status st;
+    if ((st = rq_validate(a, a_rows, cols, a_ld, had, mode, layouts, a_row, a_colT, nullptr, &ea))) return st;
+    if ((st = rq_validate(b, b_rows, cols, b_ld, had, mode, layouts, b_row, b_colT, nullptr, &eb))) return st;
+    if ((a_rows + 63) / 64 + (b_rows + 63) / 64 > 65535)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "too many rows for one launch");
+    int dev;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (ea || eb) {  // one side is empty: the other (if any) on its own
+        if (ea) {
+            if (layouts & MXFP4_LAYOUT_ROW) fill_desc(a_row, a_rows, cols, MXFP4_LAYOUT_ROW, had, mode);
+            if (layouts & MXFP4_LAYOUT_COLT) fill_desc(a_colT, cols, a_rows, MXFP4_LAYOUT_COLT, had, mode);
+        }
+        if (eb) {
+            if (layouts & MXFP4_LAYOUT_ROW) fill_desc(b_row, b_rows, cols, MXFP4_LAYOUT_ROW, had, mode);
+            if (layouts & MXFP4_LAYOUT_COLT) fill_desc(b_colT, cols, b_rows, MXFP4_LAYOUT_COLT, had, mode);
+        }
+        if (ea && eb) return ok();
+        if ((st = check_device(&dev))) return st;
+        return ea ? rq_launch(b, b_rows, cols, b_ld, had, mode, layouts, b_row, b_colT, nullptr, s)
+                  : rq_launch(a, a_rows, cols, a_ld, had, mode, layouts, a_row, a_colT, nullptr, s);
+    }
+    if ((st = check_device(&dev))) return st;
+    return rq_pair_launch(a, a_rows, a_ld, b, b_rows, b_ld, cols, had, mode, layouts, a_row, a_colT, b_row, b_colT,
+                          s);
+}
 
 mxfp4_status mxfp4_rotate_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
                                    unsigned layouts, mxfp4_tensor* row_out, mxfp4_tensor* colT_out,
@@ -574,13 +677,16 @@ mxfp4_status gemm_validate(const mxfp4_tensor* A, const mxfp4_tensor* B, const v
 // driver call, no launch).
 mxfp4_status gemm_prepare(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, int64_t ldc, int out_dtype,
                           int accumulate, GemmParams* p) {
+    if (reinterpret_cast<uintptr_t>(p) & 63u)
+        return fail(MXFP4_ERR_CUDA, "internal: GEMM parameter block not 64-byte aligned");
     *p = GemmParams{};
-    if (!encode_codes_map(&p->map_a, A->codes, A->rows, A->cols, 128) ||
-        !encode_codes_map(&p->map_b, B->codes, B->rows, B->cols, 128) ||
-        !encode_out_map(&p->map_c, C, A->rows, B->rows, ldc, out_dtype == MXFP4_OUT_BF16) ||
-        !encode_sf_map(&p->map_sfa, A->scales, A->rows, A->cols) ||
-        !encode_sf_map(&p->map_sfb, B->scales, B->rows, B->cols))
-        return fail(MXFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    const char* which = !encode_codes_map(&p->map_a, A->codes, A->rows, A->cols, 128) ? "A codes"
+                        : !encode_codes_map(&p->map_b, B->codes, B->rows, B->cols, 128) ? "B codes"
+                        : !encode_out_map(&p->map_c, C, A->rows, B->rows, ldc, out_dtype == MXFP4_OUT_BF16) ? "C"
+                        : !encode_sf_map(&p->map_sfa, A->scales, A->rows, A->cols) ? "A scales"
+                        : !encode_sf_map(&p->map_sfb, B->scales, B->rows, B->cols) ? "B scales"
+                                                                                      : nullptr;
+    if (which) return fail(MXFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed for %s (CUresult %d)", which, last_encode_result());
     p->sfa = A->scales;
     p->sfb = B->scales;
     p->M = A->rows;
@@ -593,6 +699,14 @@ mxfp4_status gemm_prepare(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C,
     p->accumulate = accumulate ? 1 : 0;
     return MXFP4_OK;
 }
+
+// The GEMM's parameter block, placed by hand on a 64-byte boundary: the driver's
+// tensor-map encoder requires it, and a host stack (for example an autograd worker
+// thread's) need not honour the alignas(64) of a local CUtensorMap.
+struct GemmParamsBox {
+    unsigned char raw[sizeof(GemmParams) + 64];
+    GemmParams* get() { return reinterpret_cast<GemmParams*>((reinterpret_cast<uintptr_t>(raw) + 63) & ~uintptr_t(63)); }
+};
 
 mxfp4_status gemm_launch(GemmParams& p, cudaStream_t s) {
     p.status = device_status_ptr();
@@ -610,6 +724,45 @@ mxfp4_status gemm_launch(GemmParams& p, cudaStream_t s) {
 
 extern "C" {
 
+mxfp4_status mxfp4_rotate_quantize_philox(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
+                                          unsigned layouts, const mxfp4_philox_opts* opts, mxfp4_tensor* row_out,
+                                          mxfp4_tensor* colT_out, mxfp4_stream_t stream) {
+    if (!opts) return fail(MXFP4_ERR_INVALID_ARG, "opts is NULL");
+    if (opts->reserved != 0) return fail(MXFP4_ERR_INVALID_ARG, "opts.reserved must be 0");
+    if ((layouts & MXFP4_LAYOUT_2D) || !layouts || (layouts & ~3u))
+        return fail(MXFP4_ERR_INVALID_ARG, "random signs / stochastic rounding: row and column layouts only");
+    bool empty;
+    mxfp4_status st = rq_validate(x, rows, cols, ld, had, mode, layouts, row_out, colT_out, nullptr, &empty);
+    if (st) return st;
+    const bool want_row = layouts & MXFP4_LAYOUT_ROW, want_colT = layouts & MXFP4_LAYOUT_COLT;
+    if (want_row) fill_desc(row_out, rows, cols, MXFP4_LAYOUT_ROW, had, mode);
+    if (want_colT) fill_desc(colT_out, cols, rows, MXFP4_LAYOUT_COLT, had, mode);
+    if (empty) return ok();
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = clear_padding({want_row ? row_out : nullptr, want_colT ? colT_out : nullptr}, s))) return st;
+    QuantParams p{};
+    p.x = static_cast<const uint16_t*>(x);
+    p.R = rows;
+    p.C = cols;
+    p.ld = ld;
+    p.mode = mode;
+    p.row = to_out(want_row ? row_out : nullptr);
+    p.colT = to_out(want_colT ? colT_out : nullptr);
+    RandOpts o{};
+    o.gen = 1;
+    o.col_sign_on = opts->col_signs != 0;
+    o.row_sign_on = opts->row_signs != 0;
+    o.sr_on = opts->stochastic_rounding != 0;
+    o.col_sign_seed = opts->col_sign_seed;
+    o.row_sign_seed = opts->row_sign_seed;
+    o.sr_seed = opts->sr_seed;
+    cudaError_t e = launch_rotate_quantize_rand(p, o, had, layouts, s);
+    if (e != cudaSuccess) return cuda_fail(e, "rotate_quantize_philox launch");
+    return ok();
+}
+
 mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, int64_t ldc, int out_dtype,
                         int accumulate, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
     (void)ws;
@@ -618,9 +771,56 @@ mxfp4_status mxfp4_gemm(const mxfp4_tensor* A, const mxfp4_tensor* B, void* C, i
     if ((st = gemm_validate(A, B, C, ldc, out_dtype, accumulate))) return st;
     int dev;
     if ((st = check_device(&dev))) return st;
-    GemmParams p;
-    if ((st = gemm_prepare(A, B, C, ldc, out_dtype, accumulate, &p))) return st;
-    return gemm_launch(p, reinterpret_cast<cudaStream_t>(stream));
+    GemmParamsBox box;
+    GemmParams* p = box.get();
+    if ((st = gemm_prepare(A, B, C, ldc, out_dtype, accumulate, p))) return st;
+    return gemm_launch(*p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mxfp4_status mxfp4_gemm_group(const mxfp4_gemm_desc* descs, int count, mxfp4_stream_t stream) {
+    if (!descs || count < 1 || count > kMaxGemmGroup)
+        return fail(MXFP4_ERR_INVALID_ARG, "count must be 1 to %d with descs non-NULL (got %d)", kMaxGemmGroup, count);
+    mxfp4_status st;
+    for (int i = 0; i < count; ++i) {
+        const mxfp4_gemm_desc& d = descs[i];
+        if ((st = gemm_validate(d.A, d.B, d.C, d.ldc, d.out_dtype, d.accumulate))) {
+            char msg[512];
+            snprintf(msg, sizeof msg, "%s", t_last_error);
+            return fail(st, "problem %d: %s", i, msg);
+        }
+    }
+    // No two outputs may share a byte: the problems run concurrently.
+    for (int i = 0; i < count; ++i)
+        for (int j = i + 1; j < count; ++j) {
+            auto span = [](const mxfp4_gemm_desc& d, uintptr_t* lo, uintptr_t* hi) {
+                const uintptr_t esz = d.out_dtype == MXFP4_OUT_BF16 ? 2 : 4;
+                *lo = reinterpret_cast<uintptr_t>(d.C);
+                *hi = *lo + ((uintptr_t)(d.A->rows - 1) * (uintptr_t)d.ldc + (uintptr_t)d.B->rows) * esz;
+            };
+            uintptr_t a0, a1, b0, b1;
+            span(descs[i], &a0, &a1);
+            span(descs[j], &b0, &b1);
+            if (a0 < b1 && b0 < a1) return fail(MXFP4_ERR_INVALID_ARG, "outputs of problems %d and %d overlap", i, j);
+        }
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    struct Box {
+        unsigned char raw[kMaxGemmGroup * sizeof(GemmParams) + 64];
+    } box;
+    GemmParams* ps = reinterpret_cast<GemmParams*>((reinterpret_cast<uintptr_t>(box.raw) + 63) & ~uintptr_t(63));
+    for (int i = 0; i < count; ++i) {
+        const mxfp4_gemm_desc& d = descs[i];
+        if ((st = gemm_prepare(d.A, d.B, d.C, d.ldc, d.out_dtype, d.accumulate, ps + i))) return st;
+        ps[i].status = device_status_ptr();
+        ps[i].wait_ns = wait_limit();
+    }
+    if (t_inject_gemm_faults > 0) {
+        --t_inject_gemm_faults;
+        ps[0].test_drop_first_stage = 1;
+    }
+    cudaError_t e = launch_gemm_group(ps, count, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gemm group launch");
+    return ok();
 }
 
 mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
@@ -670,6 +870,9 @@ size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, const mxfp
             return mxfp4_quantized_bytes(M, N, MXFP4_LAYOUT_ROW, MXFP4_SF_MMA);
         case MXFP4_OP_WGRAD:
             return 0;
+        case MXFP4_OP_BACKWARD:
+            return mxfp4_quantized_bytes(M, N, MXFP4_LAYOUT_ROW, MXFP4_SF_MMA) +
+                   mxfp4_quantized_bytes(N, M, MXFP4_LAYOUT_COLT, MXFP4_SF_MMA);
     }
     return 0;
 }
@@ -735,12 +938,19 @@ mxfp4_status mxfp4_linear_fprop(const void* x, const void* w, int64_t M, int64_t
     if ((st = gemm_validate(&xq, &wq, y, N, cfg->out_dtype, cfg->accumulate))) return st;
     int dev;
     if ((st = check_device(&dev))) return st;
-    GemmParams gp;
-    if ((st = gemm_prepare(&xq, &wq, y, N, cfg->out_dtype, cfg->accumulate, &gp))) return st;
+    GemmParamsBox box;
+    GemmParams* gp = box.get();
+    if ((st = gemm_prepare(&xq, &wq, y, N, cfg->out_dtype, cfg->accumulate, gp))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if ((st = rq_launch(x, M, K, K, cfg->had, cfg->mode, lx, &xq, save_xT, nullptr, s))) return st;
-    if ((st = rq_launch(w, N, K, K, cfg->had, cfg->mode, lw, &wq, save_wT, nullptr, s))) return st;
-    return gemm_launch(gp, s);
+    if (lx == lw && (M + 63) / 64 + (N + 63) / 64 <= 65535) {
+        // X and W in one launch: they share the contraction K
+        if ((st = rq_pair_launch(x, M, K, w, N, K, K, cfg->had, cfg->mode, lx, &xq, save_xT, &wq, save_wT, s)))
+            return st;
+    } else {
+        if ((st = rq_launch(x, M, K, K, cfg->had, cfg->mode, lx, &xq, save_xT, nullptr, s))) return st;
+        if ((st = rq_launch(w, N, K, K, cfg->had, cfg->mode, lw, &wq, save_wT, nullptr, s))) return st;
+    }
+    return gemm_launch(*gp, s);
 }
 
 mxfp4_status mxfp4_linear_dgrad(const void* dy, const mxfp4_tensor* wT, int64_t M, int64_t N, int64_t K,
@@ -770,11 +980,68 @@ mxfp4_status mxfp4_linear_dgrad(const void* dy, const mxfp4_tensor* wT, int64_t 
     if ((st = gemm_validate(&dyq, wT, dx, K, cfg->out_dtype, cfg->accumulate))) return st;
     int dev;
     if ((st = check_device(&dev))) return st;
-    GemmParams gp;
-    if ((st = gemm_prepare(&dyq, wT, dx, K, cfg->out_dtype, cfg->accumulate, &gp))) return st;
+    GemmParamsBox box;
+    GemmParams* gp = box.get();
+    if ((st = gemm_prepare(&dyq, wT, dx, K, cfg->out_dtype, cfg->accumulate, gp))) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if ((st = rq_launch(dy, M, N, N, cfg->had, cfg->mode, ld_, &dyq, save_dyT, nullptr, s))) return st;
-    return gemm_launch(gp, s);
+    return gemm_launch(*gp, s);
+}
+
+mxfp4_status mxfp4_linear_backward(const void* dy, const mxfp4_tensor* wT, const mxfp4_tensor* xT, int64_t M,
+                                   int64_t N, int64_t K, const mxfp4_config* cfg, void* dx, void* dw, void* ws,
+                                   size_t ws_bytes, mxfp4_stream_t stream) {
+    mxfp4_status st;
+    if ((st = check_cfg(cfg))) return st;
+    if (!dy || !wT || !xT || !dx || !dw) return fail(MXFP4_ERR_INVALID_ARG, "dy, wT, xT, dx and dw must be non-NULL");
+    if (M <= 0 || N <= 0 || K <= 0) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "M, N, K must be positive");
+    if (N % 32 || M % 32) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "N and M must be multiples of 32");
+    if (wT->rows != K || wT->cols != N)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "wT must be [K, N] = [%lld, %lld]", (long long)K, (long long)N);
+    if (xT->rows != K || xT->cols != M)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "xT must be [K, M] = [%lld, %lld]", (long long)K, (long long)M);
+    if (wT->layout != MXFP4_LAYOUT_COLT || xT->layout != MXFP4_LAYOUT_COLT)
+        return fail(MXFP4_ERR_INVALID_ARG, "wT and xT must be transposed copies");
+    if (wT->had != cfg->had || wT->mode != cfg->mode || xT->had != cfg->had || xT->mode != cfg->mode)
+        return fail(MXFP4_ERR_INVALID_ARG, "wT and xT must be quantised with the layer's had %d / mode %d", cfg->had,
+                    cfg->mode);
+    if ((st = check_ws(ws, ws_bytes, mxfp4_workspace_bytes(MXFP4_OP_BACKWARD, M, N, K, cfg)))) return st;
+    uint8_t* cur = static_cast<uint8_t*>(ws);
+    mxfp4_tensor dyq = carve(cur, M, N);
+    mxfp4_tensor dyT{};
+    dyT.codes = cur;
+    dyT.scales = cur + round_up(mxfp4_codes_bytes(N, M), 256);
+    dyT.sf_layout = MXFP4_SF_MMA;
+    const unsigned lay = MXFP4_LAYOUT_ROW | MXFP4_LAYOUT_COLT;
+    bool empty;
+    if ((st = rq_validate(dy, M, N, N, cfg->had, cfg->mode, lay, &dyq, &dyT, nullptr, &empty))) return st;
+    fill_desc(&dyq, M, N, MXFP4_LAYOUT_ROW, cfg->had, cfg->mode);
+    fill_desc(&dyT, N, M, MXFP4_LAYOUT_COLT, cfg->had, cfg->mode);
+    // dX = dY W in cfg->out_dtype (no accumulation); dW = dY^T X in fp32, added to dw
+    // when cfg->accumulate (gradient accumulation over micro-batches).
+    if ((st = gemm_validate(&dyq, wT, dx, K, cfg->out_dtype, 0))) return st;
+    if ((st = gemm_validate(&dyT, xT, dw, K, MXFP4_OUT_F32, cfg->accumulate))) return st;
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    struct Box {
+        unsigned char raw[2 * sizeof(GemmParams) + 64];
+    } box;
+    GemmParams* gp = reinterpret_cast<GemmParams*>((reinterpret_cast<uintptr_t>(box.raw) + 63) & ~uintptr_t(63));
+    if ((st = gemm_prepare(&dyq, wT, dx, K, cfg->out_dtype, 0, gp))) return st;
+    if ((st = gemm_prepare(&dyT, xT, dw, K, MXFP4_OUT_F32, cfg->accumulate, gp + 1))) return st;
+    for (int i = 0; i < 2; ++i) {
+        gp[i].status = device_status_ptr();
+        gp[i].wait_ns = wait_limit();
+    }
+    if (t_inject_gemm_faults > 0) {
+        --t_inject_gemm_faults;
+        gp[0].test_drop_first_stage = 1;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = rq_launch(dy, M, N, N, cfg->had, cfg->mode, lay, &dyq, &dyT, nullptr, s))) return st;
+    cudaError_t e = launch_gemm_group(gp, 2, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward gemm launch");
+    return ok();
 }
 
 mxfp4_status mxfp4_linear_wgrad(const mxfp4_tensor* dyT, const mxfp4_tensor* xT, const mxfp4_config* cfg,

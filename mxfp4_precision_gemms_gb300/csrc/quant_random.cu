@@ -9,12 +9,59 @@
 //     term exact in fp32; a >= 6 saturates; the sign is kept.
 // Same tiling as rq_kernel (64 x 128 tiles, 128 threads, bf16 tile staged in shared
 // memory for the column work, transposed rows exchanged within a warp).
+//
+// Or the kernel draws them itself (GEN) from Philox4x32-10 (Salmon, Moraes, Dror and
+// Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC'11), a counter-based
+// generator, with a fixed counter layout (so any element's numbers can be recomputed):
+//   sign bit j of a dimension's vector: bit j % 32 of output word (j % 128) / 32 of
+//     Philox(counter (j / 128, 0, 0, 0), key = the dimension's 64-bit seed);
+//   stochastic-rounding integer of (line l, position i) of copy c (0 row, 1 transposed):
+//     16-bit half i % 8 (word (i % 8) / 2, low half first) of
+//     Philox(counter (i / 8, l, c, 0), key = the SR seed).
+// A GEMM's two operands share their contraction's sign vector by sharing its seed.
 #include "quant_math.cuh"
 
 namespace mx {
 namespace {
 
 constexpr int RQ_TR = 64, RQ_TC = 128, RQ_THREADS = 128;
+
+// Philox4x32-10: ten rounds of (c0, c1, c2, c3) -> (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2),
+// hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)) with M0 = 0xD2511F53, M1 = 0xCD9E8D57, the key
+// bumped by (0x9E3779B9, 0xBB67AE85) between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t h0 = __umulhi(0xD2511F53u, c.x), l0 = 0xD2511F53u * c.x;
+        const uint32_t h1 = __umulhi(0xCD9E8D57u, c.z), l1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(h1 ^ c.y ^ k0, l1, h0 ^ c.w ^ k1, l0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// 32 sign bits of a dimension's vector starting at index j0 (a multiple of 32).
+__device__ __forceinline__ uint32_t philox_sign_word(uint64_t seed, int64_t j0) {
+    const uint4 o = philox4x32_10(make_uint4((uint32_t)(j0 >> 7), 0u, 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
+    const int w = (int)((j0 >> 5) & 3);
+    return w == 0 ? o.x : w == 1 ? o.y : w == 2 ? o.z : o.w;
+}
+
+// The 32 stochastic-rounding integers of positions i0 .. i0 + 31 (i0 a multiple of 8) of
+// line `line` of copy `copy`, two per word, in the layout load_r produces.
+__device__ __forceinline__ void philox_sr32(uint64_t seed, int64_t i0, int64_t line, uint32_t copy,
+                                            uint32_t (&w)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 o = philox4x32_10(make_uint4((uint32_t)((i0 >> 3) + j), (uint32_t)line, copy, 0u),
+                                      (uint32_t)seed, (uint32_t)(seed >> 32));
+        w[4 * j] = o.x;
+        w[4 * j + 1] = o.y;
+        w[4 * j + 2] = o.z;
+        w[4 * j + 3] = o.w;
+    }
+}
 
 // Stochastically rounded grid value of u with the 16-bit integer r.
 __device__ __forceinline__ float sr_grid(float u, uint32_t r) {
@@ -72,7 +119,7 @@ __device__ __forceinline__ void load_r(const uint16_t* src, bool valid, uint32_t
     }
 }
 
-template <int HAD, bool ROW, bool COLT, bool SR>
+template <int HAD, bool ROW, bool COLT, bool SR, bool GEN>
 __global__ void __launch_bounds__(RQ_THREADS, SR ? 4 : 6) rq_rand_kernel(const QuantParams p, const RandOpts o) {
     __shared__ __align__(16) uint32_t tile[COLT ? RQ_TR * RQ_TC / 2 : 4];
     const int t = threadIdx.x;
@@ -93,7 +140,11 @@ __global__ void __launch_bounds__(RQ_THREADS, SR ? 4 : 6) rq_rand_kernel(const Q
     }
 
     if constexpr (ROW) {
-        const uint32_t bits = (o.col_signs && gc < p.C) ? *reinterpret_cast<const uint32_t*>(o.col_signs + gc / 8) : 0u;
+        uint32_t bits;
+        if constexpr (GEN)
+            bits = o.col_sign_on ? philox_sign_word(o.col_sign_seed, gc) : 0u;
+        else
+            bits = (o.col_signs && gc < p.C) ? *reinterpret_cast<const uint32_t*>(o.col_signs + gc / 8) : 0u;
         float2 v[32];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -115,8 +166,13 @@ __global__ void __launch_bounds__(RQ_THREADS, SR ? 4 : 6) rq_rand_kernel(const Q
         uint4 qx, qy;
         if constexpr (SR) {
             uint32_t r_x[16], r_y[16];
-            load_r(o.sr_row + grx * p.C + gc, vx, r_x);
-            load_r(o.sr_row + gry * p.C + gc, vy, r_y);
+            if constexpr (GEN) {
+                philox_sr32(o.sr_seed, gc, grx, 0u, r_x);
+                philox_sr32(o.sr_seed, gc, gry, 0u, r_y);
+            } else {
+                load_r(o.sr_row + grx * p.C + gc, vx, r_x);
+                load_r(o.sr_row + gry * p.C + gc, vy, r_y);
+            }
             quant32x2_sr<HAD>(v, bytex, bytey, r_x, r_y, qx, qy);
         } else {
             quant32x2<HAD>(v, bytex, bytey, qx, qy);
@@ -135,7 +191,11 @@ __global__ void __launch_bounds__(RQ_THREADS, SR ? 4 : 6) rq_rand_kernel(const Q
         const int rb = lane >> 4, cp = 16 * (t >> 5) + (lane & 15);
         const int64_t gcol = col0 + 2 * cp, grow = row0 + 32 * rb;
         const bool valid = gcol < p.C && grow < p.R;
-        const uint32_t bits = (o.row_signs && valid) ? *reinterpret_cast<const uint32_t*>(o.row_signs + grow / 8) : 0u;
+        uint32_t bits;
+        if constexpr (GEN)
+            bits = o.row_sign_on ? philox_sign_word(o.row_sign_seed, grow) : 0u;
+        else
+            bits = (o.row_signs && valid) ? *reinterpret_cast<const uint32_t*>(o.row_signs + grow / 8) : 0u;
         float2 v[32];
         const int q = cp >> 2, wi = cp & 3;
 #pragma unroll
@@ -151,8 +211,13 @@ __global__ void __launch_bounds__(RQ_THREADS, SR ? 4 : 6) rq_rand_kernel(const Q
         uint4 qx, qy;
         if constexpr (SR) {
             uint32_t r_x[16], r_y[16];
-            load_r(o.sr_colT + gcol * p.R + grow, valid, r_x);
-            load_r(o.sr_colT + (gcol + 1) * p.R + grow, valid, r_y);
+            if constexpr (GEN) {
+                philox_sr32(o.sr_seed, grow, gcol, 1u, r_x);
+                philox_sr32(o.sr_seed, grow, gcol + 1, 1u, r_y);
+            } else {
+                load_r(o.sr_colT + gcol * p.R + grow, valid, r_x);
+                load_r(o.sr_colT + (gcol + 1) * p.R + grow, valid, r_y);
+            }
             quant32x2_sr<HAD>(v, bytex, bytey, r_x, r_y, qx, qy);
         } else {
             quant32x2<HAD>(v, bytex, bytey, qx, qy);
@@ -161,18 +226,18 @@ __global__ void __launch_bounds__(RQ_THREADS, SR ? 4 : 6) rq_rand_kernel(const Q
     }
 }
 
-template <int HAD, bool SR>
+template <int HAD, bool SR, bool GEN>
 cudaError_t launch_layouts(const QuantParams& p, const RandOpts& o, unsigned layouts, cudaStream_t s) {
     const dim3 grid((unsigned)((p.C + RQ_TC - 1) / RQ_TC), (unsigned)((p.R + RQ_TR - 1) / RQ_TR));
     switch (layouts) {
         case MXFP4_LAYOUT_ROW:
-            rq_rand_kernel<HAD, true, false, SR><<<grid, RQ_THREADS, 0, s>>>(p, o);
+            rq_rand_kernel<HAD, true, false, SR, GEN><<<grid, RQ_THREADS, 0, s>>>(p, o);
             break;
         case MXFP4_LAYOUT_COLT:
-            rq_rand_kernel<HAD, false, true, SR><<<grid, RQ_THREADS, 0, s>>>(p, o);
+            rq_rand_kernel<HAD, false, true, SR, GEN><<<grid, RQ_THREADS, 0, s>>>(p, o);
             break;
         case MXFP4_LAYOUT_ROW | MXFP4_LAYOUT_COLT:
-            rq_rand_kernel<HAD, true, true, SR><<<grid, RQ_THREADS, 0, s>>>(p, o);
+            rq_rand_kernel<HAD, true, true, SR, GEN><<<grid, RQ_THREADS, 0, s>>>(p, o);
             break;
         default:
             return cudaErrorInvalidValue;
@@ -182,8 +247,11 @@ cudaError_t launch_layouts(const QuantParams& p, const RandOpts& o, unsigned lay
 
 template <int HAD>
 cudaError_t launch_sr(const QuantParams& p, const RandOpts& o, unsigned layouts, cudaStream_t s) {
+    if (o.gen)
+        return o.sr_on ? launch_layouts<HAD, true, true>(p, o, layouts, s)
+                       : launch_layouts<HAD, false, true>(p, o, layouts, s);
     const bool sr = (layouts & MXFP4_LAYOUT_ROW && o.sr_row) || (layouts & MXFP4_LAYOUT_COLT && o.sr_colT);
-    return sr ? launch_layouts<HAD, true>(p, o, layouts, s) : launch_layouts<HAD, false>(p, o, layouts, s);
+    return sr ? launch_layouts<HAD, true, false>(p, o, layouts, s) : launch_layouts<HAD, false, false>(p, o, layouts, s);
 }
 
 }  // namespace

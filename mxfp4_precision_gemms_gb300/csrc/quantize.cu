@@ -35,14 +35,27 @@ constexpr int QTHREADS = 2 * TR;
 constexpr int QBLOCKS_PER_SM = 6;
 constexpr int TILE_BYTES = TR * TC * 2;  // the raw bf16 tile
 
-template <int HAD, bool ROW, bool COLT, bool TWOD>
-__global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel(const QuantParams p) {
+// One launch over up to two matrices with the same number of columns (a GEMM's two
+// operands share their contraction): row tiles 0 .. split-1 belong to g.p[0], the rest
+// to g.p[1].  A single matrix has split = its row-tile count.
+struct QuantGroup {
+    QuantParams p[2];
+    int32_t split;
+};
+
+// PAIR: two matrices (the parameters are then read through the CTA's matrix index);
+// one matrix keeps every parameter at a constant offset.  Measured: a single-matrix
+// launch that indexed its parameters like a pair ran 4-6% slower.
+template <int HAD, bool ROW, bool COLT, bool TWOD, bool PAIR>
+__global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel(const __grid_constant__ QuantGroup g) {
     extern __shared__ __align__(16) uint8_t q_smem[];
     uint32_t* tile_w = reinterpret_cast<uint32_t*>(q_smem);
     float* seg_amax = reinterpret_cast<float*>(q_smem + (COLT ? TILE_BYTES : 0));
 
     const int t = threadIdx.x;
-    const int64_t row0 = (int64_t)blockIdx.y * TR;
+    const int which = PAIR ? (int)blockIdx.y >= g.split : 0;
+    const QuantParams& p = g.p[which];
+    const int64_t row0 = (int64_t)((int)blockIdx.y - (which ? g.split : 0)) * TR;
     const int64_t col0 = (int64_t)blockIdx.x * TC;
 #if MXF_PDL_QUANT
     grid_dependency_wait();  // x may come from the previous kernel in the stream
@@ -152,10 +165,10 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel
     }
 }
 
-template <int HAD, bool ROW, bool COLT, bool TWOD>
-cudaError_t launch_one(const QuantParams& p, cudaStream_t s) {
+template <int HAD, bool ROW, bool COLT, bool TWOD, bool PAIR>
+cudaError_t launch_one(const QuantParams& p, const QuantParams* p2, cudaStream_t s) {
     constexpr int smem = (COLT ? TILE_BYTES : 0) + (TWOD ? TR * 4 * 4 : 0);
-    auto kern = rq_kernel<HAD, ROW, COLT, TWOD>;
+    auto kern = rq_kernel<HAD, ROW, COLT, TWOD, PAIR>;
     if constexpr (smem > 48 * 1024) {
         static DeviceSlots opted_in;
         int unused = 0;
@@ -164,21 +177,51 @@ cudaError_t launch_one(const QuantParams& p, cudaStream_t s) {
         });
         if (e != cudaSuccess) return e;
     }
-    const dim3 grid((unsigned)((p.C + TC - 1) / TC), (unsigned)((p.R + TR - 1) / TR));
-    return launch_overlapped(kern, grid, dim3(QTHREADS), smem, s, 1, MXF_PDL_QUANT != 0, p);
+    QuantGroup g{};
+    g.p[0] = p;
+    g.p[1] = p2 ? *p2 : p;
+    g.split = (int32_t)((p.R + TR - 1) / TR);
+    const int64_t tiles_y = g.split + (p2 ? (p2->R + TR - 1) / TR : 0);
+    const dim3 grid((unsigned)((p.C + TC - 1) / TC), (unsigned)tiles_y);
+    return launch_overlapped(kern, grid, dim3(QTHREADS), smem, s, 1, MXF_PDL_QUANT != 0, g);
 }
 
 template <int HAD>
-cudaError_t launch_had(const QuantParams& p, unsigned layouts, cudaStream_t s) {
+cudaError_t launch_had(const QuantParams& p, const QuantParams* p2, unsigned layouts, cudaStream_t s) {
+    if (p2) {
+        switch (layouts) {
+            case MXFP4_LAYOUT_ROW:
+                return launch_one<HAD, true, false, false, true>(p, p2, s);
+            case MXFP4_LAYOUT_COLT:
+                return launch_one<HAD, false, true, false, true>(p, p2, s);
+            case MXFP4_LAYOUT_ROW | MXFP4_LAYOUT_COLT:
+                return launch_one<HAD, true, true, false, true>(p, p2, s);
+            default:
+                return cudaErrorInvalidValue;
+        }
+    }
     switch (layouts) {
         case MXFP4_LAYOUT_ROW:
-            return launch_one<HAD, true, false, false>(p, s);
+            return launch_one<HAD, true, false, false, false>(p, nullptr, s);
         case MXFP4_LAYOUT_COLT:
-            return launch_one<HAD, false, true, false>(p, s);
+            return launch_one<HAD, false, true, false, false>(p, nullptr, s);
         case MXFP4_LAYOUT_ROW | MXFP4_LAYOUT_COLT:
-            return launch_one<HAD, true, true, false>(p, s);
+            return launch_one<HAD, true, true, false, false>(p, nullptr, s);
         case MXFP4_LAYOUT_2D:
-            return launch_one<HAD, false, false, true>(p, s);
+            return launch_one<HAD, false, false, true, false>(p, nullptr, s);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_any(const QuantParams& p, const QuantParams* p2, int had, unsigned layouts, cudaStream_t s) {
+    switch (had) {
+        case 0:
+            return launch_had<1>(p, p2, layouts, s);
+        case 16:
+            return launch_had<16>(p, p2, layouts, s);
+        case 32:
+            return launch_had<32>(p, p2, layouts, s);
         default:
             return cudaErrorInvalidValue;
     }
@@ -187,16 +230,13 @@ cudaError_t launch_had(const QuantParams& p, unsigned layouts, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_rotate_quantize(const QuantParams& p, int had, unsigned layouts, cudaStream_t s) {
-    switch (had) {
-        case 0:
-            return launch_had<1>(p, layouts, s);
-        case 16:
-            return launch_had<16>(p, layouts, s);
-        case 32:
-            return launch_had<32>(p, layouts, s);
-        default:
-            return cudaErrorInvalidValue;
-    }
+    return launch_any(p, nullptr, had, layouts, s);
+}
+
+cudaError_t launch_rotate_quantize_pair(const QuantParams& a, const QuantParams& b, int had, unsigned layouts,
+                                        cudaStream_t s) {
+    if (a.C != b.C || (layouts & MXFP4_LAYOUT_2D)) return cudaErrorInvalidValue;
+    return launch_any(a, &b, had, layouts, s);
 }
 
 }  // namespace mx

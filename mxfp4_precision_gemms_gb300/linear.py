@@ -4,9 +4,9 @@
 the three GEMMs of a linear layer in MXFP4 behind the framework's ordinary linear
 module.  This module does the same for PyTorch: the forward pass is
 ``mxfp4_linear_fprop`` (Y = X W^T, bf16 out), which also saves X^T and W^T quantised
-along the tokens and the output features; the backward pass is ``mxfp4_linear_dgrad``
-(dX = dY W, bf16 out, which also quantises dY^T) and ``mxfp4_linear_wgrad``
-(dW = dY^T X, fp32 out).  Every step runs in the CUDA library; this file only wires the
+along the tokens and the output features; the backward pass is ``mxfp4_linear_backward``
+(dY quantised once; dX = dY W, bf16 out, and dW = dY^T X, fp32 out, in one grouped
+GEMM launch).  Every step runs in the CUDA library; this file only wires the
 calls into autograd.  The quantised copies live on the autograd context between the
 two passes: about 0.53 bytes per element of X and W.
 """
@@ -32,9 +32,9 @@ class MXFP4LinearFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy: torch.Tensor):
         dy2 = dy.reshape(-1, dy.shape[-1]).to(torch.bfloat16).contiguous()
-        dx, dyT = mx.linear_dgrad(dy2, ctx.wT, mx.Config(had=ctx.had, mode=ctx.mode, out_dtype=mx.OUT_BF16))
-        # fp32 dW; autograd casts it to the weight's dtype
-        dw = mx.linear_wgrad(dyT, ctx.xT, mx.Config(had=ctx.had, mode=ctx.mode, out_dtype=mx.OUT_F32))
+        # one dY quantisation, then Dgrad (bf16 dX) and Wgrad (fp32 dW; autograd casts it
+        # to the weight's dtype) in one grouped launch
+        dx, dw = mx.linear_backward(dy2, ctx.wT, ctx.xT, mx.Config(had=ctx.had, mode=ctx.mode, out_dtype=mx.OUT_BF16))
         ctx.xT = ctx.wT = None
         return dx.reshape(*ctx.lead, dx.shape[-1]), dw, None, None
 

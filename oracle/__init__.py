@@ -82,6 +82,9 @@ def lib():
             L.oracle_quantize_row_rand.argtypes = [P, I64, I64, I64, I, I, P, P, P, P]
             L.oracle_quantize_colT_rand.argtypes = [P, I64, I64, I64, I, I, P, P, P, P]
             L.oracle_rotation_divergence.argtypes = [P, I64, I64, I64, I, I, P]
+            L.oracle_philox4x32_10.argtypes = [P, P, P]
+            L.oracle_philox_signs.argtypes = [ctypes.c_uint64, I64, P]
+            L.oracle_philox_sr.argtypes = [ctypes.c_uint64, I64, I64, ctypes.c_uint32, P]
             L.oracle_num_threads.restype = I
             L.oracle_set_num_threads.argtypes = [I]
             _lib = L
@@ -382,3 +385,47 @@ def quantize_rand(x_bf16: np.ndarray, had: int, mode: int, layout: str, signs=No
     else:
         raise ValueError(layout)
     return codes, scales
+
+
+# --------------------------------------------------------------------------- counter-based generator
+# The randomised baselines with their random numbers drawn from Philox4x32-10 (Salmon et
+# al., SC'11) instead of passed in: the sign vectors and the stochastic-rounding integers
+# are generated with the counter layout of oracle_philox_signs / oracle_philox_sr, then
+# the quantiser above runs on them unchanged.
+def philox4x32_10(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(ctr, np.uint32)
+    k = np.ascontiguousarray(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    lib().oracle_philox4x32_10(_p(c), _p(k), _p(out))
+    return out
+
+
+def philox_signs(seed: int, n: int) -> np.ndarray:
+    bits = np.zeros((n + 7) // 8, np.uint8)
+    lib().oracle_philox_signs(int(seed), n, _p(bits))
+    return bits
+
+
+def philox_sr(seed: int, lines: int, length: int, copy: int) -> np.ndarray:
+    out = np.zeros((lines, length), np.uint16)
+    lib().oracle_philox_sr(int(seed), lines, length, int(copy), _p(out))
+    return out
+
+
+def quantize_philox(x_bf16: np.ndarray, had: int, mode: int, layout: str, col_sign_seed=None, row_sign_seed=None,
+                    sr_seed=None):
+    """quantize_rand with generated numbers: 'row' uses the column-sign vector (seed
+    col_sign_seed, over C) and the SR integers of copy 0 ([R, C]); 'colT' the row-sign
+    vector (row_sign_seed, over R) and copy 1 ([C, R]).  A seed of None turns that
+    option off."""
+    x = _u16(x_bf16)
+    R, C = x.shape
+    if layout == "row":
+        signs = None if col_sign_seed is None else philox_signs(col_sign_seed, C)
+        sr = None if sr_seed is None else philox_sr(sr_seed, R, C, 0)
+    elif layout == "colT":
+        signs = None if row_sign_seed is None else philox_signs(row_sign_seed, R)
+        sr = None if sr_seed is None else philox_sr(sr_seed, C, R, 1)
+    else:
+        raise ValueError(layout)
+    return quantize_rand(x, had, mode, layout, signs=signs, sr=sr)

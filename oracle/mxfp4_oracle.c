@@ -623,6 +623,73 @@ void oracle_quantize_colT_rand(const uint16_t* x, int64_t R, int64_t C, int64_t 
 }
 
 /* ------------------------------------------------------------------------- */
+/* Counter-based random numbers for the randomised baselines                  */
+/* ------------------------------------------------------------------------- */
+
+/* Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
+ * 1, 2, 3", SC'11), written from its published definition.  A 128-bit counter
+ * (c0, c1, c2, c3) and a 64-bit key (k0, k1) give four 32-bit outputs after ten rounds.
+ * One round: the 64-bit products M0 * c0 and M1 * c2 (M0 = 0xD2511F53,
+ * M1 = 0xCD9E8D57) with high words h0, h1 and low words l0, l1 give the new counter
+ * (h1 ^ c1 ^ k0, l1, h0 ^ c3 ^ k1, l0).  The key is bumped by the Weyl constants
+ * (k0 += 0x9E3779B9, k1 += 0xBB67AE85) between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * (uint64_t)c[0];
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * (uint64_t)c[2];
+        const uint32_t h0 = (uint32_t)(p0 >> 32), l0 = (uint32_t)p0;
+        const uint32_t h1 = (uint32_t)(p1 >> 32), l1 = (uint32_t)p1;
+        const uint32_t n0 = h1 ^ c[1] ^ k0, n2 = h0 ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = l1;
+        c[2] = n2;
+        c[3] = l0;
+    }
+    for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+/* The random-sign vector of one dimension, from the 64-bit seed of that dimension:
+ * sign bit j is bit (j % 32) of output word (j % 128) / 32 of Philox4x32-10 with counter
+ * (j / 128, 0, 0, 0) and key (seed low word, seed high word).  bits: (n + 7) / 8 bytes,
+ * bit j in bit j % 8 of byte j / 8 (set = negate), the layout of the sign masks above.
+ * The operands of a GEMM share the vector of their contraction when they share its seed. */
+void oracle_philox_signs(uint64_t seed, int64_t n, uint8_t* bits) {
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    memset(bits, 0, (size_t)((n + 7) / 8));
+    for (int64_t j = 0; j < n; ++j) {
+        const uint32_t ctr[4] = {(uint32_t)(j / 128), 0u, 0u, 0u};
+        uint32_t o[4];
+        oracle_philox4x32_10(ctr, key, o);
+        if ((o[(j % 128) / 32] >> (j % 32)) & 1u) bits[j / 8] |= (uint8_t)(1u << (j % 8));
+    }
+}
+
+/* Stochastic-rounding integers of one quantised copy, lines x len of them (line = the
+ * row of the stored copy, position = the index along the quantised dimension): the
+ * integer of (line l, position i) is 16-bit half (i % 8) of Philox4x32-10 with counter
+ * (i / 8, l, copy, 0) and key (seed low, seed high) -- half h is bits 16 (h % 2) ..
+ * 16 (h % 2) + 15 of output word h / 2.  copy: 0 the row copy, 1 the transposed copy.
+ * out: lines * len uint16, row-major. */
+void oracle_philox_sr(uint64_t seed, int64_t lines, int64_t len, uint32_t copy, uint16_t* out) {
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+#pragma omp parallel for schedule(static)
+    for (int64_t l = 0; l < lines; ++l)
+        for (int64_t i = 0; i < len; ++i) {
+            const uint32_t ctr[4] = {(uint32_t)(i / 8), (uint32_t)l, copy, 0u};
+            uint32_t o[4];
+            oracle_philox4x32_10(ctr, key, o);
+            const int h = (int)(i % 8);
+            out[l * len + i] = (uint16_t)(o[h / 2] >> (16 * (h % 2)));
+        }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Diagnostic: canonical fp32 rotation against the exact rotation             */
 /* ------------------------------------------------------------------------- */
 

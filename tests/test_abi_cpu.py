@@ -243,3 +243,84 @@ def test_mma_scale_order_roundtrip(rows, cols):
         assert idx[33, 5] == 1 * 512 + 1 * 16 + 1 * 4 + 1
         if rows > 130:
             assert idx[130, 0] == (kb_pad // 4) * 512 + 2 * 16
+
+
+def test_pair_quantiser_rejects_bad_arguments(L):
+    """mxfp4_rotate_quantize_pair validates both matrices and every output before its
+    one launch."""
+    P = ctypes.c_void_p
+    t = [_tensor() for _ in range(4)]
+
+    def pq(a=0x1000, ra=64, lda=256, b=0x9000, rb=64, ldb=256, cols=256, layouts=3, outs=t):
+        r = [ctypes.byref(o) if o is not None else None for o in outs]
+        return L.mxfp4_rotate_quantize_pair(P(a), ra, lda, P(b), rb, ldb, cols, 16, 0, layouts, *r, None)
+    assert pq() == PASSED_VALIDATION
+    assert pq(layouts=4) == 1                              # no 2D
+    assert pq(b=0x9008) == 3                               # misaligned second matrix
+    assert pq(ldb=100) == 3                                # its leading dimension
+    assert pq(rb=40) == 2                                  # its transposed copy needs rows % 32
+    assert pq(cols=48, lda=48, ldb=48) == 2                # shared cols % 32
+    assert pq(outs=[t[0], t[1], t[2], None]) == 1          # a requested output missing
+    assert pq(outs=[t[0], t[1], _tensor(codes=0x1004), t[3]]) == 3
+    assert pq(ra=0, rb=0) == 0                             # both empty: nothing touched
+
+
+def test_gemm_group_rejects_bad_arguments(L):
+    """Every problem is checked (its index named), at most 8 problems, and no two outputs
+    may share a byte -- all before any launch."""
+    tensors = []
+
+    def desc(C=0x40000, ldc=128, out=0, acc=0, **kw):
+        a, b = _tensor(), _tensor(**kw)
+        tensors.extend([a, b])
+        return mx.GemmDescC(ctypes.addressof(a), ctypes.addressof(b), C, ldc, out, acc)
+
+    def g(*ds, n=None):
+        arr = (mx.GemmDescC * len(ds))(*ds)
+        return L.mxfp4_gemm_group(arr, len(ds) if n is None else n, None)
+    ok1, ok2 = desc(C=0x40000), desc(C=0x80000)
+    assert g(ok1, ok2) == PASSED_VALIDATION
+    assert g(ok1, ok2, n=0) == 1 and g(*[desc(C=0x40000 * (i + 1)) for i in range(9)]) == 1
+    assert g(ok1, desc(C=0x80000, had=32)) == 1          # problem 1: operands of two rotations
+    assert b"problem 1" in L.mxfp4_last_error()
+    assert g(ok1, desc(C=0x80000, ldc=100)) == 3         # problem 1: ldc % 8
+    assert g(ok1, desc(C=0x40000 + 128 * 127 * 4)) == 1  # overlaps problem 0's last row
+    assert b"overlap" in L.mxfp4_last_error()
+    assert g(ok1, desc(C=0x40000 + 128 * 128 * 4)) == PASSED_VALIDATION  # right after it
+
+
+def test_linear_backward_checks_roles_and_workspace(L):
+    P = ctypes.c_void_p
+    cfg = mx.MxConfigC(16, 0, 1, 0)
+    colT = dict(layout=mx.LAYOUT_COLT)
+
+    def b(wT, xT, M=256, N=256, K=256, dx=0x3000, dw=0x80000, ws=P(0x100000), nb=1 << 40):
+        return L.mxfp4_linear_backward(P(0x1000), ctypes.byref(wT), ctypes.byref(xT), M, N, K, ctypes.byref(cfg),
+                                       P(dx), P(dw), ws, nb, None)
+    wT, xT = _tensor(rows=256, cols=256, **colT), _tensor(rows=256, cols=256, **colT)
+    assert b(wT, xT) == PASSED_VALIDATION
+    assert b(_tensor(rows=256, cols=256), xT) == 1                      # W's row copy in W^T's place
+    assert b(wT, _tensor(rows=256, cols=256, had=32, **colT)) == 1      # X^T under another rotation
+    assert b(wT, _tensor(rows=256, cols=512, **colT)) == 2              # X^T must be [K, M]
+    assert b(wT, xT, ws=P(0), nb=0) == 4                                # workspace missing
+    assert b(wT, xT, dx=0x3004) == 3
+    assert mx.workspace_bytes(mx.OP_BACKWARD, 8192, 4096, 4096, mx.Config()) == (
+        L.mxfp4_quantized_bytes(8192, 4096, 1, 1) + L.mxfp4_quantized_bytes(4096, 8192, 2, 1))
+
+
+def test_philox_quantiser_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    t1, t2 = _tensor(), _tensor()
+
+    def ph(layouts=3, reserved=0, opts=True, rows=64, x=0x1000):
+        o = mx.PhiloxOptsC(1, 2, 3, 1, 1, 1, reserved)
+        return L.mxfp4_rotate_quantize_philox(P(x), rows, 256, 256, 16, 0, layouts,
+                                              ctypes.byref(o) if opts else None, ctypes.byref(t1), ctypes.byref(t2),
+                                              None)
+    assert ph() == PASSED_VALIDATION
+    assert ph(opts=False) == 1
+    assert ph(reserved=1) == 1
+    assert ph(layouts=4) == 1                             # no 2D
+    assert ph(rows=40) == 2                               # the transposed copy needs rows % 32
+    assert ph(x=0x1008) == 3
+    assert ph(rows=0) == 0                                # empty: nothing touched

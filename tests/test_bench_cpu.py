@@ -51,7 +51,7 @@ def test_traffic_record_parser(tmp_path, monkeypatch):
     os.makedirs(tmp_path / "mxfp4_precision_gemms_gb300" / "csrc")
     for f in {f for files in bench.KERNEL_SOURCES.values() for f in files}:
         (tmp_path / "mxfp4_precision_gemms_gb300" / "csrc" / f).write_text(f)
-    bench.write_traffic(str(src))
+    bench.write_traffic([str(src)])
     rec = json.load(open(out_dir / "traffic_llama8b_linears_T8192.json"))
     assert rec["gemm"]["bytes_per_launch"] == 150750000 and rec["quant"]["bytes_per_launch"] == 235000000
     t = bench.measured_traffic()

@@ -31,7 +31,7 @@ def test_rejected_fprop_leaves_every_buffer_untouched():
     M, N, K = 256, 256, 512
     X, W, _ = synth.linear_inputs(M, N, K, 0)
     x = mx.bf16_tensor(X)
-    wbuf = torch.empty(N * K + 8, dtype=torch.bfloat16, device="cuda")
+    wbuf = torch.empty(N * K + 4, dtype=torch.bfloat16, device="cuda")
     wbuf[4:].copy_(mx.bf16_tensor(W).reshape(-1))
     cfg = mx.Config(had=mx.HAD_16, mode=mx.SCALE_FLOOR, out_dtype=mx.OUT_F32)
     nb = mx.workspace_bytes(mx.OP_FPROP, M, N, K, cfg)

@@ -115,3 +115,52 @@ def test_sr_quantiser_is_unbiased_on_a_tensor():
     rne_bias = np.abs(oracle.dequant_row(c, s) - v).mean()
     sr_bias = np.abs(acc / n - v).mean()
     assert sr_bias < 0.25 * rne_bias
+
+
+# ---------------------------------------------------------------- counter-based generator
+def _kat():
+    import json
+    import os
+
+    path = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.jsonl")
+    return [json.loads(l) for l in open(path) if l.strip()]
+
+
+@pytest.mark.parametrize("case", _kat(), ids=lambda c: c["name"])
+def test_philox_known_answers(oracle_mod, case):
+    """The generator against the published known-answer vectors of Philox4x32-10 (a
+    wrong multiplier, Weyl constant, word order or round count changes every word)."""
+    h = lambda xs: [int(v, 16) for v in xs]
+    assert [int(v) for v in oracle_mod.philox4x32_10(h(case["ctr"]), h(case["key"]))] == h(case["out"])
+
+
+def test_philox_streams_are_balanced_and_distinct(oracle_mod):
+    """Sign vectors have half their bits set, distinct seeds give distinct vectors, and
+    the stochastic-rounding integers are uniform over [0, 65536): their mean and the
+    counts of their top nibble are within a few standard errors of uniform."""
+    a, b = oracle_mod.philox_signs(1, 1 << 16), oracle_mod.philox_signs(2, 1 << 16)
+    for bits in (a, b):
+        ones = int(np.unpackbits(bits).sum())
+        assert abs(ones - (1 << 15)) < 5 * 128  # sd = sqrt(n)/2 = 128
+    assert not np.array_equal(a, b)
+    r = oracle_mod.philox_sr(7, 64, 4096, 0).astype(np.float64)
+    n = r.size
+    assert abs(r.mean() - 32767.5) < 5 * 65536 / np.sqrt(12 * n)
+    counts = np.bincount((r.astype(np.int64) >> 12).ravel(), minlength=16)
+    chi2 = ((counts - n / 16) ** 2 / (n / 16)).sum()
+    assert chi2 < 50  # 15 degrees of freedom: p ~ 1e-5
+    assert not np.array_equal(oracle_mod.philox_sr(7, 4, 64, 0), oracle_mod.philox_sr(7, 4, 64, 1))
+
+
+def test_philox_stochastic_rounding_is_unbiased(oracle_mod):
+    """With the generated integers, the mean of stochastically rounded values of one
+    constant block approaches the block (the generator feeds an unbiased rounding)."""
+    v = np.float32(1.3)  # between grid values 1 and 1.5 under e = 0: rounds up with p = 0.6
+    x = np.full((4096, 32), v, np.float32)
+    x[:, 0] = 4.0  # amax 4 -> e = 0 (floor and ceil)
+    xb = synth.bf16_bits(x)
+    codes, scales = oracle_mod.quantize_philox(xb, 1, 0, "row", sr_seed=99)
+    vals = np.array([oracle_mod.e2m1_value(int(c)) for c in oracle_mod.unpack_codes(codes)[:, 1:].ravel()])
+    want = float(synth.bf16_to_f32(synth.bf16_bits(np.array([v], np.float32)))[0])
+    assert set(np.unique(vals)) <= {1.0, 1.5}
+    assert abs(vals.mean() - want) < 5 * 0.5 * np.sqrt(0.24 / vals.size)

@@ -134,3 +134,65 @@ def test_randomised_strided_inputs(torch, pad, offset):
         wc, ws = oracle.quantize_rand(xb, ORACLE_HAD[16], 0, key, signs=signs, sr=sr)
         same(out[key].plain_scales(), ws, f"{key} strided scales")
         same(out[key].codes.cpu().numpy(), wc, f"{key} strided codes")
+
+
+# ---------------------------------------------------------------- in-kernel Philox4x32-10
+@pytest.mark.parametrize("shape", [(64, 256), (96, 160), (192, 1056), (32, 32), (256, 512)])
+@pytest.mark.parametrize("had", [0, 16, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("opts", ["signs", "sr", "both"])
+def test_philox_generated_bit_exact(torch, shape, had, mode, opts):
+    """Random signs and stochastic rounding drawn in the kernel from Philox4x32-10:
+    codes and bytes bit-exact with the oracle, which draws the same numbers from its own
+    generator (pinned to the published known-answer vectors) and runs the pinned
+    randomised quantiser; and byte-identical to the array-input kernel given those
+    numbers."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    R, C = shape
+    xb = synth.heavy_tailed(R, C, 900 + R + C + had)
+    seeds = dict(col_sign_seed=0x1234_5678_9ABC_DEF0 + had if opts != "sr" else None,
+                 row_sign_seed=(7 << 40) + mode if opts != "sr" else None,
+                 sr_seed=0xFEED_0000_0000_0001 + R if opts != "signs" else None)
+    layouts = mx.LAYOUT_ROW | mx.LAYOUT_COLT
+    x = mx.bf16_tensor(xb)
+    out = mx.rotate_quantize_philox(x, had=had, mode=mode, layouts=layouts, **seeds)
+    cs = None if seeds["col_sign_seed"] is None else oracle.philox_signs(seeds["col_sign_seed"], C)
+    rs = None if seeds["row_sign_seed"] is None else oracle.philox_signs(seeds["row_sign_seed"], R)
+    srr = None if seeds["sr_seed"] is None else oracle.philox_sr(seeds["sr_seed"], R, C, 0)
+    src = None if seeds["sr_seed"] is None else oracle.philox_sr(seeds["sr_seed"], C, R, 1)
+    arr = mx.rotate_quantize_rand(x, had=had, mode=mode, layouts=layouts,
+                                  col_signs=None if cs is None else dev(torch, cs),
+                                  row_signs=None if rs is None else dev(torch, rs),
+                                  sr_row=None if srr is None else dev(torch, srr),
+                                  sr_colT=None if src is None else dev(torch, src))
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    for key in ("row", "colT"):
+        wc, ws = oracle.quantize_philox(xb, ORACLE_HAD[had], mode, key, **seeds)
+        what = f"philox {key} {shape} had={had} mode={mode} {opts}"
+        same(out[key].plain_scales(), ws, what + " scales")
+        same(out[key].codes.cpu().numpy(), wc, what + " codes")
+        assert torch.equal(out[key].codes, arr[key].codes) and torch.equal(out[key].scales, arr[key].scales)
+
+
+def test_philox_signs_cancel_in_the_gemm(torch):
+    """X and W quantised with the same Philox sign vector over K (one seed): the Fprop
+    GEMM of the two copies is within tolerance of the oracle's product of the same
+    codes, and close to the bf16 product (the signs cancel like the rotation)."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+    from tests.gpu_util import assert_within
+
+    X, W, _ = synth.linear_inputs(256, 384, 1024, 31)
+    qx = mx.rotate_quantize_philox(mx.bf16_tensor(X), had=16, col_sign_seed=2024, sr_seed=5)["row"]
+    qw = mx.rotate_quantize_philox(mx.bf16_tensor(W), had=16, col_sign_seed=2024, sr_seed=6)["row"]
+    Y = mx.gemm(qx, qw)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    cx, sx = oracle.quantize_philox(X, 16, 0, "row", col_sign_seed=2024, sr_seed=5)
+    cw, sw = oracle.quantize_philox(W, 16, 0, "row", col_sign_seed=2024, sr_seed=6)
+    want, S = oracle.gemm(cx, sx, cw, sw)
+    assert_within(Y.double().cpu().numpy(), want, S, what="philox-signed fprop")
+    dense = synth.bf16_to_f32(X).astype(np.float64) @ synth.bf16_to_f32(W).astype(np.float64).T
+    rel = np.linalg.norm(Y.double().cpu().numpy() - dense) / np.linalg.norm(dense)
+    assert rel < 0.25, rel

@@ -165,3 +165,44 @@ def test_strided_and_offset_inputs(torch, layouts, pad, offset):
         gc, gs = outs[key].codes.cpu().numpy(), outs[key].plain_scales()
         assert np.array_equal(gs, want_s), f"{key} scales, pad {pad} offset {offset}"
         assert np.array_equal(gc, want_c), f"{key} codes, pad {pad} offset {offset}"
+
+
+@pytest.mark.parametrize("had", [0, 16, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("layouts", [1, 2, 3])
+def test_pair_launch_equals_two_calls_and_the_oracle(torch, had, mode, layouts):
+    """mxfp4_rotate_quantize_pair (two matrices with the same columns in one launch):
+    every output byte-identical to two separate rotate_quantize calls, bit-exact with the
+    oracle, for row counts that end mid-tile on either side and plain and MMA scales."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    names = {mx.LAYOUT_ROW: "row", mx.LAYOUT_COLT: "colT"}
+    for (ra, rb, c), seed in (((256, 512, 512), 1), ((96, 160, 256), 2), ((224, 32, 384), 3)):
+        A = synth.activations(ra, c, seed)
+        B = synth.weights(rb, c, seed + 100)
+        for sf in (0, 1):
+            a, b = mx.bf16_tensor(A), mx.bf16_tensor(B)
+            pa, pb = mx.rotate_quantize_pair(a, b, had=had, mode=mode, layouts=layouts, sf_layout=sf)
+            sa = mx.rotate_quantize(a, had=had, mode=mode, layouts=layouts, sf_layout=sf)
+            sb = mx.rotate_quantize(b, had=had, mode=mode, layouts=layouts, sf_layout=sf)
+            torch.cuda.synchronize()
+            assert mx.device_status() == 0
+            for bit, key in names.items():
+                if not layouts & bit:
+                    continue
+                for got, ref, bits in ((pa, sa, A), (pb, sb, B)):
+                    assert torch.equal(got[key].codes, ref[key].codes), f"{key} codes {ra}/{rb}x{c}"
+                    assert torch.equal(got[key].scales, ref[key].scales), f"{key} scales {ra}/{rb}x{c}"
+                    assert got[key].had == had and got[key].mode == mode
+                    want_c, want_s = oracle.quantize(bits, ORACLE_HAD[had], mode, key)
+                    assert np.array_equal(got[key].codes.cpu().numpy(), want_c)
+                    assert np.array_equal(got[key].plain_scales(), want_s)
+
+
+def test_pair_launch_rejects_mismatched_columns(torch):
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    a = mx.bf16_tensor(synth.activations(64, 256, 1))
+    b = mx.bf16_tensor(synth.activations(64, 512, 2))
+    with pytest.raises(ValueError):
+        mx.rotate_quantize_pair(a, b)
