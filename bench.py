@@ -1026,6 +1026,29 @@ def quant_fixes_leg(flush, hbm, iters=20):
             tot += a.elapsed_time(b)
         gbs = by / (tot / iters * 1e-3) / 1e9
         out[name] = {"gbs": round(gbs, 1), "frac": round(gbs / hbm, 4), "us": round(tot / iters * 1e3, 1)}
+    # the GEMM over MBS operands (activations and weights of an o-projection, 8192 x 4096 x
+    # 4096, bf16 out) against the plain GEMM on the same codes and scales
+    xm = mx.bf16_tensor(synth.activations(8192, 4096, 21))
+    wm = mx.bf16_tensor(synth.weights(4096, 4096, 22))
+    (qa, ma), (qb, mb) = mx.rotate_quantize_mbs(xm, had=16, mode=0), mx.rotate_quantize_mbs(wm, had=16, mode=0)
+    cm = torch.empty((8192, 4096), dtype=torch.bfloat16, device="cuda")
+    gfl = 2 * 8192 * 4096 * 4096
+    for name, fn in (("mbs_gemm", lambda: mx.gemm_mbs(qa, ma, qb, mb, mx.OUT_BF16, out=cm)),
+                     ("plain_gemm_same_codes", lambda: mx.gemm(qa, qb, mx.OUT_BF16, out=cm))):
+        for _ in range(3):
+            fn()
+        tot = 0.0
+        for _ in range(iters):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        out[name] = {"tflops": round(gfl / (tot / iters * 1e-3) / 1e12, 1), "us": round(tot / iters * 1e3, 1),
+                     "shape": "8192x4096x4096, bf16 out, both operands MBS"}
+    del xm, wm, qa, qb, ma, mb, cm
     # the quantiser sweep of the heavy-tailed tensors (0.1 t(3) + 0.1% entries x100), both
     # sizes of the sweep workload: {none, H16, H32} x {row, colT, 2D} x {floor, ceil}, GB/s
     for (SR, SC), key in (((R, C), "sweep_gbs"), ((4096, 4096), "sweep_gbs_4096x4096")):

@@ -234,10 +234,27 @@ mxfp4_status mxfp4_rotate_quantize_of(const void* x, int64_t rows, int64_t cols,
  * (T = 1.5 if f <= 1.5, else 3; A zero or subnormal gives k = 0).  The values are
  * prescaled to fl32((1 + k/256) v) and quantised to q; the reconstruction is
  * dq(q) / (1 + k/256).  mbs: device bytes [rows, cols/128], row-major, written by the
- * call.  The post-scale varies along the contraction, so mxfp4_gemm does not apply it.
- * cols % 128 == 0. */
+ * call.  The post-scale varies along the contraction: mxfp4_gemm_mbs applies it per
+ * macro block (mxfp4_gemm does not).  cols % 128 == 0. */
 mxfp4_status mxfp4_rotate_quantize_mbs(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
                                        mxfp4_tensor* q, uint8_t* mbs, mxfp4_stream_t stream);
+
+/* GEMM over macro-block-scaled operands ("Decomposing MXFP4 quantization error ...",
+ * MBS: x_hat = Q((1 + m) x) / (1 + m)): C = x_hat_A . x_hat_B^T, i.e. for each macro
+ * block kb of 128 elements along K the MXFP4 partial product P_kb (fp32 on the tensor
+ * cores) is scaled by f_A[m][kb] f_B[n][kb], f = 256 / (256 + byte) computed in fp32,
+ * and the scaled partials are summed in fp32.  The page says the postscale fuses into
+ * the GEMM epilogue; it can as one factor only when it is constant along K, and here it
+ * changes every 128 elements of K, so each partial is scaled as it leaves the tensor
+ * cores instead.
+ * A, B, C, ldc, out_dtype, accumulate: as for mxfp4_gemm (A and B from
+ * mxfp4_rotate_quantize_mbs or any row-quantised copy).  mbs_a: device bytes
+ * [M, K/128] row-major (the `mbs` output of mxfp4_rotate_quantize_mbs), or NULL for
+ * a plain MXFP4 A (factor 1); mbs_b likewise [N, K/128].  K % 128 == 0 and
+ * K <= 16384 (MXFP4_ERR_UNSUPPORTED_SHAPE otherwise).  Runs 128 x 128 single-CTA
+ * tiles; within the GEMM tolerance of the oracle's fp64 product of the reconstructions. */
+mxfp4_status mxfp4_gemm_mbs(const mxfp4_tensor* A, const uint8_t* mbs_a, const mxfp4_tensor* B, const uint8_t* mbs_b,
+                            void* C, int64_t ldc, int out_dtype, int accumulate, mxfp4_stream_t stream);
 
 /* Randomised quantiser baselines of "Pretraining Large Language Models with MXFP4 on
  * Native FP4 Hardware" (A.2: random sign flips before the Hadamard; the

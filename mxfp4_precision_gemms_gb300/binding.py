@@ -95,6 +95,7 @@ def lib():
                                                  I),
                 "mxfp4_gemm": ([T, T, P, I64, I, I, P, S, P], I),
                 "mxfp4_gemm_group": ([ctypes.POINTER(GemmDescC), I, P], I),
+                "mxfp4_gemm_mbs": ([T, P, T, P, P, I64, I, I, P], I),
                 "mxfp4_workspace_bytes": ([I, I64, I64, I64, CF], S),
                 "mxfp4_linear_fprop": ([P, P, I64, I64, I64, CF, P, T, T, P, S, P], I),
                 "mxfp4_linear_dgrad": ([P, T, I64, I64, I64, CF, P, T, P, S, P], I),
@@ -368,6 +369,21 @@ def gemm(A: QTensor, B: QTensor, out_dtype: int = OUT_F32, accumulate: bool = Fa
     a, b = A.c(), B.c()
     _check(lib().mxfp4_gemm(ctypes.byref(a), ctypes.byref(b), _ptr(out), out.stride(0), out_dtype, int(accumulate),
                             None, 0, _stream(stream)))
+    return out
+
+
+def gemm_mbs(A: QTensor, mbs_a: torch.Tensor | None, B: QTensor, mbs_b: torch.Tensor | None,
+             out_dtype: int = OUT_F32, accumulate: bool = False, out: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """mxfp4_gemm_mbs: C = x_hat_A . x_hat_B^T over macro-block-scaled operands (mbs_a /
+    mbs_b: uint8 [rows, K/128] device tensors from rotate_quantize_mbs, or None)."""
+    if out is None:
+        dt = torch.float32 if out_dtype == OUT_F32 else torch.bfloat16
+        out = (torch.zeros if accumulate else torch.empty)((A.rows, B.rows), dtype=dt, device=A.codes.device)
+    a, b = A.c(), B.c()
+    _check(lib().mxfp4_gemm_mbs(ctypes.byref(a), None if mbs_a is None else _ptr(mbs_a), ctypes.byref(b),
+                                None if mbs_b is None else _ptr(mbs_b), _ptr(out), out.stride(0), out_dtype,
+                                int(accumulate), _stream(stream)))
     return out
 
 

@@ -18,7 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmxfp4.so")
-SOURCES = ("mxfp4_api.cu", "quantize.cu", "quant_fixes.cu", "quant_random.cu", "gemm.cu", "noalloc.cu", "decompose.cu", "peak.cu")
+SOURCES = ("mxfp4_api.cu", "quantize.cu", "quant_fixes.cu", "quant_random.cu", "gemm.cu", "gemm_mbs.cu", "noalloc.cu",
+           "decompose.cu", "peak.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

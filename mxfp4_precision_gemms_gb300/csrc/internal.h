@@ -96,6 +96,16 @@ struct GemmGroup {
 };
 cudaError_t launch_gemm_group(const GemmParams* probs, int n, cudaStream_t s);
 
+// GEMM over macro-block-scaled operands: the plain GEMM's parameters plus the MBS bytes
+// of A [M, K/128] and B [N, K/128] (NULL: that operand has no macro-block factor).
+constexpr int kMbsMaxMacroBlocks = 128;  // K <= 16384
+struct MbsParams {
+    GemmParams g;
+    const uint8_t* mbs_a;
+    const uint8_t* mbs_b;
+};
+cudaError_t launch_gemm_mbs(const MbsParams& mp, cudaStream_t s);
+
 cudaError_t run_mma_peak_probe(int kind, int64_t iters, float* ms, int* ctas, uint32_t* status, uint64_t wait_ns);
 
 cudaError_t launch_error_decomposition(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int had, int mode,

@@ -823,6 +823,33 @@ mxfp4_status mxfp4_gemm_group(const mxfp4_gemm_desc* descs, int count, mxfp4_str
     return ok();
 }
 
+mxfp4_status mxfp4_gemm_mbs(const mxfp4_tensor* A, const uint8_t* mbs_a, const mxfp4_tensor* B, const uint8_t* mbs_b,
+                            void* C, int64_t ldc, int out_dtype, int accumulate, mxfp4_stream_t stream) {
+    mxfp4_status st;
+    if ((st = gemm_validate(A, B, C, ldc, out_dtype, accumulate))) return st;
+    if (A->cols % 128) return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "K (%lld) %% 128 != 0 (macro blocks)", (long long)A->cols);
+    if (A->cols / 128 > kMbsMaxMacroBlocks)
+        return fail(MXFP4_ERR_UNSUPPORTED_SHAPE, "K (%lld) above %d", (long long)A->cols, 128 * kMbsMaxMacroBlocks);
+    int dev;
+    if ((st = check_device(&dev))) return st;
+    struct Box {
+        unsigned char raw[sizeof(MbsParams) + 64];
+    } box;
+    MbsParams* mp = reinterpret_cast<MbsParams*>((reinterpret_cast<uintptr_t>(box.raw) + 63) & ~uintptr_t(63));
+    if ((st = gemm_prepare(A, B, C, ldc, out_dtype, accumulate, &mp->g))) return st;
+    mp->g.status = device_status_ptr();
+    mp->g.wait_ns = wait_limit();
+    if (t_inject_gemm_faults > 0) {
+        --t_inject_gemm_faults;
+        mp->g.test_drop_first_stage = 1;
+    }
+    mp->mbs_a = mbs_a;
+    mp->mbs_b = mbs_b;
+    cudaError_t e = launch_gemm_mbs(*mp, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gemm_mbs launch");
+    return ok();
+}
+
 mxfp4_status mxfp4_error_decomposition(const void* x, int64_t rows, int64_t cols, int64_t ld, int had, int mode,
                                        double* out, mxfp4_stream_t stream) {
     if (rows < 0 || cols < 0) return fail(MXFP4_ERR_INVALID_ARG, "negative size");

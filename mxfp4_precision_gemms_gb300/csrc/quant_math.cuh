@@ -38,6 +38,16 @@ __device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
     return d;
 }
 
+// d = a * b + c on each half, one rounding (IEEE fma).
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 // Rotation of two independent 32-element vectors held as pairs (v[i] = element i of
 // vector x and of vector y) by block-diagonal H_n (n = 1, 16, 32): stages of strides
 // 1, 2, 4, 8 (, 16), each (a, b) -> (a + b, a - b) rounded to fp32.  H32 then

@@ -77,6 +77,7 @@ def lib():
             L.oracle_mbs_byte.restype = I
             L.oracle_quantize_mbs_row.argtypes = [P, I64, I64, I64, I, I, P, P, P]
             L.oracle_dequant_mbs_row.argtypes = [P, P, P, I64, I64, P]
+            L.oracle_gemm_mbs.argtypes = [P, P, P, P, P, P, I64, I64, I64, P, P]
             L.oracle_e2m1_code_sr.argtypes = [ctypes.c_float, ctypes.c_uint16]
             L.oracle_e2m1_code_sr.restype = I
             L.oracle_quantize_row_rand.argtypes = [P, I64, I64, I64, I, I, P, P, P, P]
@@ -347,6 +348,25 @@ def dequant_mbs(codes, scales, mbs) -> np.ndarray:
     out = np.empty((R, C), np.float64)
     lib().oracle_dequant_mbs_row(_p(codes), _p(scales), _p(mbs), R, C, _p(out))
     return out
+
+
+def gemm_mbs(ca, sa, mbs_a, cb, sb, mbs_b):
+    """C = x_hat_A x_hat_B^T over MBS operands (mbs_a / mbs_b [rows, K/128] bytes, or
+    None for a plain MXFP4 operand): each 128-element macro block's partial product
+    scaled by its two postscale factors 1 / (1 + byte/256).  Returns (C, S), fp64."""
+    ca, sa, cb, sb = (np.ascontiguousarray(a) for a in (ca, sa, cb, sb))
+    M, K = ca.shape[0], ca.shape[1] * 2
+    N = cb.shape[0]
+    assert K % 128 == 0 and cb.shape[1] * 2 == K
+    ma = None if mbs_a is None else np.ascontiguousarray(mbs_a, np.uint8)
+    mb = None if mbs_b is None else np.ascontiguousarray(mbs_b, np.uint8)
+    assert ma is None or ma.shape == (M, K // 128)
+    assert mb is None or mb.shape == (N, K // 128)
+    C = np.empty((M, N), np.float64)
+    S = np.empty((M, N), np.float64)
+    lib().oracle_gemm_mbs(_p(ca), _p(sa), None if ma is None else _p(ma), _p(cb), _p(sb),
+                          None if mb is None else _p(mb), M, N, K, _p(C), _p(S))
+    return C, S
 
 
 # --------------------------------------------------------------------------- randomised baselines

@@ -543,6 +543,34 @@ void oracle_dequant_mbs_row(const uint8_t* codes, const uint8_t* scales, const u
         }
 }
 
+/* GEMM over MBS operands ([DECOMP] "MBS": x_hat = Q((1 + m) x) / (1 + m), the postscale
+ * applied to each macro block of 128 consecutive elements along the quantised, i.e. the
+ * contraction, dimension): C[m][n] = sum over macro blocks kb of
+ *   f_A[m][kb] f_B[n][kb] * sum_{k in kb} dq(A)[m][k] dq(B)[n][k],
+ * f = 1 / (1 + byte / 256) (f = 1 where mbs_a / mbs_b is NULL: that operand is plain
+ * MXFP4).  The inner sums are those of oracle_gemm (exact integers per 32-block); the
+ * factors and sums are fp64.  S[m][n] = sum_k |x_hat_a| |x_hat_b|.  K % 128 == 0. */
+void oracle_gemm_mbs(const uint8_t* ca, const uint8_t* sa, const uint8_t* mbs_a, const uint8_t* cb,
+                     const uint8_t* sb, const uint8_t* mbs_b, int64_t M, int64_t N, int64_t K, double* C, double* S) {
+    const int64_t nkb = K / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, sacc = 0.0;
+            for (int64_t kb = 0; kb < nkb; ++kb) {
+                double part, spart;
+                dot_one(ca + m * (K / 2) + kb * 64, sa + m * (K / 32) + kb * 4, cb + n * (K / 2) + kb * 64,
+                        sb + n * (K / 32) + kb * 4, 128, &part, &spart);
+                const double fa = mbs_a ? 1.0 / (1.0 + mbs_a[m * nkb + kb] / 256.0) : 1.0;
+                const double fb = mbs_b ? 1.0 / (1.0 + mbs_b[n * nkb + kb] / 256.0) : 1.0;
+                acc += fa * fb * part;
+                sacc += fa * fb * spart;
+            }
+            C[m * N + n] = acc;
+            if (S) S[m * N + n] = sacc;
+        }
+}
+
 /* ------------------------------------------------------------------------- */
 /* Randomised baselines ([MXFP4-HW] A.2 and "experiments", table 1: random sign */
 /* flips before the Hadamard, stochastic rounding)                             */

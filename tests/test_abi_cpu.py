@@ -324,3 +324,14 @@ def test_philox_quantiser_rejects_bad_arguments(L):
     assert ph(rows=40) == 2                               # the transposed copy needs rows % 32
     assert ph(x=0x1008) == 3
     assert ph(rows=0) == 0                                # empty: nothing touched
+
+
+def test_gemm_mbs_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    g = lambda A, B, C=0x40000, ldc=128: L.mxfp4_gemm_mbs(ctypes.byref(A), P(0x9000), ctypes.byref(B), None, P(C),
+                                                           ldc, 0, 0, None)
+    assert g(_tensor(cols=256), _tensor(cols=256)) == PASSED_VALIDATION
+    assert g(_tensor(cols=160), _tensor(cols=160)) == 2            # K % 128
+    assert g(_tensor(cols=16512), _tensor(cols=16512)) == 2        # K above 16384
+    assert g(_tensor(cols=256, had=16), _tensor(cols=256, had=32)) == 1
+    assert g(_tensor(cols=256), _tensor(cols=256), ldc=100) == 3

@@ -190,3 +190,50 @@ def test_of_never_increases_the_error_elementwise(had, mode):
     # and it recovers most of the first pass's deadzone
     dz = (q1 == 0) & (v != 0)
     assert dz.sum() > 0 and np.mean(xof[dz] != 0) > 0.5
+
+
+# ---------------------------------------------------------------- GEMM over MBS operands
+def test_mbs_gemm_without_correction_is_the_plain_gemm():
+    """All MBS bytes zero (factor 1): the MBS GEMM is the pinned plain GEMM, exactly."""
+    qa = oracle.quantize(synth.activations(64, 512, 1), 16, 0, "row")
+    qb = oracle.quantize(synth.weights(48, 512, 2), 16, 0, "row")
+    z_a, z_b = np.zeros((64, 4), np.uint8), np.zeros((48, 4), np.uint8)
+    C, S = oracle.gemm_mbs(qa[0], qa[1], z_a, qb[0], qb[1], z_b)
+    C0, S0 = oracle.gemm(*qa, *qb)
+    assert np.array_equal(C, C0) and np.array_equal(S, S0)
+    C1, _ = oracle.gemm_mbs(qa[0], qa[1], None, qb[0], qb[1], None)
+    assert np.array_equal(C1, C0)
+
+
+@pytest.mark.parametrize("which", ["both", "a", "b"])
+def test_mbs_gemm_is_the_product_of_the_reconstructions(which):
+    """C = x_hat_A x_hat_B^T with x_hat the MBS reconstruction dq(q) / (1 + byte/256)
+    (pinned by the MBS closed-form tests above): an fp64 matmul of the reconstructions
+    agrees to fp64 rounding, for one or both operands under MBS."""
+    X = synth.activations(96, 640, 3)
+    W = synth.weights(80, 640, 4)
+    ca, sa, ma = oracle.quantize_mbs(X, 16, 0)
+    cb, sb, mb = oracle.quantize_mbs(W, 16, 1)
+    use_a, use_b = which in ("both", "a"), which in ("both", "b")
+    if not use_a:
+        ca, sa = oracle.quantize(X, 16, 0, "row")
+    if not use_b:
+        cb, sb = oracle.quantize(W, 16, 1, "row")
+    C, S = oracle.gemm_mbs(ca, sa, ma if use_a else None, cb, sb, mb if use_b else None)
+    xa = oracle.dequant_mbs(ca, sa, ma) if use_a else oracle.dequant_row(ca, sa)
+    xb = oracle.dequant_mbs(cb, sb, mb) if use_b else oracle.dequant_row(cb, sb)
+    ref = xa @ xb.T
+    assert np.all(np.abs(C - ref) <= 1e-12 * S + 1e-300)
+    assert np.allclose(S, np.abs(xa) @ np.abs(xb).T, rtol=1e-12, atol=0)
+    assert (ma > 0).any() and (mb > 0).any()  # the data exercises the correction
+
+
+def test_mbs_gemm_single_macro_block_by_hand():
+    """K = 128, every code 1.0 (code 2) under scale byte 127 on both sides: the plain dot
+    is 128; MBS bytes 128 on A (factor 1/1.5) and 64 on B (factor 1/1.25) give
+    128 / (1.5 * 1.25) = 68.2666..., exactly in rationals."""
+    codes = np.full((1, 64), 0x22, np.uint8)
+    scales = np.full((1, 4), 127, np.uint8)
+    C, S = oracle.gemm_mbs(codes, scales, np.array([[128]], np.uint8), codes, scales, np.array([[64]], np.uint8))
+    want = Fraction(128) / (Fraction(3, 2) * Fraction(5, 4))
+    assert abs(Fraction(float(C[0, 0])) - want) <= Fraction(1, 2 ** 45) and abs(Fraction(float(S[0, 0])) - want) <= Fraction(1, 2 ** 45)

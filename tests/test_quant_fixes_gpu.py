@@ -160,3 +160,76 @@ def test_of_and_mbs_strided_inputs(torch, pad, offset):
     same(q.plain_scales(), s, "MBS scales")
     same(q.codes.cpu().numpy(), c, "MBS codes")
     same(mbs.cpu().numpy(), m, "MBS bytes")
+
+
+# ---------------------------------------------------------------- GEMM over MBS operands
+def _mbs_operands(mx, X, W, which, had=16, mode=0):
+    """GPU MBS (or plain) copies of X and W and the oracle's own copies of the same."""
+    xa, xb = mx.bf16_tensor(X), mx.bf16_tensor(W)
+    out = []
+    for x, bits, use in ((xa, X, which in ("both", "a")), (xb, W, which in ("both", "b"))):
+        if use:
+            q, m = mx.rotate_quantize_mbs(x, had=had, mode=mode)
+            oc, os_, om = oracle.quantize_mbs(bits, had, mode)
+        else:
+            q, m = mx.rotate_quantize(x, had=had, mode=mode, layouts=mx.LAYOUT_ROW)["row"], None
+            (oc, os_), om = oracle.quantize(bits, had, mode, "row"), None
+        out.append((q, m, oc, os_, om))
+    return out
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 512), (200, 136, 384), (384, 520, 1024)])
+@pytest.mark.parametrize("which", ["both", "a", "b"])
+def test_gemm_over_mbs_operands(torch, shape, which):
+    """C = x_hat_A x_hat_B^T with each 128-element macro block's partial product scaled by
+    its postscale factors: within the GEMM tolerance of the oracle's fp64 MBS GEMM, for
+    ragged shapes (an odd number of macro blocks: K = 384), fp32 and bf16 output, and
+    accumulation."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+    from tests.gpu_util import assert_within
+
+    M, N, K = shape
+    X, W, _ = synth.linear_inputs(M, N, K, 90 + M)
+    (qa, ma, ca, sa, oma), (qb, mb, cb, sb, omb) = _mbs_operands(mx, X, W, which)
+    want, S = oracle.gemm_mbs(ca, sa, oma, cb, sb, omb)
+    C = mx.gemm_mbs(qa, ma, qb, mb)
+    Cb = mx.gemm_mbs(qa, ma, qb, mb, out_dtype=mx.OUT_BF16)
+    Cacc = torch.full((M, N), -1.5, dtype=torch.float32, device="cuda")
+    mx.gemm_mbs(qa, ma, qb, mb, accumulate=True, out=Cacc)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    assert_within(C.double().cpu().numpy(), want, S, what=f"mbs gemm {shape} {which}")
+    assert_within(Cb.double().cpu().numpy(), want, S, bf16=True, what=f"mbs gemm bf16 {shape} {which}")
+    assert_within(Cacc.double().cpu().numpy(), want - 1.5, S, what=f"mbs gemm accumulate {shape} {which}")
+    if which == "both":  # the correction is not a no-op on this data
+        plain, _ = oracle.gemm(ca, sa, cb, sb)
+        assert np.abs(plain - want).max() > 1e-3 * np.abs(want).max()
+
+
+def test_gemm_over_mbs_operands_full_size_sampled(torch):
+    """An o-projection-sized Fprop (8192 x 4096 x 4096) over MBS activations and weights:
+    every output row and column sampled (first, last and random 64) against the oracle."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+    from tests.gpu_util import assert_within
+
+    M, N, K = 8192, 4096, 4096
+    X, W, _ = synth.linear_inputs(M, N, K, 2011)
+    (qa, ma, ca, sa, oma), (qb, mb, cb, sb, omb) = _mbs_operands(mx, X, W, "both")
+    C = mx.gemm_mbs(qa, ma, qb, mb, out_dtype=mx.OUT_BF16)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    g = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([np.arange(64), np.arange(M - 64, M), g.integers(0, M, 64)]))
+    cols = np.unique(np.concatenate([np.arange(64), np.arange(N - 64, N), g.integers(0, N, 64)]))
+    want, S = oracle.gemm_mbs(ca[rows], sa[rows], oma[rows], cb[cols], sb[cols], omb[cols])
+    got = C[torch.as_tensor(rows, device="cuda")][:, torch.as_tensor(cols, device="cuda")]
+    assert_within(got.double().cpu().numpy(), want, S, bf16=True, what="mbs gemm 8192x4096x4096")
+
+
+def test_gemm_mbs_rejects_k_beyond_its_macro_blocks(torch):
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    q = mx.rotate_quantize(mx.bf16_tensor(synth.activations(128, 320, 1)), layouts=mx.LAYOUT_ROW)["row"]
+    with pytest.raises(mx.Mxfp4Error) as e:
+        mx.gemm_mbs(q, None, q, None)  # K = 320 is not a multiple of 128
+    assert e.value.status == 2
