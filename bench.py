@@ -1259,10 +1259,11 @@ def profile_case(which="classes"):
       classes (mxf4_gemm): gate/up Fprop 8192x14336x4096 bf16 out (-s 1), gate/up Wgrad
       14336x4096x8192 fp32 out (-s 3), k/v Dgrad 8192x4096x1024 bf16 out (-s 5), k/v Fprop
       8192x1024x4096 bf16 out (-s 7), k/v Wgrad 1024x4096x8192 fp32 out (-s 9).
-    step: the headline step's 20 launches (4 X+W pair and 4 dY quantisations, 12 GEMMs)
+    step: the headline step's 16 launches (4 X+W pair and 4 dY quantisations, 8 GEMMs)
       twice, on stream launches; capture one kernel's second round for its DRAM bytes per
-      launch: -k regex:mxf4_gemm -s 12 -c 12, or -k regex:rq_kernel -s 8 -c 8 (DRAM
-      counters only: one pass, nothing saved or restored between passes)."""
+      launch: -k regex:mxf4_gemm -s 8 -c 8 (4 Fprops and 4 grouped backward launches), or
+      -k regex:rq_kernel -s 8 -c 8 (4 X+W pair and 4 dY launches); DRAM counters only: one
+      pass, nothing saved or restored between passes."""
     import torch
 
     from mxfp4_precision_gemms_gb300 import binding as mx
@@ -1304,7 +1305,7 @@ def profile_case(which="classes"):
 
 TRAFFIC_COMMAND = (
     "python bench.py --profile-case step > gpurun_out/pc.log 2>&1 && "
-    "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none -k regex:mxf4_gemm -s 12 -c 12 "
+    "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none -k regex:mxf4_gemm -s 8 -c 8 "
     "--csv --log-file gpurun_out/traffic_gemm.csv python bench.py --profile-case step && "
     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none -k regex:rq_kernel -s 8 -c 8 "
     "--csv --log-file gpurun_out/traffic_quant.csv python bench.py --profile-case step; then "
