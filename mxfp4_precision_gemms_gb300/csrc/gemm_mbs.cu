@@ -9,9 +9,9 @@
 //   C[m][n] = sum over macro blocks kb of  f_A[m][kb] f_B[n][kb] P_kb[m][n],
 //   P_kb = the block-scaled MXFP4 product over the 128 K of macro block kb,
 //   f = 256 / (256 + byte) (1 for an operand given without MBS bytes).
-// Each P_kb is formed on the tensor cores in one of two TMEM buffers; the epilogue warps
+// Each P_kb is formed on the tensor cores in one of three TMEM buffers; the epilogue warps
 // read it, scale it and add it into an fp32 register accumulator while the tensor cores
-// fill the other buffer.  At the tile's end the accumulator is stored like the plain
+// fill the next ones.  At the tile's end the accumulator is stored like the plain
 // GEMM's (TMA, bf16 or fp32, optional add-reduce).
 //
 // Structure (persistent, one CTA of 320 threads per SM walks 128 x 128 tiles):
@@ -20,11 +20,13 @@
 //   warp 1     TMEM allocation; one thread copies each stage's scales to TMEM and issues
 //              two MMAs (K = 64 each) per macro block into the macro block's buffer;
 //   warps 2-9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows) and half
-//              of the 128 columns.  The tile's column factors are computed once per tile
-//              into shared memory (K <= 16384).
+//              of the 128 columns.  Factors come from a 256-entry table in shared memory
+//              (one per MBS byte); the tile's column factors are looked up once per tile
+//              (K <= 16384), and each row's byte for the next macro block is loaded one
+//              macro block ahead.
 // Bounds: the rescale costs one packed multiply and one packed FMA per two outputs per
 // macro block on the CUDA cores, and a 128 x 128 tile moves twice the operand bytes per
-// FLOP of the CTA-pair kernel's 256 x 256 tile (two 128-column partial buffers leave no
+// FLOP of the CTA-pair kernel's 256 x 256 tile (three 128-column partial buffers leave no
 // room for wider tiles in TMEM).  All waits are bounded.
 #include <cuda_bf16.h>
 
@@ -36,6 +38,7 @@ namespace mx {
 namespace {
 
 constexpr int MB_STAGES = 4;
+constexpr int MB_BUFS = 3;  // TMEM partial buffers of 128 columns
 constexpr int MB_EPI_WARPS = 8;
 constexpr int MB_THREADS = 64 + 32 * MB_EPI_WARPS;
 constexpr int MB_STG_BYTES = 32 * 64;  // one warp's 32-row x 64-byte staging box
@@ -49,15 +52,16 @@ struct MbsCfg {
     static constexpr int OFF_SFA = OFF_B + MB_STAGES * B_STAGE;
     static constexpr int OFF_SFB = OFF_SFA + MB_STAGES * SF_STAGE;
     static constexpr int OFF_FB = OFF_SFB + MB_STAGES * SF_STAGE;  // column factors [kb][128] fp32
-    static constexpr int OFF_BAR = OFF_FB + kMbsMaxMacroBlocks * 128 * 4;
-    // full[S], empty[S], p_full[2], p_empty[2], mma_done
-    static constexpr int OFF_TMEM = OFF_BAR + (2 * MB_STAGES + 5) * 8;
+    static constexpr int OFF_LUT = OFF_FB + kMbsMaxMacroBlocks * 128 * 4;  // 256 / (256 + byte), 256 floats
+    static constexpr int OFF_BAR = OFF_LUT + 256 * 4;
+    // full[S], empty[S], p_full[B], p_empty[B], mma_done
+    static constexpr int OFF_TMEM = OFF_BAR + (2 * MB_STAGES + 2 * MB_BUFS + 1) * 8;
     static constexpr int OFF_STG = (OFF_TMEM + 16 + 1023) / 1024 * 1024;
     static constexpr int SMEM = OFF_STG + MB_EPI_WARPS * MB_STG_BYTES + 1024;  // + base alignment slack
     static constexpr uint32_t TX = A_STAGE + B_STAGE + 2 * SF_STAGE;
     static constexpr int SF_COLS = 16;  // TMEM columns of scales per stage: 8 for A, 8 for B
     static constexpr int TMEM_COLS = 512;
-    static_assert(2 * 128 + MB_STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+    static_assert(MB_BUFS * 128 + MB_STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(OFF_B % 1024 == 0 && OFF_BAR % 8 == 0 && OFF_FB % 16 == 0 && OFF_STG % 1024 == 0, "alignment");
 };
@@ -124,9 +128,10 @@ __global__ void __launch_bounds__(MB_THREADS, 1) mxf4_gemm_mbs_kernel(const __gr
     float* fB = reinterpret_cast<float*>(smem + Cfg::OFF_FB);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* empty = full + MB_STAGES;
-    uint64_t* p_full = empty + MB_STAGES;  // [2] MMA -> epilogue: a macro block's partial is ready
-    uint64_t* p_empty = p_full + 2;        // [2] epilogue -> MMA: the partial has been read
-    uint64_t* mma_done = p_empty + 2;
+    float* lut = reinterpret_cast<float*>(smem + Cfg::OFF_LUT);
+    uint64_t* p_full = empty + MB_STAGES;   // [B] MMA -> epilogue: a macro block's partial is ready
+    uint64_t* p_empty = p_full + MB_BUFS;   // [B] epilogue -> MMA: the partial has been read
+    uint64_t* mma_done = p_empty + MB_BUFS;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_TMEM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -141,7 +146,7 @@ __global__ void __launch_bounds__(MB_THREADS, 1) mxf4_gemm_mbs_kernel(const __gr
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < MB_BUFS; ++b) {
             mbar_init(&p_full[b], 1);
             mbar_init(&p_empty[b], MB_EPI_WARPS);
         }
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(MB_THREADS, 1) mxf4_gemm_mbs_kernel(const __gr
                 if (armed[s]) wait_bounded(&full[s], (armed[s] - 1u) & 1u, p.wait_ns, p.status);
         }
     } else if (warp == 1) {
-        // ---------------- tensor-core issuer: two MMAs per macro block into buffer j % 2
+        // ---------------- tensor-core issuer: two MMAs per macro block into buffer j % 3
         if (elect_one()) {
             constexpr uint32_t idesc = idesc_mxf4(128, 128);
             uint32_t it = 0, j = 0;
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(MB_THREADS, 1) mxf4_gemm_mbs_kernel(const __gr
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + 256 + s * Cfg::SF_COLS;
+                    const uint32_t sfa_t = tmem_base + MB_BUFS * 128 + s * Cfg::SF_COLS;
                     const uint32_t sfb_t = sfa_t + 8;
 #pragma unroll
                     for (int a = 0; a < 2; ++a) {
@@ -222,9 +227,9 @@ __global__ void __launch_bounds__(MB_THREADS, 1) mxf4_gemm_mbs_kernel(const __gr
                     const uint32_t a_base = smem_u32(sA + s * Cfg::A_STAGE);
                     const uint32_t b_base = smem_u32(sB + s * Cfg::B_STAGE);
                     for (int half = 0; half < 2 && 2 * kt + half < nkb; ++half, ++j) {
-                        const uint32_t b = j & 1u;
-                        if (j >= 2) {
-                            if (!wait_bounded(&p_empty[b], ((j >> 1) - 1u) & 1u, p.wait_ns, p.status)) {
+                        const uint32_t b = j % MB_BUFS;
+                        if (j >= MB_BUFS) {
+                            if (!wait_bounded(&p_empty[b], (j / MB_BUFS - 1u) & 1u, p.wait_ns, p.status)) {
                                 ok = false;
                                 break;
                             }
@@ -255,18 +260,21 @@ __global__ void __launch_bounds__(MB_THREADS, 1) mxf4_gemm_mbs_kernel(const __gr
         uint8_t* stg = smem + Cfg::OFF_STG + (warp - 2) * MB_STG_BYTES;
         uint32_t j = 0;
         bool ok = true;
+        lut[et] = mbs_factor((uint32_t)et);  // 256 epilogue threads, one entry each
         for (int64_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int64_t m0 = (tile / num_n) * 128, n0 = (tile % num_n) * 128;
             // the tile's column factors, once every warp is done with the previous tile's
+            // (the first barrier also publishes the table)
             epi_bar_sync();
             for (int idx = et; idx < nkb * 128; idx += 32 * MB_EPI_WARPS) {
                 const int kb = idx >> 7, c = idx & 127;
                 const int64_t n = n0 + c;
-                fB[idx] = (mp.mbs_b && n < p.N) ? mbs_factor(mp.mbs_b[n * nkb + kb]) : 1.0f;
+                fB[idx] = (mp.mbs_b && n < p.N) ? lut[mp.mbs_b[n * nkb + kb]] : 1.0f;
             }
             epi_bar_sync();
             const int64_t row = m0 + q * 32 + lane;
             const uint8_t* mrow = (mp.mbs_a && row < p.M) ? mp.mbs_a + row * nkb : nullptr;
+            uint32_t next_byte = mrow ? mrow[0] : 0u;  // this row's byte, one macro block ahead
             float2 acc[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.0f, 0.0f);
@@ -274,9 +282,10 @@ __global__ void __launch_bounds__(MB_THREADS, 1) mxf4_gemm_mbs_kernel(const __gr
                 // After an expired wait the loops keep their shape (no more waits, loads or
                 // stores), so every epilogue warp still reaches the tile's two barriers.
                 if (!ok) continue;
-                const float fa = mrow ? mbs_factor(mrow[kb]) : 1.0f;
-                const uint32_t b = j & 1u;
-                if (!wait_bounded(&p_full[b], (j >> 1) & 1u, p.wait_ns, p.status)) {
+                const float fa = mrow ? lut[next_byte] : 1.0f;
+                if (mrow && kb + 1 < nkb) next_byte = mrow[kb + 1];
+                const uint32_t b = j % MB_BUFS;
+                if (!wait_bounded(&p_full[b], (j / MB_BUFS) & 1u, p.wait_ns, p.status)) {
                     ok = false;
                     continue;
                 }
