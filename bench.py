@@ -129,7 +129,7 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, mem, mx, reasons = [], [], None, set()
+        sm, mem, mx, reasons, power, capped = [], [], None, set(), [], 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             p = [x.strip() for x in line.split(",")]
@@ -140,16 +140,23 @@ class ClockSampler:
                 mx = float(p[2])
             except ValueError:
                 continue
+            try:
+                power.append(float(p[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, p[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+                    capped += n == "sw_power_cap"
             if len(p) > 9:
                 try:
                     mem.append(float(p[9]))
                 except ValueError:
                     pass
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "mem_mhz": statistics.median(mem) if mem else None, "samples": len(sm)}
+                "mem_mhz": statistics.median(mem) if mem else None, "samples": len(sm),
+                "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(power) if power else None,
+                "power_cap_samples": capped}
 
 
 # --------------------------------------------------------------------------- ncu traffic
@@ -752,6 +759,7 @@ def wgrad_stress_leg(flush, steps, fp4_peak, hbm):
 
 BLOCK_INPUTS = (("attn_in", 4096, ("q", "k", "v")), ("o_in", 4096, ("o",)), ("mlp_in", 4096, ("gate", "up")),
                 ("down_in", 14336, ("down",)))
+BLOCK_SEED = 4000
 
 
 class BlockInput:
@@ -795,6 +803,21 @@ class BlockLinear:
         self.dw = torch.empty((N, K), dtype=torch.float32, device=dev)
         self.quant_bytes = quant_bytes(N, K, True) + quant_bytes(M, N, True)
         self.gemm_flops = 3 * 2 * M * N * K
+
+
+def make_block_groups(dev, seed=BLOCK_SEED):
+    """The decoder block's activations, each with the linears that read it:
+    [(BlockInput, [BlockLinear, ...]), ...].  Activation g draws from seed + 100 g and
+    its j-th linear from seed + 100 g + 10 (j + 1) (W at +1, dY at +2)."""
+    from mxfp4_precision_gemms_gb300 import synth
+
+    shapes = dict((n, N) for n, N, _ in synth.LLAMA8B_BLOCK_LINEARS)
+    groups = []
+    for gi, (iname, K, names) in enumerate(BLOCK_INPUTS):
+        inp = BlockInput(iname, K, seed + 100 * gi, dev)
+        groups.append((inp, [BlockLinear(n, shapes[n], inp, seed + 100 * gi + 10 * (j + 1), dev)
+                             for j, n in enumerate(names)]))
+    return groups
 
 
 def run_block(groups, ev=None):
@@ -895,12 +918,7 @@ def decoder_block_leg(flush, steps, warmup, dev):
     from mxfp4_precision_gemms_gb300 import binding as mx
     from mxfp4_precision_gemms_gb300 import synth
 
-    shapes = dict((n, N) for n, N, _ in synth.LLAMA8B_BLOCK_LINEARS)
-    groups = []
-    for gi, (iname, K, names) in enumerate(BLOCK_INPUTS):
-        inp = BlockInput(iname, K, 4000 + 100 * gi, dev)
-        groups.append((inp, [BlockLinear(n, shapes[n], inp, 4000 + 100 * gi + 10 * (j + 1), dev)
-                             for j, n in enumerate(names)]))
+    groups = make_block_groups(dev)
     linears = [L for _, lins in groups for L in lins]
     fl = sum(L.gemm_flops for L in linears)
     for _ in range(warmup):

@@ -81,17 +81,11 @@ def test_decoder_block_graph_matches_serial_launches():
     import torch
 
     from mxfp4_precision_gemms_gb300 import binding as mx
-    from mxfp4_precision_gemms_gb300 import synth
 
     bench = _bench()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    shapes = dict((n, N) for n, N, _ in synth.LLAMA8B_BLOCK_LINEARS)
-    groups = []
-    for gi, (iname, K, names) in enumerate(bench.BLOCK_INPUTS):
-        inp = bench.BlockInput(iname, K, 4000 + 100 * gi, dev)
-        groups.append((inp, [bench.BlockLinear(n, shapes[n], inp, 4000 + 100 * gi + 10 * (j + 1), dev)
-                             for j, n in enumerate(names)]))
+    groups = bench.make_block_groups(dev)
     outs = lambda: [t for _, lins in groups for L in lins for t in (L.y, L.dx, L.dw)]
     bench.run_block(groups)
     torch.cuda.synchronize()

@@ -133,3 +133,28 @@ def test_linear_backward_equals_dgrad_plus_wgrad(torch, had, mode):
     torch.cuda.synchronize()
     want, S = oracle.wgrad(dY, X, {0: 1, 16: 16, 32: 32}[had], mode)
     assert_within(dw2.double().cpu().numpy(), want + 0.25, S, what="backward dW accumulate")
+
+
+def test_group_with_narrow_problems(torch):
+    """Problems with M <= 128 or N <= 128 (which a single launch would give the single-CTA
+    kernel) run on the pair kernel inside a group: half-empty tiles are zero-filled on load
+    and clipped on store.  Outputs within tolerance, and no byte outside them is written."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    shapes = [(64, 512, 512), (1024, 96, 256), (96, 64, 1024), (512, 384, 768)]
+    ops, wants, guards = [], [], []
+    for i, (M, N, K) in enumerate(shapes):
+        qa = oracle.quantize(synth.activations(M, K, 80 + i), 16, 0, "row")
+        qb = oracle.quantize(synth.weights(N, K, 90 + i), 16, 0, "row")
+        A, B = mx.qtensor_from_host(*qa, had=16), mx.qtensor_from_host(*qb, had=16)
+        # C inside a larger buffer with ldc = N + 8: the padding columns must stay untouched
+        buf = torch.full((M, N + 8), 3.25, dtype=torch.float32, device="cuda")
+        ops.append((A, B, mx.OUT_F32, False, buf[:, :N]))
+        wants.append(oracle.gemm(*qa, *qb))
+        guards.append(buf)
+    mx.gemm_group(ops)
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    for (M, N, K), buf, (want, S) in zip(shapes, guards, wants):
+        assert_within(buf[:, :N].double().cpu().numpy(), want, S, what=f"narrow group {M}x{N}x{K}")
+        assert torch.all(buf[:, N:] == 3.25), f"{M}x{N}x{K}: padding written"

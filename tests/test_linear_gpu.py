@@ -160,3 +160,36 @@ def test_cuda_graph_replay_matches_eager(torch):
         assert torch.equal(eager[k], cap[k]), k
     for k in ("xT", "wT", "dyT"):
         assert torch.equal(eager[k].codes, cap[k].codes) and torch.equal(eager[k].scales, cap[k].scales), k
+
+
+def test_decoder_block_sampled(torch):
+    """The Llama-3.1-8B-shaped decoder block (q, k, v, o, gate, up, down at T = 8192,
+    H16, OCP floor) exactly as the benchmark times it -- the 20-launch grouped graph,
+    activations quantised once and shared by the linears that read them -- against the
+    oracle on sampled Y, dX and dW of every linear, from the same seeded inputs."""
+    import importlib.util
+    import os
+
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("bench_block_mod", os.path.join(root, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    dev = torch.device("cuda", 0)
+    groups = bench.make_block_groups(dev)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        bench.run_block_grouped(groups)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    T = bench.T_TOKENS
+    for gi, (inp, lins) in enumerate(groups):
+        X = synth.activations(T, inp.K, bench.BLOCK_SEED + 100 * gi)
+        for j, L in enumerate(lins):
+            s = bench.BLOCK_SEED + 100 * gi + 10 * (j + 1)
+            W, dY = synth.weights(L.N, L.K, s + 1), synth.output_grads(T, L.N, s + 2)
+            _sampled_checks(torch, X, W, dY, 16, 0, L.y, L.dx, L.dw, n=96, seed=gi * 10 + j)
