@@ -1326,7 +1326,7 @@ TRAFFIC_COMMAND = (
     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none -k regex:mxf4_gemm -s 8 -c 8 "
     "--csv --log-file gpurun_out/traffic_gemm.csv python bench.py --profile-case step && "
     "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none -k regex:rq_kernel -s 8 -c 8 "
-    "--csv --log-file gpurun_out/traffic_quant.csv python bench.py --profile-case step; then "
+    "--csv --log-file gpurun_out/traffic_quant.csv python bench.py --profile-case step && "
     "python bench.py --traffic-from gpurun_out/traffic_gemm.csv gpurun_out/traffic_quant.csv")
 
 
