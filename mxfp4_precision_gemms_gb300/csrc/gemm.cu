@@ -394,7 +394,7 @@ struct PairCfg {
 };
 
 // The problem that global tile `tile` of a group belongs to, and the tile's index within
-// that problem (tiles are numbered problem after problem, row-major within each).
+// that problem (tiles are numbered problem after problem; pair_tile_origin places them).
 __device__ __forceinline__ int group_problem(const GemmGroup& g, int64_t tile, int64_t& local) {
     int pi = 0;
 #pragma unroll
@@ -402,6 +402,24 @@ __device__ __forceinline__ int group_problem(const GemmGroup& g, int64_t tile, i
         if (i < g.count && tile >= g.tile_start[i]) pi = i;
     local = tile - g.tile_start[pi];
     return pi;
+}
+
+// Origin (m0, n0) of tile lt of problem p's 256 x 256 tiling.  Consecutive tiles --
+// which run at the same time on neighbouring clusters -- walk the dimension with fewer
+// tiles fastest: the operand along it is then read by every wave and stays in L2, while
+// the other operand streams through once.  (Measured on the down-projection Wgrad,
+// 4096 x 14336 x 8192 with fp32 output: walking N fastest re-read the 62 MB B operand
+// from DRAM in every wave, the fp32 output evicting it from L2; walking M fastest ran
+// 8% faster.  The other Llama-shaped GEMMs were unchanged.)
+__device__ __forceinline__ void pair_tile_origin(const GemmParams& p, int64_t lt, int64_t& m0, int64_t& n0) {
+    const int64_t num_m = (p.M + 255) / 256, num_n = (p.N + 255) / 256;
+    if (num_n > num_m) {
+        m0 = (lt % num_m) * 256;
+        n0 = (lt / num_m) * 256;
+    } else {
+        m0 = (lt / num_n) * 256;
+        n0 = (lt % num_n) * 256;
+    }
 }
 
 template <int STAGES>
@@ -475,9 +493,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
                 int64_t lt;
                 const GemmParams& p = g.prob[group_problem(g, tile, lt)];
                 const int num_k = (int)((p.K + 255) / 256);
-                const int64_t num_n = (p.N + 255) / 256;
                 const int64_t atoms_per_row_block = p.kb_pad / 4;
-                const int64_t m0 = (lt / num_n) * 256, n0 = (lt % num_n) * 256;
+                int64_t m0, n0;
+                pair_tile_origin(p, lt, m0, n0);
                 const int32_t ya = (int32_t)(m0 + rank * 128), yb = (int32_t)(n0 + rank * 128);
                 const int32_t sfa_y = (int32_t)((m0 / 128 + rank) * atoms_per_row_block * 4);
                 const int32_t sfb_y0 = (int32_t)((n0 / 128) * atoms_per_row_block * 4);
@@ -586,9 +604,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) mxf4_gemm_pair_kernel(const _
             tc_fence_after();
             int64_t lt;
             const GemmParams& p = g.prob[group_problem(g, tile, lt)];
-            const int64_t num_n = (p.N + 255) / 256;
-            const int64_t row_base = (lt / num_n) * 256 + rank * 128 + q * 32;
-            const int64_t c0 = (lt % num_n) * 256 + h * 128;
+            int64_t m0, n0;
+            pair_tile_origin(p, lt, m0, n0);
+            const int64_t row_base = m0 + rank * 128 + q * 32;
+            const int64_t c0 = n0 + h * 128;
             uint32_t v[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c)
