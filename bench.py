@@ -409,6 +409,31 @@ def link_bandwidth(nbytes=256 << 20, reps=3):
     return {"h2d_gbs": round(h2d, 1), "d2h_gbs": round(d2h, 1), "concurrent_total_gbs": round(bi, 1)}
 
 
+def size_matched_copy_ms(flush, sizes, dev, reps=5):
+    """Sum over `sizes` (bytes) of the device time of a torch copy that reads and writes
+    size / 2 bytes each, L2 emptied before every copy (median of `reps`)."""
+    import torch
+
+    total = 0.0
+    for nbytes in sizes:
+        n = max(16, int(nbytes) // 2)
+        src = torch.ones(n, dtype=torch.uint8, device=dev)
+        dst = torch.empty(n, dtype=torch.uint8, device=dev)
+        dst.copy_(src)
+        t = []
+        for _ in range(reps):
+            flush()
+            a, b = _ev_pair()
+            a.record()
+            dst.copy_(src)
+            b.record()
+            b.synchronize()
+            t.append(a.elapsed_time(b))
+        total += sorted(t)[len(t) // 2]
+        del src, dst
+    return total
+
+
 class L2Flush:
     """Empties L2 between timed iterations: a 256 MB write (larger than the 129 MB L2),
     then a 256 MB read of a second buffer, which evicts the written lines.  The timed
@@ -534,6 +559,16 @@ def gpu_arm(args, rank, world, dist):
     roof_quant = {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": hbm, "unit": "GB/s",
                   "frac": round(quant_gbs / hbm, 4), "traffic": traffic["quant"], "kernel": "rq_kernel",
                   "peak_source": "measured (hbm_gbs), of measured"}
+    # Context for the quantiser's fraction: device copies (torch) moving the same bytes as
+    # each of the step's quantisation launches, one copy per launch, L2 emptied before
+    # each.  A launch of tens of MB pays ramp-up and drain that a 4 GB copy amortises.
+    q_sizes = [work for kind, _, _, work in kern_ev if kind == "quant"][:q_n // max(1, args.steps)]
+    copy_ms = size_matched_copy_ms(flush, q_sizes, dev)
+    roof_quant["size_matched_copy"] = {
+        "gbs": round(sum(q_sizes) / (copy_ms * 1e-3) / 1e9, 1),
+        "quant_over_copy": round(copy_ms * max(1, args.steps) / q_ms, 4) if q_ms else None,
+        "how": "one device copy per quantisation launch of a step, reading and writing half of that launch's "
+               "bytes each; L2 emptied before every copy; median of 5"}
     dominant = roof_gemm if gemm_share >= 0.5 else roof_quant
 
     # ---- end to end through the public API with host buffers

@@ -31,8 +31,12 @@ constexpr int TR = 64;        // tile rows
 constexpr int TC = 128;       // tile cols
 constexpr int QTHREADS = 2 * TR;
 // Launch bound: CTAs per SM the register allocation must allow.  Six (80 registers, no
-// spills) beat four (122 registers) by 7-9% on the dual pass; seven and eight spill.
+// spills) beat four (122 registers) by 7-9% on the dual pass.  The dual pass takes seven
+// (72 registers; under H16 a 12-byte spill): measured 2% faster than six on 8192 x 14336
+// and on the Llama-3.1-8B step's quantisations, outputs byte-identical.  Eight spill
+// hundreds of bytes.  Single-copy passes keep six.
 constexpr int QBLOCKS_PER_SM = 6;
+constexpr int QBLOCKS_DUAL = 7;
 constexpr int TILE_BYTES = TR * TC * 2;  // the raw bf16 tile
 
 // One launch over up to two matrices with the same number of columns (a GEMM's two
@@ -47,7 +51,7 @@ struct QuantGroup {
 // one matrix keeps every parameter at a constant offset.  Measured: a single-matrix
 // launch that indexed its parameters like a pair ran 4-6% slower.
 template <int HAD, bool ROW, bool COLT, bool TWOD, bool PAIR>
-__global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : QBLOCKS_PER_SM) rq_kernel(const __grid_constant__ QuantGroup g) {
+__global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : (ROW && COLT) ? QBLOCKS_DUAL : QBLOCKS_PER_SM) rq_kernel(const __grid_constant__ QuantGroup g) {
     extern __shared__ __align__(16) uint8_t q_smem[];
     uint32_t* tile_w = reinterpret_cast<uint32_t*>(q_smem);
     float* seg_amax = reinterpret_cast<float*>(q_smem + (COLT ? TILE_BYTES : 0));
