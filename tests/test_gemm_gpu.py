@@ -143,3 +143,15 @@ def test_back_to_back_accumulate_chain(torch):
     # each fp32 add of the running value rounds once more: allow 2^-22 of the magnitudes
     assert_within(got, w1 + 3 * w2, S1 + 3 * S2 + 2.4e-7 * (np.abs(w1) + 3 * np.abs(w2)) / 1e-5,
                   what="accumulate chain")
+
+
+@pytest.mark.parametrize("shape", [(544, 20000, 256), (20000, 544, 256)])
+def test_many_waves_both_tile_orders(torch, shape):
+    """More column tiles than row tiles (3 x 79: tiles walk M fastest) and the transpose
+    (79 x 3: N fastest), both with ragged edges and about three tiles per CTA pair, so
+    every pair wraps around the walked dimension several times."""
+    M, N, K = shape
+    qa, qb = oracle_operands(M, N, K, 15)
+    want, S = oracle.gemm(*qa, *qb)
+    assert_within(run(torch, qa, qb), want, S, what=f"{shape}")
+    assert_within(run(torch, qa, qb, out_dtype=1), want, S, bf16=True, what=f"{shape} bf16")
