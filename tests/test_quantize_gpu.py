@@ -123,12 +123,23 @@ def test_config1_4096(torch, had, mode):
     check(torch, x, had, mode, 4, 0, "4096^2 2d")
 
 
+@pytest.fixture(scope="module")
+def x_8192x14336():
+    return synth.heavy_tailed(8192, 14336, 1001)
+
+
+@pytest.mark.parametrize("had", [0, 16, 32])
 @pytest.mark.parametrize("mode", [0, 1])
-def test_config1_8192x14336(torch, mode):
-    x = synth.heavy_tailed(8192, 14336, 1001)
-    check(torch, x, 16, mode, 1 | 2, 1, "8192x14336 H16 row+colT")
-    if mode == 0:
-        check(torch, x, 32, mode, 4, 0, "8192x14336 H32 2d")
+def test_config1_8192x14336(torch, x_8192x14336, had, mode):
+    """The whole config-1 sweep at its full size, every kernel instance the benchmark's
+    sweep times: the row + transposed pass and the row-only and transposed-only passes
+    (scales in the GEMM's order), and the 2D pass (plain scales)."""
+    x = x_8192x14336
+    what = f"8192x14336 had={had} mode={mode}"
+    check(torch, x, had, mode, 1 | 2, 1, what + " row+colT")
+    check(torch, x, had, mode, 1, 1, what + " row")
+    check(torch, x, had, mode, 2, 1, what + " colT")
+    check(torch, x, had, mode, 4, 0, what + " 2d")
 
 
 def test_empty_input(torch):
