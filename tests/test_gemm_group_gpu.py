@@ -158,3 +158,30 @@ def test_group_with_narrow_problems(torch):
     for (M, N, K), buf, (want, S) in zip(shapes, guards, wants):
         assert_within(buf[:, :N].double().cpu().numpy(), want, S, what=f"narrow group {M}x{N}x{K}")
         assert torch.all(buf[:, N:] == 3.25), f"{M}x{N}x{K}: padding written"
+
+
+def test_eight_problem_group(torch):
+    """The largest group (8 problems): contractions from 256 to 2048, ragged shapes,
+    problems whose tiles walk M fastest (more column than row tiles) and N fastest, bf16
+    and fp32 outputs.  Each output equals its own launch bit for bit and the oracle
+    within tolerance."""
+    from mxfp4_precision_gemms_gb300 import binding as mx
+
+    shapes = [(256, 1024, 512), (1024, 256, 512), (384, 384, 1024), (512, 768, 256), (300, 640, 768),
+              (640, 300, 256), (256, 256, 2048), (768, 1280, 512)]
+    ops, refs = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        qa = oracle.quantize(synth.activations(M, K, 70 + i), 16, 0, "row")
+        qb = oracle.quantize(synth.weights(N, K, 80 + i), 16, 0, "row")
+        A, B = mx.qtensor_from_host(*qa, had=16), mx.qtensor_from_host(*qb, had=16)
+        od = mx.OUT_BF16 if i % 2 else mx.OUT_F32
+        ops.append((A, B, od, False, None))
+        refs.append((qa, qb, od))
+    outs = mx.gemm_group(ops)
+    singles = [mx.gemm(A, B, od) for A, B, od, _, _ in ops]
+    torch.cuda.synchronize()
+    assert mx.device_status() == 0
+    for (M, N, K), out, one, (qa, qb, od) in zip(shapes, outs, singles, refs):
+        assert torch.equal(out, one), f"group vs single launch {M}x{N}x{K}"
+        want, S = oracle.gemm(*qa, *qb)
+        assert_within(out.double().cpu().numpy(), want, S, bf16=od == mx.OUT_BF16, what=f"group of 8 {M}x{N}x{K}")

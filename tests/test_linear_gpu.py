@@ -95,6 +95,16 @@ def test_llama8b_linears_sampled(torch, name, N, K):
     _sampled_checks(torch, X, W, dY, 16, 0, y, dx, dw)
 
 
+@pytest.mark.parametrize("had,mode", [(32, 0), (0, 0), (16, 1)])
+def test_llama8b_qkv_other_rotations_sampled(torch, had, mode):
+    """The QKV linear at T = 8192 under H32 and without rotation (the H32 leg of the
+    benchmark), and under H16 with the ceiling scale."""
+    T, N, K = 8192, 6144, 4096
+    X, W, dY = synth.linear_inputs(T, N, K, 2000)
+    y, dx, dw, *_ = run_linear(torch, X, W, dY, had, mode, out_dtype=1)
+    _sampled_checks(torch, X, W, dY, had, mode, y, dx, dw, n=128, seed=had + mode)
+
+
 @pytest.mark.parametrize("had", [16, 32, 0])
 def test_wgrad_stress_sampled(torch, had):
     """Config 3: dW = dY^T X over T = 32768 tokens, dY [32768, 4096], X [32768, 14336]."""
