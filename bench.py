@@ -17,6 +17,7 @@ time is the max over ranks and the value counts all ranks' work.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -45,12 +46,13 @@ def flops_per_step(linears=None):
 
 
 def step_stats(ms):
-    """Median and 10th / 90th percentiles of the timed steps' durations (ms)."""
+    """Median, 10th / 90th percentiles and maximum of the timed steps' durations (ms)."""
     v = sorted(ms)
     if not v:
         return None
     q = lambda f: v[min(len(v) - 1, int(round(f * (len(v) - 1))))]
-    return {"median": round(statistics.median(v), 4), "p10": round(q(0.1), 4), "p90": round(q(0.9), 4)}
+    return {"median": round(statistics.median(v), 4), "p10": round(q(0.1), 4), "p90": round(q(0.9), 4),
+            "max": round(v[-1], 4)}
 
 
 def quant_bytes(R, C, dual):
@@ -583,17 +585,45 @@ def gpu_arm(args, rank, world, dist):
         for _ in range(max(1, args.warmup)):
             run_e2e_step(layers, ws, streams)
         torch.cuda.synchronize()
-        e2e_ms = []
-        barrier(dist)
-        for _ in range(args.steps):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
+        # The same step captured once as a CUDA graph (every API call, copy and event of
+        # it; the calls make no host syncs or allocations) and replayed: the host issues
+        # one launch per step, so a host-side stall cannot leave the GPU idle inside the
+        # timed interval.  The step issued call by call is timed too (`eager`), with the
+        # garbage collector paused while it is issued.
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        e2e_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(e2e_graph, stream=side):
             run_e2e_step(layers, ws, streams)
-            b.record()
-            b.synchronize()
-            e2e_ms.append(a.elapsed_time(b))
+        torch.cuda.synchronize()
+        for _ in range(max(1, args.warmup)):
+            e2e_graph.replay()
+        torch.cuda.synchronize()
+
+        def timed_steps(step):
+            ms = []
+            gc_was_on = gc.isenabled()
+            gc.disable()
+            try:
+                for _ in range(args.steps):
+                    flush()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    step()
+                    b.record()
+                    b.synchronize()
+                    ms.append(a.elapsed_time(b))
+            finally:
+                if gc_was_on:
+                    gc.enable()
+            return ms
+
+        barrier(dist)
+        e2e_ms = timed_steps(e2e_graph.replay)
+        barrier(dist)
+        eager_ms = timed_steps(lambda: run_e2e_step(layers, ws, streams))
         e2e_value, e2e_ms_per_step = job_throughput(sum(e2e_ms), fl, args.steps, world, dist, dev)
+        eager_value, eager_ms_per_step = job_throughput(sum(eager_ms), fl, args.steps, world, dist, dev)
         h2d = sum(L.x.numel() * 2 + L.w.numel() * 2 + L.dy.numel() * 2 for L in layers)
         d2h = sum(L.y.numel() * 2 + L.dx.numel() * 2 + L.dw.numel() * 4 for L in layers)
         link = link_bandwidth()
@@ -603,6 +633,10 @@ def gpu_arm(args, rank, world, dist):
         copies_ms = copy_only_step_ms(layers, streams, args.steps, max(1, args.warmup))
         e2e = {"value": round(e2e_value / 1e12, 2), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_per_step, 3),
+               "step_ms_stats": step_stats(e2e_ms),
+               "launch": "CUDA graph of the step's API calls, copies and events, replayed once per step",
+               "eager": {"value": round(eager_value / 1e12, 2), "ms_per_step": round(eager_ms_per_step, 3),
+                         "step_ms_stats": step_stats(eager_ms)},
                "link": link, "copy_bound_ms_per_step": round(bound_ms, 3),
                "copies_alone_ms_per_step": round(copies_ms, 3)}
         assert mx.device_status() == 0

@@ -59,7 +59,8 @@ def test_traffic_record_parser(tmp_path, monkeypatch):
 
 
 def test_step_stats_percentiles():
-    """The JSON line's step-time summary: median and nearest-rank 10th / 90th percentiles."""
+    """The JSON line's step-time summary: median, nearest-rank 10th / 90th percentiles and
+    the slowest step."""
     import importlib.util
 
     spec = importlib.util.spec_from_file_location("bench_stats_mod", os.path.join(ROOT, "bench.py"))
@@ -67,6 +68,6 @@ def test_step_stats_percentiles():
     spec.loader.exec_module(bench)
     ms = [1.50, 1.40, 1.60, 1.45, 1.55, 1.42, 1.48, 1.52, 1.58, 1.44, 1.46]
     st = bench.step_stats(ms)
-    assert st == {"median": 1.48, "p10": 1.42, "p90": 1.58}
+    assert st == {"median": 1.48, "p10": 1.42, "p90": 1.58, "max": 1.60}
     assert bench.step_stats([]) is None
-    assert bench.step_stats([2.0]) == {"median": 2.0, "p10": 2.0, "p90": 2.0}
+    assert bench.step_stats([2.0]) == {"median": 2.0, "p10": 2.0, "p90": 2.0, "max": 2.0}
