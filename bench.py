@@ -521,9 +521,15 @@ def gpu_arm(args, rank, world, dist):
             step_ev.append((a, b))
         torch.cuda.synchronize()
         barrier(dist)
-        for _ in range(args.steps):
-            flush()
-            run_step(layers, kern_ev, pair=pair, group=group)
+        gc_was_on = gc.isenabled()
+        gc.disable()  # a collector pause while launches are issued would count as kernel time
+        try:
+            for _ in range(args.steps):
+                flush()
+                run_step(layers, kern_ev, pair=pair, group=group)
+        finally:
+            if gc_was_on:
+                gc.enable()
         torch.cuda.synchronize()
     barrier(dist)
     status = mx.device_status()
