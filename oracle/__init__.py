@@ -96,6 +96,16 @@ def _p(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _check_rotation(had: int, mode: int | None = None) -> None:
+    """The oracle's rotation argument is the Hadamard block size (1: none, 16, 32), not
+    the library's 0 / 16 / 32; its scale rule is 0 (OCP floor) or 1 (ceiling).  Anything
+    else is refused here, before it reaches the C code."""
+    if had not in (1, 16, 32):
+        raise ValueError(f"oracle rotation block must be 1, 16 or 32 (got {had})")
+    if mode is not None and mode not in (0, 1):
+        raise ValueError(f"oracle scale rule must be 0 or 1 (got {mode})")
+
+
 def _u16(x) -> np.ndarray:
     x = np.ascontiguousarray(x)
     if x.dtype != np.uint16:
@@ -137,6 +147,7 @@ def hadamard_pm1(n: int) -> np.ndarray:
 
 def rotate_f32(x: np.ndarray, had: int) -> np.ndarray:
     """Canonical fp32 rotation of the last axis (blocks of ``had``)."""
+    _check_rotation(had)
     x = np.ascontiguousarray(x, dtype=np.float32)
     out = np.empty_like(x)
     flat_in, flat_out = x.reshape(-1), out.reshape(-1)
@@ -146,6 +157,7 @@ def rotate_f32(x: np.ndarray, had: int) -> np.ndarray:
 
 def rotate_f64(x: np.ndarray, had: int) -> np.ndarray:
     """Exact (fp64) rotation of the last axis by block-diagonal H_n / sqrt(n)."""
+    _check_rotation(had)
     x = np.ascontiguousarray(x, dtype=np.float64)
     out = np.empty_like(x)
     lib().oracle_rotate_f64(_p(x.reshape(-1)), x.size, had, _p(out.reshape(-1)))
@@ -160,6 +172,7 @@ def quantize(x_bf16: np.ndarray, had: int, mode: int, layout: str):
     layout 'colT' -> codes [C, R/2],  scales [C, R/32]   (rotation along R)
     layout '2d'   -> codes [R, C/2],  scales [R/32, C/32] (rotation along C)
     """
+    _check_rotation(had, mode)
     x = _u16(x_bf16)
     R, C = x.shape
     L = lib()
@@ -185,6 +198,7 @@ def quantize(x_bf16: np.ndarray, had: int, mode: int, layout: str):
 
 def quantize_vec(x_bf16: np.ndarray, had: int, mode: int):
     """Quantise one contiguous vector (length % 32 == 0) along itself."""
+    _check_rotation(had, mode)
     x = _u16(x_bf16).reshape(-1)
     n = x.size
     codes = np.zeros(n // 2, np.uint8)
@@ -280,6 +294,7 @@ def error_decomposition(x_bf16, had, mode):
     """Sums over a row-quantised [R, C] tensor of the three error components of the
     MXFP4 error ("Decomposing MXFP4 quantization error ...", core insight):
     dict with e2, scale2, dz2, grid2, scale_grid, n_deadzone, n (fp64 sums)."""
+    _check_rotation(had, mode)
     x = _u16(x_bf16)
     R, C = x.shape
     out = np.zeros(7, np.float64)
@@ -293,6 +308,7 @@ def rotation_divergence(x_bf16: np.ndarray, had: int, mode: int) -> dict:
     MXFP4 on Native FP4 Hardware", A.2, which defines the rotation exactly): among the
     32-blocks of the row layout of x [R, C], how many would get other codes or another
     E8M0 byte if the exact fp64 rotation were quantised instead.  Not a failure."""
+    _check_rotation(had, mode)
     x = _u16(x_bf16)
     R, C = x.shape
     out = np.zeros(3, np.int64)
@@ -316,6 +332,7 @@ def quantize_of(x_bf16: np.ndarray, had: int, mode: int, alpha_log2: int = -1):
     """Outlier fallback: q1 = Q(x), q2 = Q(x - dq(q1)) with alpha = 2^alpha_log2 folded
     into q2's scale bytes, so x_OF = dq(q1) + dq(q2).  Returns (c1, s1, c2, s2,
     number of residuals that were not exact in fp32)."""
+    _check_rotation(had, mode)
     x = _u16(x_bf16)
     R, C = x.shape
     c1 = np.zeros((R, C // 2), np.uint8)
@@ -332,6 +349,7 @@ def mbs_byte(amax: float) -> int:
 
 def quantize_mbs(x_bf16: np.ndarray, had: int, mode: int):
     """Macro-block scaling: returns (codes [R, C/2], scales [R, C/32], mbs [R, C/128])."""
+    _check_rotation(had, mode)
     x = _u16(x_bf16)
     R, C = x.shape
     assert C % 128 == 0
@@ -384,6 +402,7 @@ def pack_signs(neg: np.ndarray) -> np.ndarray:
 def quantize_rand(x_bf16: np.ndarray, had: int, mode: int, layout: str, signs=None, sr=None):
     """Like quantize() for 'row' ([R, C], signs over C, sr [R, C] uint16) and 'colT'
     ([C, R] output, signs over R, sr [C, R] uint16); signs is a bitmask (pack_signs)."""
+    _check_rotation(had, mode)
     x = _u16(x_bf16)
     R, C = x.shape
     sg = None if signs is None else np.ascontiguousarray(signs, np.uint8)

@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 from mxfp4_precision_gemms_gb300 import synth
-from tests.gpu_util import assert_within, gpu_ready
+from tests.gpu_util import ORACLE_HAD, assert_within, gpu_ready
 
 pytestmark = pytest.mark.gpu
 
@@ -155,3 +155,24 @@ def test_many_waves_both_tile_orders(torch, shape):
     want, S = oracle.gemm(*qa, *qb)
     assert_within(run(torch, qa, qb), want, S, what=f"{shape}")
     assert_within(run(torch, qa, qb, out_dtype=1), want, S, bf16=True, what=f"{shape} bf16")
+
+
+def _random_shapes(count, seed):
+    g = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        M = int(g.integers(1, 1400))
+        N = int(g.integers(1, 180)) * 8      # the output's row pitch is a multiple of 8
+        K = int(g.integers(1, 80)) * 32      # contraction in whole 32-element blocks
+        out.append((M, N, K, int(g.choice([0, 16, 32])), int(g.integers(0, 2)), int(g.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,had,mode,out_dtype", _random_shapes(24, 2026))
+def test_random_shapes(torch, M, N, K, had, mode, out_dtype):
+    """Seeded random shapes (ragged M, N and K in 32-element blocks; both kernels; every
+    rotation and scale rule; fp32 and bf16 out) against the oracle."""
+    qa, qb = oracle_operands(M, N, K, M + N + K, had=ORACLE_HAD[had], mode=mode)
+    want, S = oracle.gemm(*qa, *qb)
+    assert_within(run(torch, qa, qb, out_dtype=out_dtype), want, S, bf16=out_dtype == 1,
+                  what=f"{M}x{N}x{K} had={had} mode={mode} out={out_dtype}")

@@ -579,3 +579,19 @@ def test_rotation_divergence_on_workload_data(oracle_mod):
                 d = oracle_mod.rotation_divergence(a, had, mode)
                 print(f"rotation divergence {a.shape} H{had} mode {mode}: {d}")
                 assert d["blocks_differ"] <= max(1, d["blocks"] // 100000)
+
+
+def test_oracle_refuses_library_rotation_codes(oracle_mod):
+    """The oracle takes the Hadamard block size (1, 16, 32); the library's 0 for "no
+    rotation", or any other value, is refused before the C code runs, as is a scale rule
+    other than 0 or 1."""
+    x = synth.activations(32, 64, 1)
+    for bad in (0, 8, 64):
+        with pytest.raises(ValueError):
+            oracle_mod.quantize(x, bad, 0, "row")
+        with pytest.raises(ValueError):
+            oracle_mod.rotate_f32(np.zeros((1, 32), np.float32), bad)
+    with pytest.raises(ValueError):
+        oracle_mod.quantize(x, 16, 2, "row")
+    c, s = oracle_mod.quantize(x, 1, 0, "row")  # 1 = no rotation is accepted
+    assert c.shape == (32, 32) and s.shape == (32, 2)

@@ -217,3 +217,23 @@ def test_pair_launch_rejects_mismatched_columns(torch):
     b = mx.bf16_tensor(synth.activations(64, 512, 2))
     with pytest.raises(ValueError):
         mx.rotate_quantize_pair(a, b)
+
+
+def _random_quant_cases(count, seed):
+    g = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        R = int(g.integers(1, 60)) * 32      # rows in whole blocks (the transposed and 2D copies need it)
+        C = int(g.integers(1, 90)) * 32
+        lay = int(g.choice([1, 2, 3, 4]))
+        sf = 0 if lay == 4 else int(g.integers(0, 2))
+        out.append((R, C, int(g.choice([0, 16, 32])), int(g.integers(0, 2)), lay, sf))
+    return out
+
+
+@pytest.mark.parametrize("R,C,had,mode,layouts,sf", _random_quant_cases(24, 2027))
+def test_random_shapes_bit_exact(torch, R, C, had, mode, layouts, sf):
+    """Seeded random shapes, rotations, scale rules, layouts and scale orders: codes and
+    scale bytes bit-exact against the oracle."""
+    x = synth.heavy_tailed(R, C, R * 7 + C)
+    check(torch, x, had, mode, layouts, sf, f"{R}x{C} had={had} mode={mode} layouts={layouts} sf={sf}")
