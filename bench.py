@@ -46,13 +46,14 @@ def flops_per_step(linears=None):
 
 
 def step_stats(ms):
-    """Median, 10th / 90th percentiles and maximum of the timed steps' durations (ms)."""
+    """Median, 10th / 90th percentiles and maximum of the timed steps' durations (ms), and
+    the index of the slowest step."""
     v = sorted(ms)
     if not v:
         return None
     q = lambda f: v[min(len(v) - 1, int(round(f * (len(v) - 1))))]
     return {"median": round(statistics.median(v), 4), "p10": round(q(0.1), 4), "p90": round(q(0.9), 4),
-            "max": round(v[-1], 4)}
+            "max": round(v[-1], 4), "max_at": ms.index(v[-1])}
 
 
 def quant_bytes(R, C, dual):

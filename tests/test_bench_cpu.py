@@ -68,6 +68,6 @@ def test_step_stats_percentiles():
     spec.loader.exec_module(bench)
     ms = [1.50, 1.40, 1.60, 1.45, 1.55, 1.42, 1.48, 1.52, 1.58, 1.44, 1.46]
     st = bench.step_stats(ms)
-    assert st == {"median": 1.48, "p10": 1.42, "p90": 1.58, "max": 1.60}
+    assert st == {"median": 1.48, "p10": 1.42, "p90": 1.58, "max": 1.60, "max_at": 2}
     assert bench.step_stats([]) is None
-    assert bench.step_stats([2.0]) == {"median": 2.0, "p10": 2.0, "p90": 2.0, "max": 2.0}
+    assert bench.step_stats([2.0]) == {"median": 2.0, "p10": 2.0, "p90": 2.0, "max": 2.0, "max_at": 0}
