@@ -335,3 +335,23 @@ def test_gemm_mbs_rejects_bad_arguments(L):
     assert g(_tensor(cols=16512), _tensor(cols=16512)) == 2        # K above 16384
     assert g(_tensor(cols=256, had=16), _tensor(cols=256, had=32)) == 1
     assert g(_tensor(cols=256), _tensor(cols=256), ldc=100) == 3
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c", "c11"), ("c++", "c++11"), ("c++", "c++17")])
+def test_header_compiles_standalone(lang, std):
+    """include/mxfp4.h is a plain C ABI: it compiles on its own, without CUDA or torch
+    headers, as C and as C++, warning-free under -Wall -Wextra -pedantic (the translation
+    unit comes on standard input; nothing is written)."""
+    import os
+    import shutil
+    import subprocess
+
+    cc = "gcc" if lang == "c" else "g++"
+    if shutil.which(cc) is None:
+        pytest.skip(f"{cc} not found")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = '#include "mxfp4.h"\nint main(void) { return mxfp4_status_string(MXFP4_OK) == 0; }\n'
+    r = subprocess.run([cc, "-fsyntax-only", f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(root, "include"), "-x", lang, "-"], input=src, capture_output=True,
+                       text=True)
+    assert r.returncode == 0, r.stderr
